@@ -1,0 +1,108 @@
+"""FlexiCache side of the oracle (test infrastructure only; see oracle/__init__.py).
+
+Source: "FlexiCache: Leveraging Temporal Stability of Attention Heads for
+Efficient KV Cache Management (MLSys 2026)" (paper-review page):
+
+* "Core method / Sparse decode": every KV head attends only to its top-K
+  pages; page importance is the Quest-style min-max key bound, an upper bound
+  of max q.k over the page;
+* "Assumption 2": the per-page min/max vectors live in a MinMax cache kept on
+  the GPU, decoupled from the KV pages;
+* "System engineering / Block Allocator": one block table per (head, layer).
+
+Readings (also listed in the design doc):
+
+* the min/max vectors are elementwise over the valid keys of a page, in the
+  keys' own bf16 values (exact);
+* the bound of query j on page p is sum_d max(q_jd * mn_pd, q_jd * mx_pd); a
+  KV head's page score is the max of the bound over its g query heads;
+* the page score is taken in float32 in one fixed order, so that a GPU and
+  this oracle pick the same pages: d is cut into 16 equal slices, each slice
+  is summed left to right in float32, then the 16 partial sums are added
+  pairwise (j, j+8), then (j, j+4), (j, j+2), (j, j+1).  Every product of
+  two bf16 values is exact in float32, so only the additions round;
+* top-K keeps the K highest scores, ties to the lower page index, and lists
+  the pages in ascending order; no page is forced in;
+* sparse decode = exact attention over the tokens of the selected pages.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def page_minmax(K_row: np.ndarray, P: int):
+    """Elementwise min and max of the keys of each page: (mn, mx) [n_pages][d]."""
+    K_row = np.asarray(K_row, dtype=np.float32)
+    N, d = K_row.shape
+    n_pages = -(-N // P)
+    mn = np.empty((n_pages, d), dtype=np.float32)
+    mx = np.empty((n_pages, d), dtype=np.float32)
+    for p in range(n_pages):
+        page = K_row[p * P:min(N, (p + 1) * P)]
+        mn[p] = page.min(axis=0)
+        mx[p] = page.max(axis=0)
+    return mn, mx
+
+
+def quest_bound_f64(q: np.ndarray, mn: np.ndarray, mx: np.ndarray) -> np.ndarray:
+    """Quest bound of one query in float64: sum_d max(q_d mn_pd, q_d mx_pd) per page."""
+    q = np.asarray(q, dtype=np.float64)
+    return np.sum(np.maximum(q * np.asarray(mn, np.float64), q * np.asarray(mx, np.float64)), axis=1)
+
+
+def quest_bound_f32(q: np.ndarray, mn: np.ndarray, mx: np.ndarray) -> np.ndarray:
+    """Quest bound of one query in float32, summed in the fixed order of the module docstring."""
+    q = np.asarray(q, dtype=np.float32)
+    mn = np.asarray(mn, dtype=np.float32)
+    mx = np.asarray(mx, dtype=np.float32)
+    n_pages, d = mn.shape
+    if d % 16:
+        raise ValueError("d must be a multiple of 16")
+    e = np.maximum(q[None, :] * mn, q[None, :] * mx).astype(np.float32)   # exact products
+    w = d // 16
+    partial = np.zeros((16, n_pages), dtype=np.float32)
+    for j in range(16):
+        acc = np.zeros(n_pages, dtype=np.float32)
+        for t in range(w):
+            acc = (acc + e[:, j * w + t]).astype(np.float32)
+        partial[j] = acc
+    for half in (8, 4, 2, 1):
+        partial = (partial[:half] + partial[half:2 * half]).astype(np.float32)
+    return partial[0]
+
+
+def page_scores(q_heads: np.ndarray, mn: np.ndarray, mx: np.ndarray) -> np.ndarray:
+    """Score of every page for one KV head: max over its query heads of the float32 bound."""
+    return np.max(np.stack([quest_bound_f32(q, mn, mx) for q in np.asarray(q_heads)]), axis=0)
+
+
+def top_pages(score: np.ndarray, K: int) -> np.ndarray:
+    """The K best pages, ties to the lower page index, ascending."""
+    score = np.asarray(score, dtype=np.float32)
+    if np.isnan(score).any():
+        raise ValueError("NaN page score")
+    order = np.lexsort((np.arange(score.size), -score.astype(np.float64)))
+    return np.sort(order[:K])
+
+
+def select_pages(q_l, mn_l, mx_l, K: int) -> np.ndarray:
+    """Per-(request, KV head) top-K page ids of one layer: int [batch][H][K].
+
+    q_l [batch][H_q][d]; mn_l/mx_l [batch][H][n_pages][d].
+    """
+    q_l = np.asarray(q_l, dtype=np.float32)
+    batch, H_q, d = q_l.shape
+    H = np.asarray(mn_l).shape[1]
+    g = H_q // H
+    sel = np.empty((batch, H, K), dtype=np.int64)
+    for b in range(batch):
+        for h in range(H):
+            sc = page_scores(q_l[b, h * g:(h + 1) * g], mn_l[b, h], mx_l[b, h])
+            sel[b, h] = top_pages(sc, K)
+    return sel
+
+
+def page_tokens(pages: np.ndarray, P: int, N: int) -> np.ndarray:
+    """Token indices covered by a list of pages (ascending pages -> ascending tokens)."""
+    return np.concatenate([np.arange(p * P, min(N, (p + 1) * P)) for p in pages]) \
+        if len(pages) else np.zeros(0, dtype=np.int64)

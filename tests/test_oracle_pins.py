@@ -1,0 +1,503 @@
+"""Pins for the CPU oracle: each oracle function checked against something
+other than itself -- closed forms, brute force on tiny inputs, library
+routines for special cases, invariants.  A second group of tests plants a
+plausible mistake in the oracle and checks that some pin catches it.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import flexicache as fx
+from oracle import tangram as tg
+
+
+# ------------------------------------------------------------- budgets / n
+
+def pin_retained_count(fn=tg.retained_count):
+    # B = 1 keeps everything; B = 0.5 keeps ceil(N/2)
+    for N in (1, 2, 3, 16, 4095, 4096, 100000):
+        assert fn(1.0, N) == N
+        assert fn(0.5, N) == (N + 1) // 2
+    # float32(0.3) = 0.300000011920928955078125, so 0.3f * 1000 = 300.0000119... -> 301
+    assert fn(np.float32(0.3), 1000) == 301
+    # float32(0.25) is exact: 0.25 * 1000 = 250 -> 250
+    assert fn(np.float32(0.25), 1000) == 250
+    # an empty context keeps nothing; any positive budget keeps at least one token
+    assert fn(0.7, 0) == 0
+    assert fn(np.float32(1e-30), 5) == 1
+    # for N < 2^29 the float64 product B*N is exact, so ceil of it is the answer
+    r = np.random.default_rng(0)
+    for _ in range(2000):
+        B = np.float32(r.uniform(1e-4, 1.0))
+        N = int(r.integers(1, 1 << 20))
+        exact = float(B) * N
+        n = fn(B, N)
+        assert exact <= n < exact + 1 and 1 <= n <= N
+
+
+def pin_effective_budget(fn=tg.effective_budget):
+    b = fn(np.array([0.3, 0.6, 0.1, 2e-3], np.float32), 2.0)
+    assert b[0] == np.float32(0.6000000238418579)   # 2 * 0.3f (doubling is exact)
+    assert b[1] == 1.0                              # 1.2 clamped
+    b3 = fn(np.array([0.1], np.float32), 3.0)[0]
+    assert b3 == np.float32(3.0 * float(np.float32(0.1)))   # one rounding of the exact product
+    assert fn(np.array([0.4], np.float32), 1.0)[0] == np.float32(0.4)
+
+
+def test_retained_count():
+    pin_retained_count()
+
+
+def test_effective_budget():
+    pin_effective_budget()
+
+
+# ---------------------------------------------------------------- top(n, s)
+
+def brute_top(s, n):
+    """The unique subset of size n that beats every left-out index (score desc, index asc)."""
+    N = len(s)
+    found = []
+    for I in itertools.combinations(range(N), n):
+        out = [j for j in range(N) if j not in I]
+        if all(s[i] > s[j] or (s[i] == s[j] and i < j) for i in I for j in out):
+            found.append(list(I))
+    assert len(found) == 1
+    return found[0]
+
+
+def pin_top_indices(fn=tg.top_indices):
+    r = np.random.default_rng(1)
+    cases = [np.array([0.0, -0.0, 1.0, 1.0, -1.0, 0.0], np.float32),
+             np.array([2.0, 2.0, 2.0, 2.0], np.float32),
+             np.array([-0.0, 0.0, -0.0, 0.0, 5.0], np.float32)]
+    for _ in range(40):
+        N = int(r.integers(1, 10))
+        cases.append(r.choice(np.array([-1.0, 0.0, -0.0, 0.5, 1.0], np.float32), size=N))
+        cases.append(r.standard_normal(N).astype(np.float32))
+    for s in cases:
+        for n in range(0, len(s) + 1):
+            got = list(fn(s, n))
+            assert got == sorted(got)
+            assert got == (brute_top(list(s), n) if n else [])
+
+
+def test_top_indices():
+    pin_top_indices()
+
+
+def test_top_indices_nan_rejected():
+    with pytest.raises(ValueError):
+        tg.top_indices(np.array([1.0, np.nan], np.float32), 1)
+
+
+# ------------------------------------------------------------ ragged pages
+
+def _pages(L=3, batch=4, H=8, H_p=2, P=16, alpha=1.0, cluster=False, seed=0, N=None):
+    r = np.random.default_rng(seed)
+    Bhat = r.uniform(0.01, 1.0, size=(L, H)).astype(np.float32)
+    N = np.array(N if N is not None else r.integers(0, 300, size=batch), np.int32)
+    return tg.build_pages(L, batch, H, H_p, P, alpha, Bhat, N, cluster), Bhat, N
+
+
+def pin_build_pages(fn=tg.build_pages):
+    for cluster in (False, True):
+        for H_p in (1, 2, 4, 8):
+            r = np.random.default_rng(H_p)
+            L, batch, H, P = 3, 4, 8, 16
+            Bhat = r.uniform(0.01, 1.0, size=(L, H)).astype(np.float32)
+            N = np.array([0, 1, 37, 299], np.int32)
+            res = fn(L, batch, H, H_p, P, 1.0, Bhat, N, cluster)
+            G = H // H_p
+            ids = res["pt_ids"]
+            # ids: a permutation of 0..n_pages-1, handed out in (b, l, g, page) order
+            assert sorted(ids.tolist()) == list(range(res["n_pages"]))
+            seq = [ids[res["pt_off"][(l * batch + b) * G + g] + p]
+                   for b in range(batch) for l in range(L) for g in range(G)
+                   for p in range(res["pt_off"][(l * batch + b) * G + g + 1]
+                                  - res["pt_off"][(l * batch + b) * G + g])]
+            assert seq == list(range(res["n_pages"]))
+            for l in range(L):
+                order = list(res["order"][l])
+                assert sorted(order) == list(range(H))
+                for b in range(batch):
+                    for g in range(G):
+                        cnt = res["pt_off"][(l * batch + b) * G + g + 1] - res["pt_off"][(l * batch + b) * G + g]
+                        ns = [res["ntok"][l, b, h] for h in order[g * H_p:(g + 1) * H_p]]
+                        # a group's pages hold its longest head and nothing more
+                        assert cnt * P >= max(ns) and (cnt - 1) * P < max(ns) or (cnt == 0 and max(ns) == 0)
+                    # retained counts: Top size of section 3.1
+                    for h in range(H):
+                        assert res["ntok"][l, b, h] == math.ceil(Fraction(float(Bhat[l, h])) * int(N[b])) \
+                            if N[b] else res["ntok"][l, b, h] == 0
+                if cluster:
+                    Bl = [float(Bhat[l, h]) for h in order]
+                    assert Bl == sorted(Bl, reverse=True)
+                else:
+                    assert order == list(range(H))
+                # Phi: aggregate retained tokens of each group
+                for g in range(G):
+                    assert res["Phi"][l, g] == sum(res["ntok"][l, b, h] for b in range(batch)
+                                                   for h in order[g * H_p:(g + 1) * H_p])
+            # ragged paging never needs more bytes than one monolithic table
+            ragged_bytes = res["n_pages"] * H_p
+            mono_bytes = res["n_pages_monolithic"] * H
+            assert ragged_bytes <= mono_bytes
+            if H_p == H:
+                assert res["n_pages"] == res["n_pages_monolithic"]
+
+
+def test_build_pages():
+    pin_build_pages()
+
+
+def test_clustering_minimises_pages_over_all_partitions():
+    """Sorted chunking gives the fewest pages among all equal-size partitions (H=6, H_p=2,3)."""
+    r = np.random.default_rng(5)
+    H, P = 6, 16
+    for H_p in (2, 3):
+        for trial in range(6):
+            B = r.uniform(0.05, 1.0, size=H).astype(np.float32)
+            N = [int(x) for x in r.integers(1, 400, size=3)]
+            n = [[tg.retained_count(B[h], Nb) for h in range(H)] for Nb in N]
+            res = tg.build_pages(1, len(N), H, H_p, P, 1.0, B[None, :], np.array(N, np.int32), True)
+            best = None
+            for perm in itertools.permutations(range(H)):
+                pages = sum(-(-max(n[b][h] for h in perm[g * H_p:(g + 1) * H_p]) // P)
+                            for b in range(len(N)) for g in range(H // H_p))
+                best = pages if best is None else min(best, pages)
+            assert res["n_pages"] == best
+
+
+# --------------------------------------------------------------- split map
+
+def brute_split(Phi, N_CTA):
+    """Hamilton apportionment by search: minimise sum (a_i - q_i)^2 over a_i >= 0, sum a = R,
+    then the lexicographically largest minimiser (ties to the lower group)."""
+    G = len(Phi)
+    tot = sum(Phi) or G
+    Phi = Phi if sum(Phi) else [1] * G
+    R = N_CTA - G
+    q = [Fraction(R * x, tot) for x in Phi]
+    best, best_a = None, None
+    for a in itertools.product(range(R + 1), repeat=G):
+        if sum(a) != R:
+            continue
+        cost = sum((a[i] - q[i]) ** 2 for i in range(G))
+        if best is None or cost < best or (cost == best and a > best_a):
+            best, best_a = cost, a
+    return [1 + x for x in best_a]
+
+
+def pin_split_map(fn=tg.split_map_row):
+    r = np.random.default_rng(2)
+    cases = [([1, 1], 2), ([1, 1], 3), ([5, 5, 5], 7), ([0, 0, 0], 8), ([0, 9, 0, 1], 12),
+             ([3, 1], 12), ([7, 7, 1, 1], 11)]
+    for _ in range(60):
+        G = int(r.integers(1, 5))
+        cases.append((list(r.integers(0, 50, size=G)), int(r.integers(G, 13))))
+    for Phi, N_CTA in cases:
+        S = fn(Phi, N_CTA)
+        assert S == brute_split(list(Phi), N_CTA), (Phi, N_CTA, S)
+        assert sum(S) == N_CTA and min(S) >= 1
+        for i in range(len(Phi)):
+            for j in range(len(Phi)):
+                if Phi[i] < Phi[j]:
+                    assert S[i] <= S[j]
+
+
+def test_split_map():
+    pin_split_map()
+
+
+def test_split_map_rejects_too_few_ctas():
+    with pytest.raises(ValueError):
+        tg.split_map_row([1, 2, 3], 2)
+
+
+# --------------------------------------------------------------- work list
+
+def pin_work_list(fn=tg.work_list):
+    r = np.random.default_rng(3)
+    for trial in range(30):
+        batch, H, H_p = int(r.integers(1, 4)), 4, int(r.choice([1, 2, 4]))
+        G = H // H_p
+        ntok = r.integers(0, 60, size=(batch, H))
+        order = list(r.permutation(H))
+        N_CTA = int(r.integers(G, 3 * G + 9))
+        Phi = [sum(int(ntok[b, h]) for b in range(batch) for h in order[g * H_p:(g + 1) * H_p])
+               for g in range(G)]
+        S = tg.split_map_row(Phi, N_CTA)
+        ctas = fn(S, ntok, order, H_p)
+        assert len(ctas) == N_CTA
+        base = 0
+        for g in range(G):
+            # unit u of the group (b, head-in-group, token order) belongs to the CTA j with
+            # floor(j W / S) <= u < floor((j+1) W / S)
+            units = [(b, order[g * H_p + j], t) for b in range(batch) for j in range(H_p)
+                     for t in range(int(ntok[b, order[g * H_p + j]]))]
+            W = len(units)
+            owner = {}
+            for c in range(S[g]):
+                for (b, h, j, lst, t0, t1, nparts, part) in ctas[base + c]:
+                    assert lst == b * G + g and order[g * H_p + j] == h
+                    for t in range(t0, t1):
+                        assert (b, h, t) not in owner
+                        owner[(b, h, t)] = c
+            assert len(owner) == W
+            for u, key in enumerate(units):
+                j = max(c for c in range(S[g]) if c * W // S[g] <= u)
+                assert owner[key] == j
+            base += S[g]
+
+
+def test_work_list():
+    pin_work_list()
+
+
+# ------------------------------------------------------------- attention
+
+def _attn_inputs(r, n, d=16):
+    q = r.standard_normal(d)
+    K = r.standard_normal((n, d))
+    V = r.standard_normal((n, d))
+    return q, K, V
+
+
+def pin_attention(fn=tg.attention, partial=tg.attention_partial, merge=tg.merge_partials):
+    r = np.random.default_rng(4)
+    # library routines: scipy softmax and logsumexp
+    for n in (1, 2, 7, 50):
+        q, K, V = _attn_inputs(r, n)
+        scale = 0.37
+        out, lse = fn(q, K, V, scale)
+        z = scale * (K @ q)
+        np.testing.assert_allclose(out, scipy.special.softmax(z) @ V, rtol=1e-12, atol=1e-12)
+        assert abs(lse - scipy.special.logsumexp(z)) < 1e-12
+    # a single token returns its value row exactly
+    q, K, V = _attn_inputs(r, 1)
+    out, lse = fn(q, K, V, 0.5)
+    assert np.array_equal(out, V[0]) and lse == pytest.approx(0.5 * float(K[0] @ q), abs=1e-12)
+    # identical keys: the mean of V, and lse = z + ln n
+    q, K, V = _attn_inputs(r, 9)
+    K[:] = K[0]
+    out, lse = fn(q, K, V, 1.0)
+    np.testing.assert_allclose(out, V.mean(axis=0), rtol=1e-12, atol=1e-13)
+    assert lse == pytest.approx(float(K[0] @ q) + math.log(9), abs=1e-12)
+    # the token order does not matter
+    q, K, V = _attn_inputs(r, 33)
+    p = r.permutation(33)
+    np.testing.assert_allclose(fn(q, K, V, 0.2)[0], fn(q, K[p], V[p], 0.2)[0], rtol=1e-12, atol=1e-14)
+    # split-KV: merging the partials of any split equals the unsplit result
+    for _ in range(10):
+        q, K, V = _attn_inputs(r, 40)
+        cuts = sorted(set(r.integers(1, 40, size=3).tolist()))
+        bounds = [0] + cuts + [40]
+        parts = [partial(q, K[a:b], V[a:b], 0.3) for a, b in zip(bounds, bounds[1:])]
+        o_m, lse_m = merge(parts)
+        o_u, lse_u = fn(q, K, V, 0.3)
+        np.testing.assert_allclose(o_m, o_u, rtol=1e-12, atol=1e-14)
+        assert lse_m == pytest.approx(lse_u, abs=1e-12)
+
+
+def test_attention():
+    pin_attention()
+
+
+def test_attention_empty():
+    out, lse = tg.attention(np.ones(4), np.zeros((0, 4)), np.zeros((0, 4)), 1.0)
+    assert np.array_equal(out, np.zeros(4)) and lse == -math.inf
+
+
+def test_full_budget_is_dense_attention():
+    """B = 1 retains every token: ragged decode equals torch's dense SDPA (float64)."""
+    r = np.random.default_rng(6)
+    batch, H_q, H, N, d = 2, 8, 2, 45, 32
+    q = r.standard_normal((batch, H_q, d))
+    K = r.standard_normal((batch, H, N, d))
+    V = r.standard_normal((batch, H, N, d))
+    s = r.standard_normal((batch, H, N)).astype(np.float32)
+    ntok = np.array([[tg.retained_count(1.0, N)] * H] * batch)
+    idx = tg.retained_sets(s, ntok, [N] * batch)
+    scale = 1 / math.sqrt(d)
+    out, _ = tg.decode_layer(q, K, V, idx, scale)
+    g = H_q // H
+    Kq = torch.from_numpy(K).repeat_interleave(g, dim=1)
+    Vq = torch.from_numpy(V).repeat_interleave(g, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, :, None, :], Kq, Vq, scale=scale)[:, :, 0, :]
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------------------------------------------- Quest
+
+def pin_page_minmax(fn=fx.page_minmax):
+    r = np.random.default_rng(7)
+    for N in (16, 40, 1):
+        K = r.standard_normal((N, 8)).astype(np.float32)
+        mn, mx = fn(K, 16)
+        assert mn.shape[0] == -(-N // 16)
+        for p in range(mn.shape[0]):
+            page = K[p * 16:(p + 1) * 16]
+            assert (page >= mn[p]).all() and (page <= mx[p]).all()
+            for c in range(8):
+                assert mn[p, c] in page[:, c] and mx[p, c] in page[:, c]
+
+
+def pin_quest_bound(f32=fx.quest_bound_f32):
+    r = np.random.default_rng(8)
+    d, P = 128, 16
+    for _ in range(20):
+        K = r.standard_normal((5 * P, d)).astype(np.float32)
+        q = r.standard_normal(d).astype(np.float32)
+        mn, mx = fx.page_minmax(K, P)
+        b64 = fx.quest_bound_f64(q, mn, mx)
+        b32 = f32(q, mn, mx).astype(np.float64)
+        # the bound dominates every q.k of the page (float64)
+        for p in range(5):
+            assert b64[p] >= (K[p * P:(p + 1) * P].astype(np.float64) @ q.astype(np.float64)).max() - 1e-9
+        # float32 sum within the classic recursive-summation bound of the exact value
+        e = np.maximum(q * mn, q * mx).astype(np.float64)
+        bound = (d * np.finfo(np.float32).eps) * np.abs(e).sum(axis=1)
+        assert (np.abs(b32 - b64) <= bound).all()
+    # one key per page: mn = mx = k, bound = q.k
+    k = r.standard_normal((3, d)).astype(np.float32)
+    q = r.standard_normal(d).astype(np.float32)
+    np.testing.assert_allclose(f32(q, k, k), k.astype(np.float64) @ q.astype(np.float64), rtol=1e-5, atol=1e-5)
+    # the fixed float32 order: slices of d/16 summed left to right, then pairs (j, j+8), (j, j+4), ...
+    # slice 0 = [1, 2^-24, ...]: left to right each 2^-24 rounds away (ties to even) -> 1
+    # partials p0 = 1, p1 = p8 = p9 = 2^-24: (p0+p8) = 1, (p1+p9) = 2^-23, total 1 + 2^-23
+    tiny = np.float32(2.0 ** -24)
+    e = np.zeros(d, np.float32)
+    w = d // 16
+    e[0] = 1.0
+    e[1] = tiny
+    e[1 * w] = tiny
+    e[8 * w] = tiny
+    e[9 * w] = tiny
+    ones = np.ones(d, np.float32)
+    got = f32(ones, e[None, :], e[None, :])[0]
+    assert got == np.float32(1.0) + np.float32(2.0 ** -23)
+    # and a slice summed left to right: [2^-24, 2^-24, 1, ...] -> 2^-23 + 1 exactly
+    e = np.zeros(d, np.float32)
+    e[0] = tiny
+    e[1] = tiny
+    e[2] = 1.0
+    assert f32(ones, e[None, :], e[None, :])[0] == np.float32(1.0) + np.float32(2.0 ** -23)
+
+
+def pin_top_pages(fn=fx.top_pages):
+    r = np.random.default_rng(9)
+    for _ in range(40):
+        n = int(r.integers(1, 10))
+        sc = r.choice(np.array([0.0, -0.0, 1.0, 2.5, -3.0], np.float32), size=n)
+        for K in range(0, n + 1):
+            got = list(fn(sc, K))
+            assert got == (brute_top(list(sc), K) if K else [])
+
+
+def test_page_minmax():
+    pin_page_minmax()
+
+
+def test_quest_bound():
+    pin_quest_bound()
+
+
+def test_top_pages():
+    pin_top_pages()
+
+
+def test_all_pages_is_dense():
+    """K = n_pages selects every page, so sparse decode equals dense attention."""
+    r = np.random.default_rng(10)
+    N, P, d, g = 64, 16, 32, 2
+    K = r.standard_normal((N, d)).astype(np.float32)
+    V = r.standard_normal((N, d))
+    qh = r.standard_normal((g, d)).astype(np.float32)
+    mn, mx = fx.page_minmax(K, P)
+    sel = fx.top_pages(fx.page_scores(qh, mn, mx), N // P)
+    assert list(sel) == list(range(N // P))
+    tok = fx.page_tokens(sel, P, N)
+    for j in range(g):
+        o1, _ = tg.attention(qh[j], K[tok], V[tok], 0.1)
+        o2 = scipy.special.softmax(0.1 * (K.astype(np.float64) @ qh[j].astype(np.float64))) @ V
+        np.testing.assert_allclose(o1, o2, rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------- planted mistakes are caught
+
+def _wrong_ceil(B, N):
+    return 0 if N <= 0 else max(1, min(N, round(float(np.float32(B)) * N)))
+
+
+def _ties_high(s, n):
+    s = np.asarray(s, np.float32)
+    idx = np.arange(s.size)
+    order = np.lexsort((-idx, -s.astype(np.float64)))
+    return np.sort(order[:n])
+
+
+def _split_ties_high(Phi, N_CTA):
+    Phi = [int(x) for x in Phi]
+    G = len(Phi)
+    if sum(Phi) == 0:
+        Phi = [1] * G
+    R, tot = N_CTA - G, sum(Phi)
+    fl = [R * x // tot for x in Phi]
+    rem = [R * x % tot for x in Phi]
+    bonus = [0] * G
+    for i in sorted(range(G), key=lambda i: (-rem[i], -i))[:R - sum(fl)]:
+        bonus[i] = 1
+    return [1 + fl[i] + bonus[i] for i in range(G)]
+
+
+def _attn_sign(q, K, V, scale):
+    return tg.attention(q, K, V, -scale)
+
+
+def _attn_no_max(q, K, V, scale):
+    m, l, o = tg.attention_partial(q, K, V, scale)
+    return o / l, m   # drops the log-sum term of the LSE
+
+
+def _quest_min(q, mn, mx):
+    return fx.quest_bound_f32(q, mn, mn)
+
+
+def _quest_flat(q, mn, mx):
+    e = np.maximum(q[None, :] * mn, q[None, :] * mx).astype(np.float32)
+    acc = np.zeros(mn.shape[0], np.float32)
+    for t in range(mn.shape[1]):
+        acc = (acc + e[:, t]).astype(np.float32)
+    return acc
+
+
+def _work_list_off_by_one(S_row, ntok_l, order_l, H_p):
+    ctas = tg.work_list(S_row, ntok_l, order_l, H_p)
+    for items in ctas:
+        for it in items:
+            if it[5] > it[4] + 1:
+                it[5] -= 1
+    return ctas
+
+
+@pytest.mark.parametrize("pin,mutant", [
+    (pin_retained_count, _wrong_ceil),
+    (pin_top_indices, _ties_high),
+    (pin_split_map, _split_ties_high),
+    (pin_attention, _attn_sign),
+    (pin_attention, _attn_no_max),
+    (pin_quest_bound, _quest_min),
+    (pin_quest_bound, _quest_flat),
+    (pin_top_pages, _ties_high),
+    (pin_work_list, _work_list_off_by_one),
+])
+def test_planted_mistake_is_caught(pin, mutant):
+    with pytest.raises(AssertionError):
+        pin(mutant)
