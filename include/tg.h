@@ -1,0 +1,261 @@
+/*
+ * tg.h -- C ABI of the GB300 ragged paged decode-attention library.
+ *
+ * Decode attention over a head-wise non-uniform ("ragged") KV cache, after
+ *   [Tangram] "Tangram: Unlocking Non-Uniform KV Cache Compression for
+ *             Efficient Multi-turn LLM Serving" (paper-review page), section 3
+ *             (3.1 Budget Reservation, 3.2 Ragged Paging, 3.3 AOT Load Balancing);
+ * and Quest-style page scoring with per-KV-head top-K pages, after
+ *   [FlexiCache] "FlexiCache: Leveraging Temporal Stability of Attention Heads
+ *             for Efficient KV Cache Management (MLSys 2026)" (paper-review page),
+ *             "Core method / Sparse decode" and "Assumption 2".
+ *
+ * Conventions
+ *  - Every function returns TG_OK (0) or a negative TG_ERR_* code; the
+ *    calling thread's tg_last_error_string() then says why.  No C++ exception
+ *    crosses this boundary.
+ *  - The caller owns every buffer.  "host" pointers are ordinary CPU memory,
+ *    "device" pointers are CUDA device memory of the current device.  Nothing
+ *    is allocated on the caller's behalf; sizes are queried first (size
+ *    outputs, or NULL data outputs).
+ *  - GPU entry points take a CUDA stream (cudaStream_t; NULL = legacy default
+ *    stream), validate their arguments on the host and return synchronously,
+ *    then run asynchronously on that stream.  Faults that only the device can
+ *    see (a page id past the pool, a NaN score, a wait that gave up) set bits
+ *    of the caller's int32 device status word (TG_STATUS_*), which
+ *    tg_check_status() reads back.  No kernel traps.
+ *  - Tensors are dense row-major.  bf16 values travel as uint16_t bit patterns.
+ *
+ * Notation: L layers, batch requests, H KV heads, H_q query heads, g = H_q/H
+ * (query head j reads KV head j/g), d head dim, P tokens per page, H_p heads
+ * per page group, G = H/H_p groups, N_b context length of request b,
+ * n_{l,b,h} = ceil(B_{l,h} * N_b) retained tokens of a head.
+ */
+#ifndef TG_H
+#define TG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *tg_stream_t;   /* same type as cudaStream_t */
+
+enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = -1, /* a NULL pointer, a non-positive size, a bad flag   */
+  TG_ERR_SHAPE = -2,       /* sizes that do not fit together (H % H_p, d, g...) */
+  TG_ERR_NONFINITE = -3,   /* NaN/Inf in a host input that must be finite       */
+  TG_ERR_CAPACITY = -4,    /* an output buffer is too small                     */
+  TG_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed                 */
+  TG_ERR_TIMEOUT = -6,     /* reported by tg_check_status for TG_STATUS_TIMEOUT */
+  TG_ERR_DEVICE = -7       /* reported by tg_check_status for other status bits */
+};
+
+/* Bits of the device status word. */
+#define TG_STATUS_NONFINITE 0x1 /* a NaN score reached a top-k selection            */
+#define TG_STATUS_BAD_PAGE 0x2  /* a page id outside [0, pool_pages)                */
+#define TG_STATUS_TIMEOUT 0x4   /* a copy wait gave up (about 2 s); outputs invalid */
+#define TG_STATUS_BAD_INPUT 0x8 /* a device-side size outside its limits            */
+
+/* Reason for the last non-zero return on the calling thread ("" if none). */
+const char *tg_last_error_string(void);
+
+/* Library version: 10000 * major + 100 * minor + patch. */
+int tg_version(void);
+
+/* ------------------------------------------------------------------ a1 ---
+ * tg_build_pages -- ragged page tables with budget-aware head clustering.
+ *   [Tangram] 3.1: B = min(1, alpha * B^) with safety coefficient alpha;
+ *   n = ceil(B * N_b), the size of Top(ceil(B N), s).  3.2: H_p-head groups,
+ *   one page table per group, a page holds H_p x 2 x P x d elements, a group
+ *   gets ceil(max_{h in group} n / P) pages; budget-aware clustering puts heads
+ *   of similar retention in one group.  3.3: Phi = aggregate budget of a group.
+ * Readings: B is float32; n is the exact ceiling of that float32 times N_b,
+ *   clamped to [1, N_b] (0 when N_b = 0).  cluster != 0 sorts each layer's
+ *   heads by (B descending, head ascending) and cuts the order into chunks of
+ *   H_p; cluster == 0 keeps heads i*H_p .. i*H_p+H_p-1 in group i.  Page ids
+ *   are numbered from 0 in (request, layer, group, page) order.
+ * Inputs (host): Bhat float32 [L][H], each > 0 and finite; N int32 [batch],
+ *   each >= 0; alpha > 0; H % H_p == 0; P % 16 == 0.
+ * Outputs (host, each may be NULL):
+ *   head_order int32 [L][H]  group i holds head_order[l][i*H_p + j], j < H_p
+ *   ntok       int32 [L][batch][H]
+ *   Phi        int64 [L][G]  sum of ntok over the requests and heads of a group
+ *   pt_off     int64 [L*batch*G + 1]  CSR offsets; list (l, b, g) is index (l*batch + b)*G + g
+ *   pt_ids     int32 [pt_cap]  page ids; TG_ERR_CAPACITY if pt_cap < *n_pages
+ *   n_pages             total ragged pages
+ *   n_pages_monolithic  pages (of H x 2 x P x d elements) one shared table would need
+ * Pool layout implied: pool bf16 [n_pages][H_p][2][P][d]; retained token k of the
+ *   head at group position j sits in page pt_ids[pt_off[list] + k/P], row k%P of
+ *   block [j][0] (K) and [j][1] (V).
+ */
+int tg_build_pages(int L, int batch, int H, int H_p, int P, float alpha,
+                   const float *Bhat, const int32_t *N, int cluster,
+                   int32_t *head_order, int32_t *ntok, int64_t *Phi,
+                   int64_t *pt_off, int32_t *pt_ids, int64_t pt_cap,
+                   int64_t *n_pages, int64_t *n_pages_monolithic);
+
+/* ------------------------------------------------------------------ a3 ---
+ * tg_split_map -- the static Workload Split Map S in N^{L x G}.
+ *   [Tangram] 3.3 (Algorithm 1): CTAs are given to each head group in
+ *   proportion to its aggregate budget Phi_{l,i}; larger groups get more CTAs.
+ * Reading: per layer row, every group gets 1 CTA, then R = N_CTA - G more by
+ *   largest remainder of R*Phi_i/sum(Phi), ties to the lower group index; a
+ *   row of zeros counts as equal Phi.  Each row sums to N_CTA.
+ * Inputs (host): Phi int64 [L][G], each >= 0; N_CTA >= G.
+ * Output (host): S int32 [L][G].
+ */
+int tg_split_map(int L, int G, int N_CTA, const int64_t *Phi, int32_t *S);
+
+/* tg_query_ncta -- occupancy-derived N_CTA for tg_decode_attn on the current
+ *   device: resident CTAs per SM of the kernel chosen for (d, g) times the SM
+ *   count ([Tangram] 3.3, N_CTA from the CUDA max-occupancy query).
+ *   d in {128, 256}, 1 <= g <= 8.  Output (host): *N_CTA. */
+int tg_query_ncta(int d, int g, int *N_CTA);
+
+/* ------------------------------------------------------------------ a4 ---
+ * Decode plan: the split map turned into per-CTA work ([Tangram] 3.3: each
+ * group's CTAs share its work evenly).  Inside group i of layer l the retained
+ * tokens are laid end to end in (request, head-in-group, token) order, W =
+ * Phi_{l,i} units; CTA j of the group's S_{l,i} CTAs takes units
+ * [floor(j W / S), floor((j+1) W / S)).  Each piece of one head's run is one
+ * tg_work_item.  A plan is a single self-describing byte buffer:
+ *   tg_plan_header | tg_plan_layer[L] | per layer: int32 cta_off[N_CTA+1], tg_work_item[]
+ * (every section 16-byte aligned; offsets are in bytes from the buffer start). */
+#define TG_PLAN_MAGIC 0x31504754u /* "TGP1" */
+
+typedef struct tg_plan_header {
+  uint32_t magic;
+  int32_t version;
+  int32_t L, batch, H, H_q, H_p, P, d, G, N_CTA;
+  int32_t max_slots;       /* most partial slots any layer uses */
+  int64_t plan_bytes;      /* size of the whole buffer */
+  int64_t workspace_bytes; /* device workspace tg_decode_attn needs */
+  int64_t layers;          /* byte offset of tg_plan_layer[L] */
+} tg_plan_header;
+
+typedef struct tg_plan_layer {
+  int64_t cta_off; /* byte offset of int32 [N_CTA + 1]: items of CTA c are [cta_off[c], cta_off[c+1]) */
+  int64_t items;   /* byte offset of tg_work_item [n_items] */
+  int32_t n_items;
+  int32_t n_slots; /* partial slots of this layer */
+} tg_plan_layer;
+
+typedef struct tg_work_item {
+  int32_t b, h;    /* request, KV head */
+  int32_t hpos, g; /* position of h in its group, group index */
+  int32_t t0, t1;  /* retained-token range [t0, t1) of (b, h); t0 == t1 only for an empty head */
+  int32_t slot0;   /* first partial slot of the run of (b, h) (when nparts > 1) */
+  int32_t part;    /* this CTA's piece of the run, 0 .. nparts-1 */
+  int32_t nparts;  /* CTAs that share the run; 1 = this CTA finishes it alone */
+  int32_t reserved[3];
+} tg_work_item;
+
+/* tg_plan_decode -- build the plan for all L layers.
+ * Inputs (host): S int32 [L][G] (tg_split_map), head_order int32 [L][H] and
+ *   ntok int32 [L][batch][H] (tg_build_pages).  N_CTA = each row's sum.
+ *   d in {128, 256}; g = H_q / H in [1, 8]; P % 16 == 0.
+ * Outputs (host): plan (NULL to query the size) of plan_cap bytes;
+ *   *plan_bytes; *workspace_bytes = device scratch tg_decode_attn needs.
+ *   TG_ERR_CAPACITY if plan_cap < *plan_bytes. */
+int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, int d, int N_CTA,
+                   const int32_t *S, const int32_t *head_order, const int32_t *ntok,
+                   void *plan, int64_t plan_cap, int64_t *plan_bytes, int64_t *workspace_bytes);
+
+/* ------------------------------------------------------------- a5 + a6 ---
+ * tg_decode_attn -- split-KV flash decoding of one layer over the ragged pool,
+ *   with the log-sum-exp merge fused in (the last CTA of a shared run merges).
+ *   [Tangram] 3.3: one launch of N_CTA CTAs per layer under the static split
+ *   map, no re-planning.  [FlexiCache] "Sparse decode": the same kernel runs
+ *   over a per-head list of selected pages (H_p = 1 tables).
+ *   For query head j = h*g + i of request b:
+ *     out = sum_t softmax_t(scale * q . k_t) v_t over the retained tokens t of (b, h),
+ *     lse = ln sum_t exp(scale * q . k_t)     (out = 0, lse = -inf for an empty head).
+ *   bf16 inputs, float32 accumulation, bf16 output.
+ * Arguments:
+ *   plan_host / plan_dev  the same tg_plan_decode bytes in host and device memory
+ *   layer                 which plan layer to run (0 <= layer < L)
+ *   q     device bf16 [batch][H_q][d]
+ *   pool  device bf16 [pool_pages][H_p][2][P][d]; 16-byte aligned.  Rows of a
+ *         head's last page past its ntok must hold finite values
+ *         (tg_compact_topk writes zeros there).
+ *   pt_off device int64: the page-table offsets of THIS layer's lists,
+ *         batch*G + 1 entries, list b*G + g; values index pt_ids
+ *   pt_ids device int32 page ids
+ *   scale  softmax scale (1/sqrt(d) for standard attention)
+ *   workspace device, workspace_bytes >= the plan's; zero-filled before the
+ *         first call.  The kernel returns its counters to zero, so one buffer
+ *         serves every later call on the same stream; concurrent calls must
+ *         use separate workspaces.  After a TG_STATUS_TIMEOUT, zero it again.
+ *   out   device bf16 [batch][H_q][d];  lse device float32 [batch][H_q] (may be NULL)
+ *   dev_status device int32, OR-ed with TG_STATUS_* (may be NULL)
+ *   cta_time device int64 [2*N_CTA] (may be NULL): %globaltimer ns at each
+ *         CTA's start and end, for CTA skew = max/mean of (end - start). */
+int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
+                   const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
+                   const int64_t *pt_off, const int32_t *pt_ids, float scale,
+                   void *workspace, int64_t workspace_bytes,
+                   uint16_t *out, float *lse, int32_t *dev_status, int64_t *cta_time);
+
+/* ------------------------------------------------------------------ a2 ---
+ * tg_compact_topk -- retain Top(n, s) of every head of one layer and write the
+ *   retained K/V rows into the group pages.
+ *   [Tangram] 3.1: I_{l,h} = Top(ceil(B_{l,h} N), s_{l,h}); 3.2: per-group pages.
+ * Reading: ties go to the lower token index, -0.0 == +0.0; retained tokens
+ *   are stored in ascending token order (token I[k] -> page k/P, row k%P).
+ *   The rows of a head's last page past n are zero-filled.  A NaN score sets
+ *   TG_STATUS_NONFINITE (the selection of that row is then unspecified).
+ * Arguments (device unless stated):
+ *   N int32 [batch] with N_b <= Nmax; scores float32 [batch][H][Nmax];
+ *   K, V bf16 [batch][H][Nmax][d]; head_order int32 [H] and ntok int32 [batch][H]
+ *   of this layer; pt_off int64 [batch*G + 1] of this layer's lists; pt_ids int32;
+ *   pool bf16 [pool_pages][H_p][2][P][d] (output, 16-byte aligned);
+ *   kept_idx int32 [batch][H][Nmax] (output, may be NULL): row (b, h) starts with
+ *   the n retained token indices, ascending; dev_status may be NULL.
+ *   Host sizes: d % 8 == 0, d <= 512, P % 16 == 0, Nmax >= 1. */
+int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int Nmax,
+                    const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
+                    const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
+                    const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool,
+                    int32_t *kept_idx, int32_t *dev_status);
+
+/* ------------------------------------------------------------------ a9 ---
+ * tg_build_minmax -- per-page elementwise min and max of the keys (the MinMax
+ *   cache of [FlexiCache] "Assumption 2"), exact in bf16.
+ *   K device bf16 [batch][H][N][d]; minmax device bf16 [batch][H][ceil(N/P)][2][d]
+ *   (row 0 = min, row 1 = max over the page's valid keys). */
+int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d,
+                    const uint16_t *K, uint16_t *minmax, int32_t *dev_status);
+
+/* ------------------------------------------------------------------ a7 ---
+ * tg_page_score_topk -- Quest page bound and per-KV-head top-K pages.
+ *   [FlexiCache] "Core method / Sparse decode": every KV head attends only to
+ *   its top-K pages, ranked by the min-max key bound of max q.k.
+ *   score(b,h,p) = max over the g query heads j of sum_d max(q_jd mn_pd, q_jd mx_pd).
+ * Reading: float32 arithmetic in one fixed order (d cut into 16 slices summed
+ *   left to right, then partial sums added pairwise (j, j+8), (j, j+4), (j, j+2),
+ *   (j, j+1)); ties to the lower page; output ascending.  NaN -> TG_STATUS_NONFINITE.
+ * Arguments (device): q bf16 [batch][H*g][d]; minmax bf16 [batch][H][n_pages][2][d];
+ *   sel int32 [batch][H][K] (output, page indices 0..n_pages-1);
+ *   pt_ids int32 [batch][H][K] (output, may be NULL): (b*H + h)*n_pages + sel,
+ *   i.e. the ids of the selected pages in a dense pool [batch][H][n_pages] of
+ *   H_p = 1 pages, ready as the page lists of tg_decode_attn.
+ *   Host sizes: d in {128, 256}, 1 <= g <= 8, 1 <= K <= n_pages <= 16384. */
+int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
+                       const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
+                       int32_t *dev_status);
+
+/* tg_check_status -- synchronously read a device status word (waits for the
+ *   device).  Returns TG_OK when it is 0, TG_ERR_TIMEOUT when TG_STATUS_TIMEOUT
+ *   is set, TG_ERR_DEVICE for any other bit; *host_status (may be NULL) gets
+ *   the raw bits. */
+int tg_check_status(const int32_t *dev_status, int32_t *host_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TG_H */

@@ -1,0 +1,250 @@
+"""Python binding of libtg, the GB300 ragged paged decode-attention library.
+
+Argument marshalling only: every function below has the name of the C entry
+point it calls (include/tg.h), turns numpy arrays / torch tensors into
+pointers, allocates host-side outputs of the planning calls, and raises
+``TGError`` when the C call returns an error.  All device work runs in the
+library's CUDA kernels; nothing here computes a result itself.  There is no
+fallback: if libtg.so cannot be built or loaded, the import of a function
+fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from . import _build
+
+__all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
+           "tg_decode_attn", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
+           "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
+           "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
+
+STATUS_NONFINITE, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_INPUT = 0x1, 0x2, 0x4, 0x8
+PLAN_MAGIC = 0x31504754
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_F = ctypes.c_float
+
+_SIGS = {
+    "tg_last_error_string": (ctypes.c_char_p, []),
+    "tg_version": (_I, []),
+    "tg_build_pages": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _P, _P, _L, _P, _P]),
+    "tg_split_map": (_I, [_I, _I, _I, _P, _P]),
+    "tg_query_ncta": (_I, [_I, _I, _P]),
+    "tg_plan_decode": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P]),
+    "tg_decode_attn": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _L, _P, _P, _P, _P]),
+    "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]),
+    "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_check_status": (_I, [_P, _P]),
+}
+
+
+class TGError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def load(build: bool = True) -> ctypes.CDLL:
+    """Load libtg.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        if build:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libtg.so is missing at {_build.LIB}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise TGError(rc, _lib.tg_last_error_string().decode())
+
+
+def _np(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+def _dev(t, dtype=None, name="tensor"):
+    """Pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def tg_version() -> int:
+    return load().tg_version()
+
+
+# ------------------------------------------------------------------ host planning
+
+def tg_build_pages(L, batch, H, H_p, P, alpha, Bhat, N, cluster) -> dict:
+    """Ragged page tables (tg.h: tg_build_pages).  Returns numpy arrays."""
+    lib = load()
+    G = H // H_p if H_p else 0
+    Bhat, pB = _np(np.asarray(Bhat).reshape(L, H), np.float32)
+    N, pN = _np(np.asarray(N).reshape(batch), np.int32)
+    order = np.zeros((L, H), np.int32)
+    ntok = np.zeros((L, batch, H), np.int32)
+    Phi = np.zeros((L, max(G, 1)), np.int64)
+    pt_off = np.zeros(L * batch * max(G, 1) + 1, np.int64)
+    n_pages, n_mono = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.tg_build_pages(L, batch, H, H_p, P, float(alpha), pB, pN, int(bool(cluster)),
+                              order.ctypes.data, ntok.ctypes.data, Phi.ctypes.data, pt_off.ctypes.data,
+                              None, 0, ctypes.addressof(n_pages), ctypes.addressof(n_mono)))
+    pt_ids = np.zeros(max(n_pages.value, 1), np.int32)
+    _check(lib.tg_build_pages(L, batch, H, H_p, P, float(alpha), pB, pN, int(bool(cluster)),
+                              None, None, None, None, pt_ids.ctypes.data, pt_ids.size,
+                              None, None))
+    return dict(order=order, ntok=ntok, Phi=Phi, pt_off=pt_off, pt_ids=pt_ids[:n_pages.value],
+                n_pages=n_pages.value, n_pages_monolithic=n_mono.value)
+
+
+def tg_split_map(Phi, N_CTA: int) -> np.ndarray:
+    """Workload Split Map (tg.h: tg_split_map).  Phi int64 [L][G] -> S int32 [L][G]."""
+    lib = load()
+    Phi, pP = _np(np.atleast_2d(Phi), np.int64)
+    S = np.zeros(Phi.shape, np.int32)
+    _check(lib.tg_split_map(Phi.shape[0], Phi.shape[1], int(N_CTA), pP, S.ctypes.data))
+    return S
+
+
+def tg_query_ncta(d: int, g: int) -> int:
+    lib = load()
+    n = ctypes.c_int(0)
+    _check(lib.tg_query_ncta(int(d), int(g), ctypes.addressof(n)))
+    return n.value
+
+
+def tg_plan_decode(S, head_order, ntok, H_q: int, H_p: int, P: int, d: int):
+    """Decode plan for all layers (tg.h: tg_plan_decode) -> (plan uint8 array, workspace bytes)."""
+    lib = load()
+    S, pS = _np(S, np.int32)
+    head_order, pO = _np(head_order, np.int32)
+    ntok, pT = _np(ntok, np.int32)
+    L, batch, H = ntok.shape
+    N_CTA = int(S[0].sum())
+    nbytes, wbytes = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.tg_plan_decode(L, batch, H, H_q, H_p, P, d, N_CTA, pS, pO, pT, None, 0,
+                              ctypes.addressof(nbytes), ctypes.addressof(wbytes)))
+    plan = np.zeros(nbytes.value, np.uint8)
+    _check(lib.tg_plan_decode(L, batch, H, H_q, H_p, P, d, N_CTA, pS, pO, pT, plan.ctypes.data, plan.size,
+                              ctypes.addressof(nbytes), ctypes.addressof(wbytes)))
+    return plan, wbytes.value
+
+
+_HEADER_DTYPE = np.dtype([("magic", "<u4"), ("version", "<i4"), ("L", "<i4"), ("batch", "<i4"), ("H", "<i4"),
+                          ("H_q", "<i4"), ("H_p", "<i4"), ("P", "<i4"), ("d", "<i4"), ("G", "<i4"),
+                          ("N_CTA", "<i4"), ("max_slots", "<i4"), ("plan_bytes", "<i8"),
+                          ("workspace_bytes", "<i8"), ("layers", "<i8")])
+_LAYER_DTYPE = np.dtype([("cta_off", "<i8"), ("items", "<i8"), ("n_items", "<i4"), ("n_slots", "<i4")])
+WORK_ITEM_DTYPE = np.dtype([("b", "<i4"), ("h", "<i4"), ("hpos", "<i4"), ("g", "<i4"), ("t0", "<i4"),
+                            ("t1", "<i4"), ("slot0", "<i4"), ("part", "<i4"), ("nparts", "<i4"),
+                            ("reserved", "<i4", (3,))])
+
+
+def plan_header(plan: np.ndarray) -> dict:
+    """Read the documented plan header (tg.h: tg_plan_header)."""
+    h = np.frombuffer(plan[:_HEADER_DTYPE.itemsize].tobytes(), _HEADER_DTYPE)[0]
+    if int(h["magic"]) != PLAN_MAGIC:
+        raise ValueError("not a tg plan")
+    return {k: int(h[k]) for k in _HEADER_DTYPE.names}
+
+
+def plan_items(plan: np.ndarray, layer: int):
+    """(cta_off int32 [N_CTA+1], items WORK_ITEM_DTYPE [n]) of one plan layer."""
+    hd = plan_header(plan)
+    lt = np.frombuffer(plan[hd["layers"]:hd["layers"] + _LAYER_DTYPE.itemsize * hd["L"]].tobytes(),
+                       _LAYER_DTYPE)[layer]
+    off = np.frombuffer(plan[lt["cta_off"]:lt["cta_off"] + 4 * (hd["N_CTA"] + 1)].tobytes(), np.int32)
+    n = int(lt["n_items"])
+    items = np.frombuffer(plan[lt["items"]:lt["items"] + n * WORK_ITEM_DTYPE.itemsize].tobytes(), WORK_ITEM_DTYPE)
+    return off, items
+
+
+# ------------------------------------------------------------------ GPU entry points
+
+def tg_decode_attn(plan_host: np.ndarray, plan_dev, layer: int, q, pool, pool_pages: int, pt_off, pt_ids,
+                   scale: float, workspace, out, lse=None, dev_status=None, cta_time=None, stream=None):
+    """One layer of ragged split-KV decode attention (tg.h: tg_decode_attn); asynchronous."""
+    import torch
+    lib = load()
+    if not (isinstance(plan_host, np.ndarray) and plan_host.dtype == np.uint8 and plan_host.flags.c_contiguous):
+        raise TypeError("plan_host must be the contiguous uint8 array from tg_plan_decode")
+    _check(lib.tg_decode_attn(_stream(stream), plan_host.ctypes.data, _dev(plan_dev, torch.uint8, "plan_dev"),
+                              int(layer), _dev(q, torch.bfloat16, "q"), _dev(pool, torch.bfloat16, "pool"),
+                              int(pool_pages), _dev(pt_off, torch.int64, "pt_off"),
+                              _dev(pt_ids, torch.int32, "pt_ids"), float(scale), _dev(workspace, None, "workspace"),
+                              workspace.numel() * workspace.element_size(), _dev(out, torch.bfloat16, "out"),
+                              _dev(lse, torch.float32, "lse"), _dev(dev_status, torch.int32, "dev_status"),
+                              _dev(cta_time, torch.int64, "cta_time")))
+
+
+def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok, pt_off, pt_ids, pool_pages,
+                    pool, kept_idx=None, dev_status=None, stream=None):
+    """Top-n retention + compaction of one layer into the group pages (tg.h: tg_compact_topk)."""
+    import torch
+    lib = load()
+    _check(lib.tg_compact_topk(_stream(stream), batch, H, H_p, P, d, Nmax, _dev(N, torch.int32, "N"),
+                               _dev(scores, torch.float32, "scores"), _dev(K, torch.bfloat16, "K"),
+                               _dev(V, torch.bfloat16, "V"), _dev(head_order, torch.int32, "head_order"),
+                               _dev(ntok, torch.int32, "ntok"), _dev(pt_off, torch.int64, "pt_off"),
+                               _dev(pt_ids, torch.int32, "pt_ids"), int(pool_pages),
+                               _dev(pool, torch.bfloat16, "pool"), _dev(kept_idx, torch.int32, "kept_idx"),
+                               _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_build_minmax(batch, H, N, P, d, K, minmax, dev_status=None, stream=None):
+    """Per-page min/max key vectors (tg.h: tg_build_minmax)."""
+    import torch
+    lib = load()
+    _check(lib.tg_build_minmax(_stream(stream), batch, H, N, P, d, _dev(K, torch.bfloat16, "K"),
+                               _dev(minmax, torch.bfloat16, "minmax"), _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, dev_status=None, stream=None):
+    """Quest page bound + per-KV-head top-K pages (tg.h: tg_page_score_topk)."""
+    import torch
+    lib = load()
+    _check(lib.tg_page_score_topk(_stream(stream), batch, H, g, d, n_pages, K, _dev(q, torch.bfloat16, "q"),
+                                  _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
+                                  _dev(pt_ids, torch.int32, "pt_ids"), _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_check_status(dev_status) -> int:
+    """Raw bits of a device status word (synchronous); raises TGError if any is set."""
+    import torch
+    lib = load()
+    v = ctypes.c_int32(0)
+    _check(lib.tg_check_status(_dev(dev_status, torch.int32, "dev_status"), ctypes.addressof(v)))
+    return v.value

@@ -1,0 +1,96 @@
+// Block-wide helpers for exact top-k selection with ties to the lower index:
+// an exclusive scan of per-thread flags and an MSB-first radix select over
+// order-preserving uint32 keys.  Used by the token top-k compaction and by the
+// page top-K.
+#pragma once
+
+#include <cstdint>
+
+namespace tgk {
+
+// Exclusive prefix count of `flag` over the block (thread order), plus the total.
+// `scratch` holds at least 33 ints of shared memory.  Contains two __syncthreads.
+template <int NT>
+__device__ __forceinline__ int block_excl_count(bool flag, int *scratch, int &total) {
+  static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+  constexpr int NWARP = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
+  const int in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) scratch[warp] = __popc(bal);
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < NWARP ? scratch[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane < NWARP) scratch[lane] = inc - v;
+    if (lane == 31) scratch[32] = inc;
+  }
+  __syncthreads();
+  total = scratch[32];
+  return scratch[warp] + in_warp;
+}
+
+// Find the key T of the k-th largest of `count` keys (1 <= k <= count) and the
+// number of keys equal to T that a top-k must take (the lowest-indexed ones):
+// need_eq = k - #{key > T}.  get(i) returns key i.  `hist` is 256 ints and
+// `scratch` 4 ints of shared memory.
+template <int NT, typename GetKey>
+__device__ __forceinline__ void block_radix_select(int count, int k, GetKey get, int *hist, int *scratch,
+                                                   uint32_t &T, int &need_eq) {
+  uint32_t prefix = 0, mask = 0;
+  int k_rem = k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < count; i += NT) {
+      const uint32_t key = get(i);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down
+      int local[8];
+      int s = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        local[t] = hist[255 - 8 * lane - t];
+        s += local[t];
+      }
+      int inc = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const int before = inc - s;  // keys in digits above this lane's block
+      if (before < k_rem && k_rem <= inc) {
+        int above = before;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (above + local[t] >= k_rem) {
+            scratch[0] = 255 - 8 * lane - t;
+            scratch[1] = above;
+            break;
+          }
+          above += local[t];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t digit = (uint32_t)scratch[0];
+    k_rem -= scratch[1];
+    prefix |= digit << shift;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  T = prefix;
+  need_eq = k_rem;
+}
+
+}  // namespace tgk

@@ -1,0 +1,177 @@
+// Token top-k retention and compaction into the ragged group pages.
+//
+// Source: "Tangram: Unlocking Non-Uniform KV Cache Compression for Efficient
+// Multi-turn LLM Serving" (paper-review page), 3.1 Budget Reservation
+// (I_{l,h} = Top(ceil(B_{l,h} N), s_{l,h}), done as each prefill chunk's KV is
+// ready) and 3.2 Ragged Paging (each H_p-head group writes into its own pages
+// of H_p x 2 x P x d elements).
+//
+// One CTA per (request, KV head) row:
+//  1. exact top-n by an MSB-first radix select over order-preserving keys of
+//     the float32 scores (cached in shared memory when they fit), giving the
+//     n-th largest key T and how many keys equal to T to keep;
+//  2. one ascending sweep that keeps key > T, plus the lowest-indexed keys
+//     equal to T, numbers them with a block scan and copies their K and V rows
+//     (16-byte vector loads/stores, one row per 16-thread group at d=128) to
+//     page k/P, row k%P of the head's block inside its group page;
+//  3. zero-fills the rows of the head's last page past n, so a decode kernel
+//     may read whole tiles.
+#include "block_select.cuh"
+#include "ptx.cuh"
+#include "tg_internal.h"
+
+#include <cuda_runtime.h>
+
+namespace {
+
+using namespace tgk;
+
+constexpr int kThreads = 1024;
+constexpr int kSmemKeys = 40960;  // rows up to this length keep their keys in shared memory
+
+struct CompactArgs {
+  const int32_t *N;
+  const float *scores;
+  const uint16_t *K, *V;
+  const int32_t *head_order, *ntok;
+  const int64_t *pt_off;
+  const int32_t *pt_ids;
+  int64_t pool_pages;
+  uint16_t *pool;
+  int32_t *kept_idx;
+  int32_t *status;
+  int H, H_p, G, P, d, Nmax;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const CompactArgs a) {
+  extern __shared__ uint32_t cache[];  // kSmemKeys keys when the row fits, else unused
+  __shared__ int hist[256];
+  __shared__ int scan[33];
+  __shared__ int sel_scratch[4];
+  __shared__ int tok_list[kThreads];
+  __shared__ int err_flag;
+
+  const int row = blockIdx.x, b = row / a.H, h = row % a.H;
+  const int Nb = a.N[b], n = a.ntok[row];
+  if (threadIdx.x == 0) err_flag = 0;
+  __syncthreads();
+  if (Nb < 0 || Nb > a.Nmax || n < 0 || n > Nb) {
+    if (threadIdx.x == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    return;
+  }
+  // position of h in its group
+  int pos = -1;
+  for (int i = 0; i < a.H; ++i)
+    if (a.head_order[i] == h) pos = i;
+  if (pos < 0) {
+    if (threadIdx.x == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    return;
+  }
+  const int grp = pos / a.H_p, hpos = pos % a.H_p;
+  const int64_t base = a.pt_off[b * a.G + grp];
+  const int64_t npages = a.pt_off[b * a.G + grp + 1] - base;
+  if ((int64_t)(n + a.P - 1) / a.P > npages) {
+    if (threadIdx.x == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    return;
+  }
+  if (n == 0) return;
+
+  const float *srow = a.scores + (size_t)row * a.Nmax;
+  const bool cached = a.Nmax <= kSmemKeys;  // the launch sized the cache for Nmax keys
+  bool nan_seen = false;
+  if (cached) {
+    for (int t = threadIdx.x; t < Nb; t += kThreads) {
+      const float f = srow[t];
+      nan_seen |= is_nan(f);
+      cache[t] = float_key(f);
+    }
+  } else {
+    for (int t = threadIdx.x; t < Nb; t += kThreads) nan_seen |= is_nan(srow[t]);
+  }
+  if (nan_seen) err_flag = 1;
+  __syncthreads();
+  if (err_flag && threadIdx.x == 0) report(a.status, TG_STATUS_NONFINITE);
+  auto key_of = [&](int t) -> uint32_t { return cached ? cache[t] : float_key(srow[t]); };
+
+  uint32_t T;
+  int need_eq;
+  block_radix_select<kThreads>(Nb, n, key_of, hist, sel_scratch, T, need_eq);
+
+  const int d16 = a.d / 8;  // 16-byte chunks per row
+  const size_t src_row0 = (size_t)row * a.Nmax;
+  int taken = 0, eq_seen = 0;
+  for (int c0 = 0; c0 < Nb && taken < n; c0 += kThreads) {
+    const int t = c0 + threadIdx.x;
+    const uint32_t key = t < Nb ? key_of(t) : 0u;
+    const bool gt = t < Nb && key > T, eq = t < Nb && key == T;
+    int eq_total, sel_total;
+    const int eq_rank = eq_seen + block_excl_count<kThreads>(eq, scan, eq_total);
+    const bool sel = gt || (eq && eq_rank < need_eq);
+    const int k_in = block_excl_count<kThreads>(sel, scan, sel_total);
+    if (sel) {
+      tok_list[k_in] = t;
+      if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in] = t;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < sel_total * d16; e += kThreads) {
+      const int r = e / d16, c = e % d16;
+      const int k = taken + r;
+      const int32_t page = a.pt_ids[base + k / a.P];
+      if (page < 0 || (int64_t)page >= a.pool_pages) {
+        report(a.status, TG_STATUS_BAD_PAGE);
+        continue;
+      }
+      const size_t dst = ((((size_t)page * a.H_p + hpos) * 2) * a.P + (k % a.P)) * a.d + (size_t)c * 8;
+      const size_t src = (src_row0 + tok_list[r]) * a.d + (size_t)c * 8;
+      *reinterpret_cast<uint4 *>(a.pool + dst) = *reinterpret_cast<const uint4 *>(a.K + src);
+      *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = *reinterpret_cast<const uint4 *>(a.V + src);
+    }
+    taken += sel_total;
+    eq_seen += eq_total;
+    __syncthreads();
+  }
+
+  // zero the rows of the last page past n (K and V blocks)
+  const int rem = n % a.P;
+  if (rem) {
+    const int32_t page = a.pt_ids[base + (n - 1) / a.P];
+    if (page >= 0 && (int64_t)page < a.pool_pages) {
+      const int rows = a.P - rem;
+      for (int e = threadIdx.x; e < 2 * rows * d16; e += kThreads) {
+        const int kv = e / (rows * d16), r = (e / d16) % rows, c = e % d16;
+        const size_t dst = ((((size_t)page * a.H_p + hpos) * 2 + kv) * a.P + rem + r) * a.d + (size_t)c * 8;
+        *reinterpret_cast<uint4 *>(a.pool + dst) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int Nmax,
+                               const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
+                               const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
+                               const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool, int32_t *kept_idx,
+                               int32_t *dev_status) {
+  if (batch < 0 || H <= 0 || H_p <= 0 || P <= 0 || d <= 0 || Nmax <= 0)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: sizes must be positive");
+  if (H % H_p) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: H %% H_p != 0");
+  if (P % 16 || d % 8 || d > 512) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: need P %% 16 == 0, d %% 8 == 0, d <= 512");
+  if (batch == 0) return tgi::ok();
+  if (!N || !scores || !K || !V || !head_order || !ntok || !pt_off || !pt_ids || !pool)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: NULL pointer argument");
+  if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(pool)) & 15)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: K, V and pool must be 16-byte aligned");
+  CompactArgs a;
+  a.N = N; a.scores = scores; a.K = K; a.V = V; a.head_order = head_order; a.ntok = ntok;
+  a.pt_off = pt_off; a.pt_ids = pt_ids; a.pool_pages = pool_pages; a.pool = pool; a.kept_idx = kept_idx;
+  a.status = dev_status; a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
+  const int smem = (Nmax <= kSmemKeys ? Nmax : 0) * (int)sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
+  if (e == cudaSuccess) {
+    compact_topk_kernel<<<batch * H, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: %s", cudaGetErrorString(e));
+  return tgi::ok();
+}

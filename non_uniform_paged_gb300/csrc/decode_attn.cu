@@ -1,0 +1,507 @@
+// Split-KV flash decoding over the ragged (head-wise non-uniform) page pool,
+// with the log-sum-exp merge fused in.
+//
+// Source: "Tangram: Unlocking Non-Uniform KV Cache Compression for Efficient
+// Multi-turn LLM Serving" (paper-review page), 3.2 Ragged Paging (group pages
+// of H_p x 2 x P x d elements) and 3.3 AOT Load Balancing (one launch of N_CTA
+// CTAs per layer, each CTA given an equal share of its group's retained tokens
+// by the static split map); "FlexiCache ... (MLSys 2026)" (paper-review page),
+// "Core method / Sparse decode" (flash decoding restricted to per-head page
+// lists).
+//
+// Design (GB300):
+//  * One persistent CTA per SM slot, NW warps.  The CTA walks its work items
+//    (pieces of one (request, KV head) run); inside an item, 16-token tiles go
+//    round-robin to the warps.
+//  * Each warp owns an R-stage ring in shared memory.  Its lane 0 streams the
+//    K and V rows of a tile with 2-D TMA loads (128-byte swizzle) that complete
+//    on the stage's mbarrier; the warp waits with a time limit.
+//  * Q.K^T and P.V run on the tensor cores as bf16 m16n8k16 MMAs with float32
+//    accumulation: S^T[16 tokens x 8] = K[16 x d] . Q^T[d x 8] (the g <= 8
+//    query heads of the KV head are the N columns), then O^T[d x 8] +=
+//    V^T[d x 16] . P^T[16 x 8].  movmatrix turns the S^T accumulator into the
+//    P^T operand without shared memory.  Online softmax in base 2.
+//  * At the end of an item the warps' (m, l, O) are merged in shared memory.
+//    A run finished by one CTA is normalised and written directly; a run
+//    shared by several CTAs leaves a float32 partial in the workspace, and the
+//    last CTA to finish (atomic counter, no waiting) merges all partials and
+//    resets the counter.
+#include "ptx.cuh"
+#include "tg_internal.h"
+
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+namespace {
+
+using namespace tgk;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up a copy wait after 2 s
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+struct DecodeArgs {
+  const tg_work_item *items;
+  const int32_t *cta_off;
+  const uint16_t *q;
+  uint16_t *out;
+  float *lse;
+  const int64_t *pt_off;
+  const int32_t *pt_ids;
+  int64_t pool_pages;
+  int32_t *counters;
+  float *ws_ml;
+  float *ws_o;
+  int32_t *status;
+  int64_t *cta_time;
+  int H, H_q, g, G, H_p, P;
+  float scale_log2;
+};
+
+template <int D>
+struct KCfg;
+template <>
+struct KCfg<128> {
+  static constexpr int NW = 8, R = 3;
+};
+template <>
+struct KCfg<256> {
+  static constexpr int NW = 4, R = 3;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int NW = KCfg<D>::NW, R = KCfg<D>::R;
+  static constexpr int TILE = 16 * D * 2;  // bytes of 16 rows of K (or V)
+  static constexpr int STAGE = 2 * TILE;   // K tile then V tile
+  static constexpr int RING = NW * R * STAGE;
+  static constexpr int OSTRIDE = D + 4;    // floats per (warp, head) row of the merge buffer
+  static int smem_bytes(int g) {
+    return 1024 + RING + NW * g * OSTRIDE * 4 + NW * 8 * 4 * 2 + NW * R * 8 + 16;
+  }
+};
+
+// byte offset of element (row, col) of a TMA tile loaded as D/64 boxes of
+// [16 rows][64 cols] bf16 with the 128-byte swizzle (16-byte chunk ^= row % 8)
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return (uint32_t)((col >> 6) * 2048 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void item_tiles(const tg_work_item &it, int &k_lo, int &k_hi) {
+  if (it.t1 > it.t0) {
+    k_lo = it.t0 >> 4;
+    k_hi = (it.t1 + 15) >> 4;
+  } else {
+    k_lo = k_hi = 0;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
+    ragged_decode_kernel(const __grid_constant__ CUtensorMap pool_map, const DecodeArgs a) {
+  using LY = Layout<D>;
+  constexpr int NW = LY::NW, R = LY::R, NT = NW * 32, KS = D / 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = smem;
+  float *comb_o = reinterpret_cast<float *>(smem + LY::RING);  // [NW][g][OSTRIDE]
+  float *comb_m = comb_o + NW * a.g * LY::OSTRIDE;              // [NW][8]
+  float *comb_l = comb_m + NW * 8;                              // [NW][8]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(comb_l + NW * 8);  // [NW][R]
+  int *flag = reinterpret_cast<int *>(bars + NW * R);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int cta = blockIdx.x;
+  uint64_t t_start = 0;
+  if (tid == 0) t_start = globaltimer_ns();
+
+  const int i_begin = a.cta_off[cta], i_end = a.cta_off[cta + 1];
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&bars[warp * R + s], 1);
+  }
+  if (tid == 0) prefetch_tensormap(&pool_map);
+  fence_barrier_init();
+  __syncthreads();
+
+  // ---------------- producer cursor: this warp's tiles across the CTA's items
+  int p_item = i_begin, p_k = 0, p_khi = 0, p_hpos = 0;
+  int64_t p_base = 0;
+  auto p_seek = [&](int from) {  // first item >= from in which this warp has a tile
+    for (p_item = from; p_item < i_end; ++p_item) {
+      const tg_work_item it = a.items[p_item];
+      int lo, hi;
+      item_tiles(it, lo, hi);
+      if (hi - lo > warp) {
+        p_k = lo + warp;
+        p_khi = hi;
+        p_hpos = it.hpos;
+        p_base = a.pt_off[it.b * a.G + it.g];
+        return;
+      }
+    }
+  };
+  auto p_advance = [&]() {
+    p_k += NW;
+    if (p_k >= p_khi) p_seek(p_item + 1);
+  };
+  int issued = 0, consumed = 0;
+  auto issue = [&]() {  // lane 0: load tile p_k of the current producer item into stage issued % R
+    const int s = issued % R;
+    uint64_t *bar = &bars[warp * R + s];
+    uint8_t *dst = ring + (warp * R + s) * LY::STAGE;
+    const int tok = p_k * 16;
+    const int32_t page = a.pt_ids[p_base + tok / a.P];
+    if (page < 0 || (int64_t)page >= a.pool_pages) {
+      report(a.status, TG_STATUS_BAD_PAGE);
+      mbar_arrive(bar);  // complete the phase without data
+      return;
+    }
+    const int row_k = (int)(((int64_t)page * a.H_p + p_hpos) * 2 * a.P + (tok % a.P));
+    mbar_arrive_expect_tx(bar, LY::STAGE);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_2d(dst + c * 2048, &pool_map, bar, c * 64, row_k);
+      tma_load_2d(dst + LY::TILE + c * 2048, &pool_map, bar, c * 64, row_k + a.P);
+    }
+  };
+
+  p_seek(i_begin);
+  for (int s = 0; s < R && p_item < i_end; ++s) {
+    if (lane == 0) issue();
+    ++issued;
+    p_advance();
+  }
+
+  // ---------------- consumer state
+  bool dead = false;  // a wait timed out: skip all further work, keep the barriers
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[KS][4];
+#pragma unroll
+  for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  uint32_t qf[KS][2];
+
+  for (int ii = i_begin; ii < i_end; ++ii) {
+    const tg_work_item it = a.items[ii];
+    int k_lo, k_hi;
+    item_tiles(it, k_lo, k_hi);
+    if (k_hi - k_lo > warp && !dead) {
+      const uint16_t *qrow = a.q + ((size_t)it.b * a.H_q + (size_t)it.h * a.g + gid) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qf[ks][0] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tig) : 0u;
+        qf[ks][1] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
+      }
+      for (int kk = k_lo + warp; kk < k_hi; kk += NW) {
+        const int s = consumed % R;
+        bool ok = mbar_wait(&bars[warp * R + s], (uint32_t)((consumed / R) & 1), kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) report(a.status, TG_STATUS_TIMEOUT);
+          dead = true;
+          break;
+        }
+        const uint32_t kbase = smem_addr(ring + (warp * R + s) * LY::STAGE);
+        const uint32_t vbase = kbase + LY::TILE;
+        const int r0 = it.t0 - kk * 16, r1 = it.t1 - kk * 16;  // valid rows [r0, r1) of the tile
+
+        // S^T = K . Q^T  (rows: tokens, cols: query heads)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbase + swz((lane & 7) + ((lane >> 3) & 1) * 8, ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+          mma_16816(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
+        // online softmax, base 2; thread holds tokens gid, gid+8 of heads 2*tig, 2*tig+1
+        const bool v0 = gid >= r0 && gid < r1, v1 = gid + 8 >= r0 && gid + 8 < r1;
+        float z0 = v0 ? sc[0] * a.scale_log2 : -INFINITY;
+        float z1 = v0 ? sc[1] * a.scale_log2 : -INFINITY;
+        float z2 = v1 ? sc[2] * a.scale_log2 : -INFINITY;
+        float z3 = v1 ? sc[3] * a.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float c0 = ex2(m0 - mn0), c1 = ex2(m1 - mn1);
+        const float p0 = ex2(z0 - mn0), p1 = ex2(z1 - mn1), p2 = ex2(z2 - mn0), p3 = ex2(z3 - mn1);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+        m0 = mn0;
+        m1 = mn1;
+        const uint32_t b0 = movmatrix_t(pack_bf16x2(p0, p1));
+        const uint32_t b1 = movmatrix_t(pack_bf16x2(p2, p3));
+        // O^T += V^T . P^T
+#pragma unroll
+        for (int mb = 0; mb < KS; ++mb) {
+          o[mb][0] *= c0;
+          o[mb][1] *= c1;
+          o[mb][2] *= c0;
+          o[mb][3] *= c1;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vbase + swz((lane & 7) + (lane >> 4) * 8, mb * 16 + ((lane >> 3) & 1) * 8), a0, a1, a2, a3);
+          mma_16816(o[mb], a0, a1, a2, a3, b0, b1);
+        }
+        ++consumed;
+        __syncwarp();
+        if (p_item < i_end) {
+          if (lane == 0) {
+            fence_proxy_async_smem();  // our ldmatrix reads of this stage come before the refill
+            issue();
+          }
+          ++issued;
+          p_advance();
+        }
+      }
+    }
+
+    // ---- merge the warps' states of this item in shared memory
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (gid == 0) {
+      comb_m[warp * 8 + 2 * tig] = m0;
+      comb_m[warp * 8 + 2 * tig + 1] = m1;
+      comb_l[warp * 8 + 2 * tig] = l0;
+      comb_l[warp * 8 + 2 * tig + 1] = l1;
+    }
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+    for (int mb = 0; mb < KS; ++mb) {
+      if (h0 < a.g) {
+        comb_o[(warp * a.g + h0) * LY::OSTRIDE + mb * 16 + gid] = o[mb][0];
+        comb_o[(warp * a.g + h0) * LY::OSTRIDE + mb * 16 + gid + 8] = o[mb][2];
+      }
+      if (h1 < a.g) {
+        comb_o[(warp * a.g + h1) * LY::OSTRIDE + mb * 16 + gid] = o[mb][1];
+        comb_o[(warp * a.g + h1) * LY::OSTRIDE + mb * 16 + gid + 8] = o[mb][3];
+      }
+      o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
+    }
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+    __syncthreads();
+
+    const size_t out_row0 = (size_t)it.b * a.H_q + (size_t)it.h * a.g;
+    if (it.t1 <= it.t0) {  // a head with no retained token
+      for (int e = tid; e < a.g * D; e += NT) {
+        a.out[(out_row0 + e / D) * D + e % D] = 0;
+        if (e % D == 0 && a.lse) a.lse[out_row0 + e / D] = -INFINITY;
+      }
+    } else {
+      const int slot = it.slot0 + it.part;
+      for (int e = tid; e < a.g * D; e += NT) {
+        const int hd = e / D, dd = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, comb_m[w * 8 + hd]);
+        float Ls = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float f = ex2(comb_m[w * 8 + hd] - M);
+          Ls += comb_l[w * 8 + hd] * f;
+          O += comb_o[(w * a.g + hd) * LY::OSTRIDE + dd] * f;
+        }
+        if (it.nparts == 1) {
+          __nv_bfloat16 v = __float2bfloat16_rn(O / Ls);
+          a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
+          if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (M + log2f(Ls)) * kLn2;
+        } else {
+          a.ws_o[((size_t)slot * a.g + hd) * D + dd] = O;
+          if (dd == 0) {
+            a.ws_ml[((size_t)slot * a.g + hd) * 2] = M;
+            a.ws_ml[((size_t)slot * a.g + hd) * 2 + 1] = Ls;
+          }
+        }
+      }
+      if (it.nparts > 1) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+          const int prev = atomicAdd(&a.counters[it.b * a.H + it.h], 1);
+          *flag = prev == it.nparts - 1;
+        }
+        __syncthreads();
+        if (*flag) {  // the last CTA of this run merges every partial
+          __threadfence();
+          for (int e = tid; e < a.g * D; e += NT) {
+            const int hd = e / D, dd = e % D;
+            float M = -INFINITY;
+            for (int p = 0; p < it.nparts; ++p)
+              M = fmaxf(M, __ldcg(&a.ws_ml[((size_t)(it.slot0 + p) * a.g + hd) * 2]));
+            float Ls = 0.f, O = 0.f;
+            for (int p = 0; p < it.nparts; ++p) {
+              const size_t sp = (size_t)(it.slot0 + p) * a.g + hd;
+              const float f = ex2(__ldcg(&a.ws_ml[sp * 2]) - M);
+              Ls += __ldcg(&a.ws_ml[sp * 2 + 1]) * f;
+              O += __ldcg(&a.ws_o[sp * D + dd]) * f;
+            }
+            __nv_bfloat16 v = __float2bfloat16_rn(O / Ls);
+            a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
+            if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (M + log2f(Ls)) * kLn2;
+          }
+          if (tid == 0) atomicExch(&a.counters[it.b * a.H + it.h], 0);
+        }
+      }
+    }
+    __syncthreads();  // the merge buffer is reused by the next item
+  }
+
+  // drain copies still in flight (only after a timeout; otherwise issued == consumed)
+  if (lane == 0) {
+    for (int t = consumed; t < issued; ++t)
+      if (!mbar_wait(&bars[warp * R + t % R], (uint32_t)((t / R) & 1), kWaitLimitNs)) break;
+  }
+  __syncwarp();
+  if (tid == 0 && a.cta_time) {
+    a.cta_time[2 * cta] = (int64_t)t_start;
+    a.cta_time[2 * cta + 1] = (int64_t)globaltimer_ns();
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <int D>
+void *kernel_ptr() {
+  return reinterpret_cast<void *>(&ragged_decode_kernel<D>);
+}
+
+int kernel_config(int d, int g, void **fn, int *threads, int *smem) {
+  if (d == 128) {
+    *fn = kernel_ptr<128>();
+    *threads = KCfg<128>::NW * 32;
+    *smem = Layout<128>::smem_bytes(g);
+  } else if (d == 256) {
+    *fn = kernel_ptr<256>();
+    *threads = KCfg<256>::NW * 32;
+    *smem = Layout<256>::smem_bytes(g);
+  } else {
+    return tgi::fail(TG_ERR_SHAPE, "tg_decode_attn: d=%d (128 or 256)", d);
+  }
+  if (g < 1 || g > 8) return tgi::fail(TG_ERR_SHAPE, "tg_decode_attn: g=%d (1..8)", g);
+  cudaError_t e = cudaFuncSetAttribute(*fn, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  return TG_OK;
+}
+
+}  // namespace
+
+extern "C" int tg_query_ncta(int d, int g, int *N_CTA) {
+  if (!N_CTA) return tgi::fail(TG_ERR_INVALID_ARG, "tg_query_ncta: NULL N_CTA");
+  void *fn;
+  int threads, smem;
+  int rc = kernel_config(d, g, &fn, &threads, &smem);
+  if (rc) return rc;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_query_ncta: %s", cudaGetErrorString(e));
+  *N_CTA = per_sm * sms;
+  return tgi::ok();
+}
+
+extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
+                              const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
+                              const int64_t *pt_off, const int32_t *pt_ids, float scale,
+                              void *workspace, int64_t workspace_bytes,
+                              uint16_t *out, float *lse, int32_t *dev_status, int64_t *cta_time) {
+  if (!plan_host || !plan_dev || !q || !pool || !pt_off || !pt_ids || !workspace || !out)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: NULL pointer argument");
+  const tg_plan_header *hd = static_cast<const tg_plan_header *>(plan_host);
+  if (hd->magic != TG_PLAN_MAGIC || hd->version != 1)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: plan_host is not a tg_plan_decode buffer");
+  if (layer < 0 || layer >= hd->L) return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: layer %d of %d", layer, hd->L);
+  if (!std::isfinite(scale)) return tgi::fail(TG_ERR_NONFINITE, "tg_decode_attn: scale is not finite");
+  if (workspace_bytes < hd->workspace_bytes)
+    return tgi::fail(TG_ERR_CAPACITY, "tg_decode_attn: workspace %lld < %lld bytes", (long long)workspace_bytes,
+                     (long long)hd->workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(pool) & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255) ||
+      (reinterpret_cast<uintptr_t>(plan_dev) & 15) || (reinterpret_cast<uintptr_t>(q) & 3))
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: pool/plan must be 16-byte, workspace 256-byte aligned");
+  const int64_t rows = pool_pages * hd->H_p * 2 * hd->P;
+  if (pool_pages <= 0 || rows > INT32_MAX)
+    return tgi::fail(TG_ERR_CAPACITY, "tg_decode_attn: pool_pages=%lld gives %lld rows (1..2^31-1)",
+                     (long long)pool_pages, (long long)rows);
+  const int g = hd->H_q / hd->H;
+  void *fn;
+  int threads, smem;
+  int rc = kernel_config(hd->d, g, &fn, &threads, &smem);
+  if (rc) return rc;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn: cuTensorMapEncodeTiled is unavailable");
+
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)hd->d, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)hd->d * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), gdim, gstride, box,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+
+  const tg_plan_layer *lt =
+      reinterpret_cast<const tg_plan_layer *>(static_cast<const uint8_t *>(plan_host) + hd->layers) + layer;
+  const uint8_t *pd = static_cast<const uint8_t *>(plan_dev);
+  const tgi::WorkspaceLayout wl = tgi::workspace_layout(hd->batch, hd->H, g, hd->d, hd->max_slots);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeArgs args;
+  args.items = reinterpret_cast<const tg_work_item *>(pd + lt->items);
+  args.cta_off = reinterpret_cast<const int32_t *>(pd + lt->cta_off);
+  args.q = q;
+  args.out = out;
+  args.lse = lse;
+  args.pt_off = pt_off;
+  args.pt_ids = pt_ids;
+  args.pool_pages = pool_pages;
+  args.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+  args.ws_ml = reinterpret_cast<float *>(ws + wl.ml);
+  args.ws_o = reinterpret_cast<float *>(ws + wl.o);
+  args.status = dev_status;
+  args.cta_time = cta_time;
+  args.H = hd->H;
+  args.H_q = hd->H_q;
+  args.g = g;
+  args.G = hd->G;
+  args.H_p = hd->H_p;
+  args.P = hd->P;
+  args.scale_log2 = scale * kLog2e;
+  // without a caller status word, faults are recorded in the workspace's own
+  if (!dev_status) args.status = reinterpret_cast<int32_t *>(ws + wl.status);
+  void *params[] = {&map, &args};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(hd->N_CTA), dim3(threads), params, (size_t)smem,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn: launch failed: %s", cudaGetErrorString(e));
+  return tgi::ok();
+}
+
+extern "C" int tg_check_status(const int32_t *dev_status, int32_t *host_status) {
+  if (!dev_status) return tgi::fail(TG_ERR_INVALID_ARG, "tg_check_status: NULL");
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpy(&v, dev_status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_check_status: %s", cudaGetErrorString(e));
+  if (host_status) *host_status = v;
+  if (v & TG_STATUS_TIMEOUT) return tgi::fail(TG_ERR_TIMEOUT, "device status 0x%x: a copy wait timed out", v);
+  if (v) return tgi::fail(TG_ERR_DEVICE, "device status 0x%x", v);
+  return tgi::ok();
+}

@@ -1,0 +1,143 @@
+"""Device state for ragged paged decode attention, built on the C ABI.
+
+``RaggedCache`` owns the buffers of one model's ragged KV cache -- page pool,
+page tables, head groups, the decode plan and its workspace -- and sequences
+the library calls: page tables and split map on the host (tg_build_pages,
+tg_split_map, tg_plan_decode), then per layer tg_compact_topk at prefill and
+tg_decode_attn at every decode step.  (Tangram paper-review page, 3.1-3.3.)
+
+``SparseDecoder`` runs the FlexiCache-style path over a dense paged cache
+with one page table per KV head: tg_page_score_topk picks each head's top-K
+pages from the MinMax cache, then tg_decode_attn attends to those pages only.
+(FlexiCache paper-review page, "Core method / Sparse decode".)
+
+This module only allocates tensors and passes pointers; all arithmetic runs
+in libtg's kernels.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
+               tg_compact_topk, tg_build_minmax, tg_page_score_topk)
+
+BYTES_BF16 = 2
+
+
+class RaggedCache:
+    def __init__(self, L, batch, H, H_q, d, P, H_p, alpha, Bhat, N, cluster=False, n_cta=None,
+                 uniform_split=False, device="cuda", alloc_pool=True):
+        self.L, self.batch, self.H, self.H_q, self.d, self.P, self.H_p = L, batch, H, H_q, d, P, H_p
+        self.G = H // H_p
+        self.g = H_q // H
+        self.device = torch.device(device)
+        self.N = np.asarray(N, np.int32)
+        self.pages = tg_build_pages(L, batch, H, H_p, P, alpha, Bhat, self.N, cluster)
+        self.n_pages = self.pages["n_pages"]
+        self.n_cta = int(n_cta) if n_cta else tg_query_ncta(d, self.g)
+        Phi = np.ones_like(self.pages["Phi"]) if uniform_split else self.pages["Phi"]
+        self.S = tg_split_map(Phi, self.n_cta)
+        self.plan, self.workspace_bytes = tg_plan_decode(self.S, self.pages["order"], self.pages["ntok"],
+                                                         H_q, H_p, P, d)
+        dev = self.device
+        self.N_dev = torch.from_numpy(self.N).to(dev)
+        self.order_dev = torch.from_numpy(self.pages["order"]).to(dev)
+        self.ntok_dev = torch.from_numpy(self.pages["ntok"]).to(dev)
+        self.pt_off_dev = torch.from_numpy(self.pages["pt_off"]).to(dev)
+        self.pt_ids_dev = torch.from_numpy(self.pages["pt_ids"]).to(dev)
+        self.plan_dev = torch.from_numpy(self.plan).to(dev)
+        self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pool = None
+        if alloc_pool:
+            self.pool = torch.empty(max(self.n_pages, 1) * H_p * 2 * P * d, dtype=torch.bfloat16, device=dev)
+        self.scale = 1.0 / math.sqrt(d)
+
+    # ---- sizes
+    def list_offsets(self, layer: int) -> torch.Tensor:
+        n = self.batch * self.G
+        return self.pt_off_dev[layer * n:(layer + 1) * n + 1]
+
+    def retained_tokens(self, layer=None) -> int:
+        nt = self.pages["ntok"] if layer is None else self.pages["ntok"][layer]
+        return int(nt.sum(dtype=np.int64))
+
+    def algorithmic_bytes(self, layer=None) -> int:
+        """Bytes a decode step must move: retained K+V rows, page-table ids, q and out."""
+        layers = range(self.L) if layer is None else [layer]
+        total = 0
+        for l in layers:
+            ids = int(self.pages["pt_off"][(l + 1) * self.batch * self.G] - self.pages["pt_off"][l * self.batch * self.G])
+            total += self.retained_tokens(l) * 2 * self.d * BYTES_BF16 + 4 * ids
+            total += 2 * self.batch * self.H_q * self.d * BYTES_BF16
+        return total
+
+    # ---- prefill: top-n retention into the pages
+    def compact_layer(self, layer, scores, K, V, kept_idx=None, stream=None):
+        Nmax = scores.shape[-1]
+        tg_compact_topk(self.batch, self.H, self.H_p, self.P, self.d, Nmax, self.N_dev, scores, K, V,
+                        self.order_dev[layer], self.ntok_dev[layer], self.list_offsets(layer), self.pt_ids_dev,
+                        self.n_pages, self.pool, kept_idx=kept_idx, dev_status=self.status, stream=stream)
+
+    # ---- decode: one layer's attention
+    def decode_layer(self, layer, q, out, lse=None, cta_time=None, stream=None, pool=None):
+        tg_decode_attn(self.plan, self.plan_dev, layer, q, self.pool if pool is None else pool, self.n_pages,
+                       self.list_offsets(layer), self.pt_ids_dev, self.scale, self.workspace, out, lse=lse,
+                       dev_status=self.status, cta_time=cta_time, stream=stream)
+
+
+class SparseDecoder:
+    """Top-K page sparse decode over a dense cache [batch][H][n_pages][2][P][d] (H_p = 1 tables)."""
+
+    def __init__(self, batch, H, H_q, d, P, n_pages, K, n_cta=None, device="cuda"):
+        self.batch, self.H, self.H_q, self.d, self.P, self.n_pages, self.K = batch, H, H_q, d, P, n_pages, K
+        self.g = H_q // H
+        dev = torch.device(device)
+        self.n_cta = int(n_cta) if n_cta else tg_query_ncta(d, self.g)
+        # every head attends K full pages: one plan serves every layer
+        ntok = np.full((1, batch, H), K * P, np.int32)
+        order = np.arange(H, dtype=np.int32)[None]
+        Phi = ntok.sum(axis=1).astype(np.int64)
+        self.S = tg_split_map(Phi, self.n_cta)
+        self.plan, self.workspace_bytes = tg_plan_decode(self.S, order, ntok, H_q, 1, P, d)
+        self.plan_dev = torch.from_numpy(self.plan).to(dev)
+        self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pt_off = torch.arange(0, batch * H * K + 1, K, dtype=torch.int64, device=dev)
+        self.sel = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
+        self.pt_ids = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
+        self.scale = 1.0 / math.sqrt(d)
+
+    def select(self, q, minmax, stream=None):
+        tg_page_score_topk(self.batch, self.H, self.g, self.d, self.n_pages, self.K, q, minmax, self.sel,
+                           pt_ids=self.pt_ids, dev_status=self.status, stream=stream)
+
+    def attend(self, q, pool, out, lse=None, cta_time=None, stream=None):
+        tg_decode_attn(self.plan, self.plan_dev, 0, q, pool, self.batch * self.H * self.n_pages, self.pt_off,
+                       self.pt_ids, self.scale, self.workspace, out, lse=lse, dev_status=self.status,
+                       cta_time=cta_time, stream=stream)
+
+    def step(self, q, minmax, pool, out, lse=None, stream=None):
+        self.select(q, minmax, stream=stream)
+        self.attend(q, pool, out, lse=lse, stream=stream)
+
+    def algorithmic_bytes(self) -> int:
+        """MinMax read + selected K/V pages + page ids + q and out, one layer."""
+        mm = self.batch * self.H * self.n_pages * 2 * self.d * BYTES_BF16
+        kv = self.batch * self.H * self.K * self.P * 2 * self.d * BYTES_BF16
+        ids = self.batch * self.H * self.K * 4
+        qo = 2 * self.batch * self.H_q * self.d * BYTES_BF16
+        return mm + kv + ids + qo
+
+
+def build_minmax(K, P, minmax=None, stream=None):
+    """MinMax cache of dense keys K [batch][H][N][d] -> [batch][H][ceil(N/P)][2][d]."""
+    batch, H, N, d = K.shape
+    n_pages = -(-N // P)
+    if minmax is None:
+        minmax = torch.empty((batch, H, n_pages, 2, d), dtype=torch.bfloat16, device=K.device)
+    tg_build_minmax(batch, H, N, P, d, K, minmax, stream=stream)
+    return minmax

@@ -1,0 +1,45 @@
+"""The C-ABI library loads and exports every symbol include/tg.h declares (no GPU calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "tg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tg_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_named_calls():
+    names = declared_functions()
+    for n in ("tg_build_pages", "tg_compact_topk", "tg_split_map", "tg_decode_attn", "tg_page_score_topk"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib._build.LIB)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_binding_names_match_header(lib):
+    for n in declared_functions():
+        if n in ("tg_last_error_string",):
+            continue
+        assert hasattr(lib, n), n
+
+
+def test_version_and_error_string(lib):
+    assert lib.tg_version() >= 100
+    with pytest.raises(lib.TGError) as e:
+        lib.tg_split_map([[1, 2, 3]], 1)
+    assert "N_CTA" in str(e.value)
+
+
+def test_struct_sizes_match_header(lib):
+    assert lib.WORK_ITEM_DTYPE.itemsize == 48
+    assert lib._HEADER_DTYPE.itemsize == 72

@@ -1,0 +1,136 @@
+"""Parity of the ragged decode path on the GPU (through the C ABI) with the
+float64 oracle: top-n compaction into group pages, split-KV decode with the
+fused log-sum-exp merge, over several tiles, ragged tails, empty heads and
+many CTA splits."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import tangram as otg
+
+from gpu_helpers import compare_out, oracle_layer, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def _cache(lib, w, device, n_cta=None, uniform=False, N=None):
+    from non_uniform_paged_gb300.ragged import RaggedCache
+    N = synth.contexts(w) if N is None else N
+    return RaggedCache(w.L, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, synth.budgets_hat(w), N,
+                       cluster=w.cluster, n_cta=n_cta or w.n_cta, uniform_split=uniform, device=device), N
+
+
+def _decode_and_check(lib, w, cuda, n_cta=None, uniform=False, N=None, layers=None):
+    cache, N = _cache(lib, w, cuda, n_cta=n_cta, uniform=uniform, N=N)
+    results = []
+    for layer in (range(w.L) if layers is None else layers):
+        s, K, V, kept = run_layer(lib, w, layer, cache, cuda)
+        q = synth.queries(w, layer, cuda)
+        out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+        lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+        cache.decode_layer(layer, q, out, lse)
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(cache.status) == 0
+        ref_out, ref_lse, idx = oracle_layer(w, layer, s, K, V, q, cache.pages["ntok"][layer], N)
+        # retained index sets are bit-exact
+        kept_h = kept.cpu().numpy()
+        for b in range(w.batch):
+            for h in range(w.H):
+                n = cache.pages["ntok"][layer, b, h]
+                assert np.array_equal(kept_h[b, h, :n], idx[b][h]), (layer, b, h)
+        results.append(compare_out(out, lse, ref_out, ref_lse))
+    return cache, results
+
+
+@pytest.mark.parametrize("n_cta", [1, 2, 5, 16, 152, 600])
+def test_small_many_splits(lib, cuda, n_cta):
+    w = synth.small()
+    n_cta = max(n_cta, w.G)
+    _decode_and_check(lib, w, cuda, n_cta=n_cta)
+
+
+@pytest.mark.parametrize("H_p,cluster", [(1, False), (2, True), (4, False), (4, True)])
+def test_small_groupings(lib, cuda, H_p, cluster):
+    w = synth.small(H=8, H_q=32, H_p=H_p, cluster=cluster, N=900, batch=2)
+    _decode_and_check(lib, w, cuda, n_cta=40)
+
+
+@pytest.mark.parametrize("g", [1, 2, 3, 8])
+def test_small_gqa_widths(lib, cuda, g):
+    w = synth.small(H=4, H_q=4 * g, H_p=2)
+    _decode_and_check(lib, w, cuda, n_cta=24)
+
+
+def test_small_d256(lib, cuda):
+    w = synth.small(d=256, H=8, H_q=16, H_p=4, batch=2, N=640)
+    _decode_and_check(lib, w, cuda, n_cta=20)
+
+
+def test_empty_and_tiny_requests(lib, cuda):
+    w = synth.small(batch=4, N=300)
+    N = np.array([0, 1, 17, 300], np.int32)
+    _decode_and_check(lib, w, cuda, n_cta=9, N=N)
+
+
+def test_full_budget_is_dense_attention(lib, cuda):
+    """B = 1 keeps every token: the kernel reproduces dense softmax attention."""
+    w = synth.small(budget_dist="ones", budget_args=(), ctx_dist="fixed", N=513, batch=2)
+    cache, _ = _decode_and_check(lib, w, cuda, n_cta=30)
+    assert (cache.pages["ntok"] == 513).all()
+
+
+def test_uniform_split_gives_same_result(lib, cuda):
+    """Outputs do not depend on how the work is split across CTAs."""
+    w = synth.small(N=800, batch=2)
+    outs = []
+    for uniform, n_cta in ((False, 37), (True, 37), (False, 3)):
+        cache, N = _cache(lib, w, cuda, n_cta=n_cta, uniform=uniform)
+        s, K, V, _ = run_layer(lib, w, 0, cache, cuda)
+        q = synth.queries(w, 0, cuda)
+        out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+        cache.decode_layer(0, q, out)
+        outs.append(out.float().cpu())
+    # different split points change float32 summation order only
+    assert (outs[0] - outs[1]).abs().max() < 4e-3
+    assert (outs[0] - outs[2]).abs().max() < 4e-3
+
+
+def test_config1_full(lib, cuda):
+    """Config 1 at full size: one Llama-3.1-8B layer, N=4096, N_CTA=148, every output checked."""
+    w = synth.workload(1)
+    _, res = _decode_and_check(lib, w, cuda, n_cta=148)
+    print("config 1 max/mean abs", res)
+
+
+def test_repeat_calls_reuse_workspace(lib, cuda):
+    """The merge counters return to zero, so the workspace serves repeated calls."""
+    w = synth.small(N=700, batch=3)
+    cache, N = _cache(lib, w, cuda, n_cta=50)
+    s, K, V, _ = run_layer(lib, w, 0, cache, cuda)
+    q = synth.queries(w, 0, cuda)
+    out1 = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    out2 = torch.empty_like(out1)
+    cache.decode_layer(0, q, out1)
+    for _ in range(5):
+        cache.decode_layer(0, q, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+    hd = cache.workspace[:w.batch * w.H * 4].view(torch.int32)
+    assert int(hd.abs().sum()) == 0
+
+
+def test_bad_page_id_is_reported(lib, cuda):
+    """A page id past the pool sets TG_STATUS_BAD_PAGE instead of reading out of bounds."""
+    w = synth.small(N=200, batch=1, L=1)
+    cache, N = _cache(lib, w, cuda, n_cta=4)
+    run_layer(lib, w, 0, cache, cuda)
+    cache.pt_ids_dev[0] = cache.n_pages + 5
+    q = synth.queries(w, 0, cuda)
+    out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    cache.status.zero_()
+    cache.decode_layer(0, q, out)
+    torch.cuda.synchronize()
+    with pytest.raises(lib.TGError):
+        lib.tg_check_status(cache.status)
+    assert int(cache.status.item()) & lib.STATUS_BAD_PAGE

@@ -1,0 +1,140 @@
+"""Parity of the FlexiCache-style path on the GPU with the oracle: MinMax cache
+(bit-exact), Quest page score + per-KV-head top-K (bit-exact page ids, the
+score taken in the same float32 order on both sides), and sparse decode over
+the selected pages (float tolerance)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import flexicache as ofx
+from oracle import tangram as otg
+
+from gpu_helpers import compare_out
+
+pytestmark = pytest.mark.gpu
+
+
+def _dense_pool(K, V, P):
+    """Dense paged cache [batch][H][n_pages][2][P][d] from K, V [batch][H][N][d] (N % P == 0)."""
+    b, H, N, d = K.shape
+    n_pages = N // P
+    return torch.stack([K.view(b, H, n_pages, P, d), V.view(b, H, n_pages, P, d)], dim=3).contiguous()
+
+
+def _check_minmax(lib, K, P, mm):
+    mn_ref_all = []
+    K_h = K.float().cpu().numpy()
+    mm_h = mm.float().cpu().numpy()
+    b, H = K.shape[:2]
+    for bb in range(b):
+        for h in range(H):
+            mn, mx = ofx.page_minmax(K_h[bb, h], P)
+            assert np.array_equal(mm_h[bb, h, :, 0], mn) and np.array_equal(mm_h[bb, h, :, 1], mx)
+
+
+@pytest.mark.parametrize("N", [16, 100, 257, 640])
+def test_minmax_exact(lib, cuda, N):
+    from non_uniform_paged_gb300.ragged import build_minmax
+    w = synth.small(N=N, ctx_dist="fixed", batch=2, H=4)
+    K, _ = synth.keys_values(w, 0, cuda)
+    mm = build_minmax(K, 16)
+    torch.cuda.synchronize()
+    _check_minmax(lib, K, 16, mm)
+
+
+def _select_case(lib, cuda, batch, H, g, d, n_pages, K, seed=0, ties=False):
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(seed)
+    q = torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16)
+    mm = torch.randn((batch, H, n_pages, 2, d), generator=gen, device=cuda).to(torch.bfloat16)
+    mm = torch.stack([torch.minimum(mm[:, :, :, 0], mm[:, :, :, 1]), torch.maximum(mm[:, :, :, 0], mm[:, :, :, 1])], 3)
+    if ties:
+        # planted ties: repeat pages, so equal scores must go to the lower page
+        mm[:, :, 1::3] = mm[:, :, 0:-1:3][:, :, :mm[:, :, 1::3].shape[2]]
+        mm[:, :, -1] = mm[:, :, 0]
+    mm = mm.contiguous()
+    sel = torch.empty((batch, H, K), dtype=torch.int32, device=cuda)
+    ids = torch.empty((batch, H, K), dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    lib.tg_page_score_topk(batch, H, g, d, n_pages, K, q, mm, sel, pt_ids=ids, dev_status=status)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(status) == 0
+    q_h = q.float().cpu().numpy()
+    mm_h = mm.float().cpu().numpy()
+    ref = ofx.select_pages(q_h, mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
+    assert np.array_equal(sel.cpu().numpy(), ref)
+    rows = np.arange(batch * H).reshape(batch, H, 1)
+    assert np.array_equal(ids.cpu().numpy(), rows * n_pages + ref)
+
+
+@pytest.mark.parametrize("g,d", [(4, 128), (2, 256), (1, 128), (3, 128), (8, 128)])
+@pytest.mark.parametrize("n_pages,K", [(625, 64), (625, 128), (37, 37), (1000, 1), (2049, 300)])
+def test_page_topk_exact(lib, cuda, g, d, n_pages, K):
+    _select_case(lib, cuda, 2, 2, g, d, n_pages, K, seed=n_pages + K + g)
+
+
+@pytest.mark.parametrize("K", [1, 5, 33])
+def test_page_topk_ties(lib, cuda, K):
+    _select_case(lib, cuda, 2, 3, 4, 128, 200, K, seed=K, ties=True)
+
+
+def test_page_topk_max_pages(lib, cuda):
+    _select_case(lib, cuda, 1, 1, 4, 128, 16384, 2048, seed=3)
+
+
+@pytest.mark.parametrize("K", [4, 10, 25])
+def test_sparse_decode_small(lib, cuda, K):
+    """Score + top-K + attention over the selected pages vs the oracle (small shape)."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=3, N=400, L=1)
+    P = w.P
+    n_pages = w.N // P
+    Kt, Vt = synth.keys_values(w, 0, cuda)
+    q = synth.queries(w, 0, cuda)
+    pool = _dense_pool(Kt, Vt, P)
+    mm = build_minmax(Kt, P)
+    dec = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=64, device=cuda)
+    out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+    dec.step(q, mm, pool, out, lse)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(dec.status) == 0
+    K_h, V_h, q_h = Kt.float().cpu().numpy(), Vt.float().cpu().numpy(), q.float().cpu().numpy()
+    mm_h = mm.float().cpu().numpy()
+    sel_ref = ofx.select_pages(q_h, mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
+    assert np.array_equal(dec.sel.view(w.batch, w.H, K).cpu().numpy(), sel_ref)
+    ref_out = np.zeros((w.batch, w.H_q, w.d))
+    ref_lse = np.zeros((w.batch, w.H_q))
+    for b in range(w.batch):
+        for j in range(w.H_q):
+            h = j // w.g
+            tok = ofx.page_tokens(sel_ref[b, h], P, w.N)
+            ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], K_h[b, h][tok], V_h[b, h][tok],
+                                                         1.0 / math.sqrt(w.d))
+    compare_out(out, lse, ref_out, ref_lse)
+
+
+def test_all_pages_equals_dense(lib, cuda):
+    """K = n_pages: sparse decode is dense attention over the whole context."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=2, N=320, L=1)
+    n_pages = w.N // w.P
+    Kt, Vt = synth.keys_values(w, 0, cuda)
+    q = synth.queries(w, 0, cuda)
+    dec = SparseDecoder(w.batch, w.H, w.H_q, w.d, w.P, n_pages, n_pages, n_cta=40, device=cuda)
+    out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+    dec.step(q, build_minmax(Kt, w.P), _dense_pool(Kt, Vt, w.P), out, lse)
+    torch.cuda.synchronize()
+    assert (dec.sel.view(w.batch, w.H, n_pages).cpu() == torch.arange(n_pages, dtype=torch.int32)).all()
+    K_h, V_h, q_h = Kt.float().cpu().numpy(), Vt.float().cpu().numpy(), q.float().cpu().numpy()
+    ref_out = np.zeros((w.batch, w.H_q, w.d))
+    ref_lse = np.zeros((w.batch, w.H_q))
+    for b in range(w.batch):
+        for j in range(w.H_q):
+            ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], K_h[b, j // w.g], V_h[b, j // w.g],
+                                                         1.0 / math.sqrt(w.d))
+    compare_out(out, lse, ref_out, ref_lse)
