@@ -153,7 +153,7 @@ def oracle_sample(w, budget_s: float, max_heads: int, device, seed: int = 0):
         K, V = synth.keys_values(w, int(layer), device)
         q = synth.queries(w, int(layer), device)
         pairs = [(b, h) for b in range(w.batch) for h in range(w.H)]
-        for i in r.permutation(len(pairs))[:4]:
+        for i in r.permutation(len(pairs))[:16]:
             b, h = pairs[i]
             n = otg.retained_count(B[layer, h], int(N[b]))
             idx = otg.top_indices(s[b, h, :N[b]].cpu().numpy(), n)
@@ -212,6 +212,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -228,6 +230,9 @@ def main():
     from non_uniform_paged_gb300.ragged import RaggedCache
 
     w = synth.workload(args.config)
+    if args.layers or args.batch:
+        w = w.replace(L=args.layers or w.L, batch=args.batch or w.batch,
+                      name=f"{w.name}-override-L{args.layers or w.L}-b{args.batch or w.batch}")
     Bhat = synth.budgets_hat(w)
     N = synth.contexts(w)
     t0 = time.perf_counter()
@@ -264,14 +269,29 @@ def main():
     torch.cuda.synchronize()
     tg.tg_check_status(cache.status)
 
-    # CTA skew under the static split map (one extra, untimed step)
-    cta_time = torch.zeros((w.L, 2 * cache.n_cta), dtype=torch.int64, device=device)
-    for l in range(w.L):
-        cache.decode_layer(l, q[l], out[l], lse[l], cta_time=cta_time[l], stream=stream)
-    torch.cuda.synchronize()
-    ct = cta_time.cpu().numpy().astype(np.float64)
-    busy = ct[:, 1::2] - ct[:, 0::2]
-    skew_per_layer = busy.max(axis=1) / busy.mean(axis=1)
+    # CTA skew (max/mean CTA busy time) of isolated launches, static split map vs a
+    # uniform split of the CTAs over the groups (untimed; same pool, own plan)
+    uni = RaggedCache(w.L, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, Bhat, N, cluster=w.cluster,
+                      n_cta=cache.n_cta, uniform_split=True, device=device, alloc_pool=False)
+    skew = {}
+    for name, c in (("static", cache), ("uniform", uni)):
+        cta_time = torch.zeros((w.L, 2 * c.n_cta), dtype=torch.int64, device=device)
+        ms = []
+        for l in range(w.L):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            c.decode_layer(l, q[l], out[l], lse[l], cta_time=cta_time[l], stream=stream, pool=cache.pool)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        ct = cta_time.cpu().numpy().astype(np.float64)
+        busy = ct[:, 1::2] - ct[:, 0::2]
+        per_layer = busy.max(axis=1) / busy.mean(axis=1)
+        skew[name] = {"max_over_mean_busy": float(per_layer.max()), "mean_over_layers": float(per_layer.mean()),
+                      "isolated_launch_us_mean": 1e3 * statistics.mean(ms)}
+    tg.tg_check_status(cache.status)
+    del uni
 
     # timed region: K steps, one event after every launch
     n_ev = args.steps * w.L + 1
@@ -361,8 +381,7 @@ def main():
         "pct_of_hbm_peak": 100.0 * gbs / peak,
         "retained_kv_tokens_per_s": all_tokens / (ms_step * 1e-3),
         "us_per_step": 1e3 * ms_step,
-        "cta_skew": {"max_over_mean_busy": float(skew_per_layer.max()),
-                     "mean_over_layers": float(skew_per_layer.mean()), "split": "static split map"},
+        "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
                      "kernel": "ragged_decode_kernel<128>",

@@ -72,16 +72,20 @@ struct KCfg<256> {
   static constexpr int NW = 4, R = 3;
 };
 
+constexpr int kMaxItems = 16;  // work items per CTA kept in shared memory (more are read from global)
+
 template <int D>
 struct Layout {
   static constexpr int NW = KCfg<D>::NW, R = KCfg<D>::R;
   static constexpr int TILE = 16 * D * 2;  // bytes of 16 rows of K (or V)
   static constexpr int STAGE = 2 * TILE;   // K tile then V tile
   static constexpr int RING = NW * R * STAGE;
-  static constexpr int OSTRIDE = D + 4;    // floats per (warp, head) row of the merge buffer
-  static int smem_bytes(int g) {
-    return 1024 + RING + NW * g * OSTRIDE * 4 + NW * 8 * 4 * 2 + NW * R * 8 + 16;
-  }
+  // small region at the start of dynamic shared memory (16-byte aligned base):
+  // mbarriers, item copies, page-table bases, per-warp (m, l), a flag
+  static constexpr int SMALL = NW * R * 8 + kMaxItems * (8 + (int)sizeof(tg_work_item)) + NW * 8 * 4 * 2 + 16;
+  // floats per (warp, head) row of the merge buffer: padded against bank conflicts when it fits
+  __host__ __device__ static int ostride(int g) { return g <= 4 ? D + 4 : D; }
+  static int smem_bytes(int g) { return SMALL + 1008 + RING + NW * g * ostride(g) * 4; }
 };
 
 // byte offset of element (row, col) of a TMA tile loaded as D/64 boxes of
@@ -104,14 +108,17 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
     ragged_decode_kernel(const __grid_constant__ CUtensorMap pool_map, const DecodeArgs a) {
   using LY = Layout<D>;
   constexpr int NW = LY::NW, R = LY::R, NT = NW * 32, KS = D / 16;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem;
-  float *comb_o = reinterpret_cast<float *>(smem + LY::RING);  // [NW][g][OSTRIDE]
-  float *comb_m = comb_o + NW * a.g * LY::OSTRIDE;              // [NW][8]
-  float *comb_l = comb_m + NW * 8;                              // [NW][8]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(comb_l + NW * 8);  // [NW][R]
-  int *flag = reinterpret_cast<int *>(bars + NW * R);
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);                   // [NW][R]
+  int64_t *s_base = reinterpret_cast<int64_t *>(bars + NW * R);              // [kMaxItems]
+  tg_work_item *s_items = reinterpret_cast<tg_work_item *>(s_base + kMaxItems);  // [kMaxItems]
+  float *comb_m = reinterpret_cast<float *>(s_items + kMaxItems);            // [NW][8]
+  float *comb_l = comb_m + NW * 8;                                           // [NW][8]
+  int *flag = reinterpret_cast<int *>(comb_l + NW * 8);
+  uint8_t *ring = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + LY::SMALL + 1023) & ~uintptr_t(1023));  // [NW][R][STAGE]
+  const int ostride = LY::ostride(a.g);
+  float *comb_o = reinterpret_cast<float *>(ring + LY::RING);                // [NW][g][ostride]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -119,62 +126,92 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   uint64_t t_start = 0;
   if (tid == 0) t_start = globaltimer_ns();
 
-  const int i_begin = a.cta_off[cta], i_end = a.cta_off[cta + 1];
+  // ---------------- this CTA's work items and their page-table bases, one parallel round trip
+  const int i_begin = a.cta_off[cta];
+  const int n_items = a.cta_off[cta + 1] - i_begin;
+  const bool items_in_smem = n_items <= kMaxItems;
+  if (items_in_smem) {
+    for (int i = tid; i < n_items; i += NT) {
+      const tg_work_item it = a.items[i_begin + i];
+      s_items[i] = it;
+      s_base[i] = a.pt_off[it.b * a.G + it.g];
+    }
+  }
   if (lane == 0) {
     for (int s = 0; s < R; ++s) mbar_init(&bars[warp * R + s], 1);
   }
   if (tid == 0) prefetch_tensormap(&pool_map);
   fence_barrier_init();
   __syncthreads();
+  auto get_item = [&](int i) -> tg_work_item { return items_in_smem ? s_items[i] : a.items[i_begin + i]; };
+  auto get_base = [&](int i, const tg_work_item &it) -> int64_t {
+    return items_in_smem ? s_base[i] : a.pt_off[it.b * a.G + it.g];
+  };
+  // tiles of item `it` that this warp takes: lo + warp, lo + warp + NW, ...
+  auto warp_tiles = [&](const tg_work_item &it, int &lo) -> int {
+    int hi;
+    item_tiles(it, lo, hi);
+    return hi - lo > warp ? (hi - lo - warp + NW - 1) / NW : 0;
+  };
+  int total_tiles = 0;
+  for (int i = 0; i < n_items; ++i) {
+    int lo;
+    total_tiles += warp_tiles(get_item(i), lo);
+  }
 
-  // ---------------- producer cursor: this warp's tiles across the CTA's items
-  int p_item = i_begin, p_k = 0, p_khi = 0, p_hpos = 0;
-  int64_t p_base = 0;
-  auto p_seek = [&](int from) {  // first item >= from in which this warp has a tile
-    for (p_item = from; p_item < i_end; ++p_item) {
-      const tg_work_item it = a.items[p_item];
-      int lo, hi;
-      item_tiles(it, lo, hi);
-      if (hi - lo > warp) {
-        p_k = lo + warp;
-        p_khi = hi;
-        p_hpos = it.hpos;
-        p_base = a.pt_off[it.b * a.G + it.g];
+  // ---------------- producer: page ids of the warp's tiles, 32 at a time, one per lane,
+  // loaded a batch ahead so no TMA issue waits on a global load
+  auto tile_info = [&](int n, int32_t &page, int &row_in_page) {
+    page = -1;
+    row_in_page = -1;
+    if (n >= total_tiles) return;
+    int rem = n;
+    for (int i = 0; i < n_items; ++i) {
+      const tg_work_item it = get_item(i);
+      int lo;
+      const int cnt = warp_tiles(it, lo);
+      if (rem < cnt) {
+        const int tok = 16 * (lo + warp + NW * rem);
+        page = a.pt_ids[get_base(i, it) + tok / a.P];
+        row_in_page = it.hpos * 2 * a.P + tok % a.P;  // first K row of the tile inside its page
         return;
       }
+      rem -= cnt;
     }
   };
-  auto p_advance = [&]() {
-    p_k += NW;
-    if (p_k >= p_khi) p_seek(p_item + 1);
-  };
+  int32_t pg_cur, pg_nxt;
+  int rw_cur, rw_nxt;
+  tile_info(lane, pg_cur, rw_cur);
+  tile_info(32 + lane, pg_nxt, rw_nxt);
   int issued = 0, consumed = 0;
-  auto issue = [&]() {  // lane 0: load tile p_k of the current producer item into stage issued % R
-    const int s = issued % R;
-    uint64_t *bar = &bars[warp * R + s];
-    uint8_t *dst = ring + (warp * R + s) * LY::STAGE;
-    const int tok = p_k * 16;
-    const int32_t page = a.pt_ids[p_base + tok / a.P];
-    if (page < 0 || (int64_t)page >= a.pool_pages) {
-      report(a.status, TG_STATUS_BAD_PAGE);
-      mbar_arrive(bar);  // complete the phase without data
-      return;
-    }
-    const int row_k = (int)(((int64_t)page * a.H_p + p_hpos) * 2 * a.P + (tok % a.P));
-    mbar_arrive_expect_tx(bar, LY::STAGE);
+  auto issue = [&]() {  // whole warp: tile number `issued` of this warp into stage issued % R
+    const int32_t page = __shfl_sync(0xffffffffu, pg_cur, issued & 31);
+    const int rip = __shfl_sync(0xffffffffu, rw_cur, issued & 31);
+    if (lane == 0) {
+      const int s = issued % R;
+      uint64_t *bar = &bars[warp * R + s];
+      uint8_t *dst = ring + (warp * R + s) * LY::STAGE;
+      if (page < 0 || (int64_t)page >= a.pool_pages || rip < 0) {
+        report(a.status, TG_STATUS_BAD_PAGE);
+        mbar_arrive(bar);  // complete the phase without data
+      } else {
+        const int row_k = (int)((int64_t)page * a.H_p * 2 * a.P + rip);
+        mbar_arrive_expect_tx(bar, LY::STAGE);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_2d(dst + c * 2048, &pool_map, bar, c * 64, row_k);
-      tma_load_2d(dst + LY::TILE + c * 2048, &pool_map, bar, c * 64, row_k + a.P);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_2d(dst + c * 2048, &pool_map, bar, c * 64, row_k);
+          tma_load_2d(dst + LY::TILE + c * 2048, &pool_map, bar, c * 64, row_k + a.P);
+        }
+      }
+    }
+    ++issued;
+    if ((issued & 31) == 0) {
+      pg_cur = pg_nxt;
+      rw_cur = rw_nxt;
+      tile_info(issued + 32 + lane, pg_nxt, rw_nxt);
     }
   };
-
-  p_seek(i_begin);
-  for (int s = 0; s < R && p_item < i_end; ++s) {
-    if (lane == 0) issue();
-    ++issued;
-    p_advance();
-  }
+  for (int s = 0; s < R && issued < total_tiles; ++s) issue();
 
   // ---------------- consumer state
   bool dead = false;  // a wait timed out: skip all further work, keep the barriers
@@ -182,19 +219,38 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   float o[KS][4];
 #pragma unroll
   for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  uint32_t qf[KS][2];
+  // query fragments (B operand of S^T = K Q^T): this item's, and the next item's in flight
+  uint32_t qf[KS][2], qn[KS][2];
+  auto load_q = [&](int i) {
+    if (i >= n_items) return;
+    const tg_work_item it = get_item(i);
+    const uint16_t *qrow = a.q + ((size_t)it.b * a.H_q + (size_t)it.h * a.g + gid) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qn[ks][0] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tig) : 0u;
+      qn[ks][1] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
+    }
+  };
+  auto next_item_with_tiles = [&](int from) {
+    for (int i = from; i < n_items; ++i) {
+      int lo;
+      if (warp_tiles(get_item(i), lo) > 0) return i;
+    }
+    return n_items;
+  };
+  load_q(next_item_with_tiles(0));
 
-  for (int ii = i_begin; ii < i_end; ++ii) {
-    const tg_work_item it = a.items[ii];
+  for (int ii = 0; ii < n_items; ++ii) {
+    const tg_work_item it = get_item(ii);
     int k_lo, k_hi;
     item_tiles(it, k_lo, k_hi);
     if (k_hi - k_lo > warp && !dead) {
-      const uint16_t *qrow = a.q + ((size_t)it.b * a.H_q + (size_t)it.h * a.g + gid) * D;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][0] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tig) : 0u;
-        qf[ks][1] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
+        qf[ks][0] = qn[ks][0];
+        qf[ks][1] = qn[ks][1];
       }
+      load_q(next_item_with_tiles(ii + 1));
       for (int kk = k_lo + warp; kk < k_hi; kk += NW) {
         const int s = consumed % R;
         bool ok = mbar_wait(&bars[warp * R + s], (uint32_t)((consumed / R) & 1), kWaitLimitNs);
@@ -250,13 +306,9 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
         }
         ++consumed;
         __syncwarp();
-        if (p_item < i_end) {
-          if (lane == 0) {
-            fence_proxy_async_smem();  // our ldmatrix reads of this stage come before the refill
-            issue();
-          }
-          ++issued;
-          p_advance();
+        if (issued < total_tiles) {
+          if (lane == 0) fence_proxy_async_smem();  // our ldmatrix reads of this stage come before the refill
+          issue();
         }
       }
     }
@@ -277,12 +329,12 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
 #pragma unroll
     for (int mb = 0; mb < KS; ++mb) {
       if (h0 < a.g) {
-        comb_o[(warp * a.g + h0) * LY::OSTRIDE + mb * 16 + gid] = o[mb][0];
-        comb_o[(warp * a.g + h0) * LY::OSTRIDE + mb * 16 + gid + 8] = o[mb][2];
+        comb_o[(warp * a.g + h0) * ostride + mb * 16 + gid] = o[mb][0];
+        comb_o[(warp * a.g + h0) * ostride + mb * 16 + gid + 8] = o[mb][2];
       }
       if (h1 < a.g) {
-        comb_o[(warp * a.g + h1) * LY::OSTRIDE + mb * 16 + gid] = o[mb][1];
-        comb_o[(warp * a.g + h1) * LY::OSTRIDE + mb * 16 + gid + 8] = o[mb][3];
+        comb_o[(warp * a.g + h1) * ostride + mb * 16 + gid] = o[mb][1];
+        comb_o[(warp * a.g + h1) * ostride + mb * 16 + gid + 8] = o[mb][3];
       }
       o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
     }
@@ -308,7 +360,7 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
         for (int w = 0; w < NW; ++w) {
           const float f = ex2(comb_m[w * 8 + hd] - M);
           Ls += comb_l[w * 8 + hd] * f;
-          O += comb_o[(w * a.g + hd) * LY::OSTRIDE + dd] * f;
+          O += comb_o[(w * a.g + hd) * ostride + dd] * f;
         }
         if (it.nparts == 1) {
           __nv_bfloat16 v = __float2bfloat16_rn(O / Ls);

@@ -38,7 +38,8 @@ def compare_out(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
     if rows is None:
         mask = ~np.isnan(lse_ref)
         diff = np.abs(o - out_ref)[mask]
-        ldiff = np.abs(l - lse_ref)[mask & np.isfinite(lse_ref)]
+        fin = mask & np.isfinite(lse_ref)
+        ldiff = np.abs(l[fin] - lse_ref[fin])
         assert np.array_equal(np.isneginf(l[mask]), np.isneginf(lse_ref[mask]))
     else:
         diff = np.concatenate([np.abs(o[b, j] - out_ref[b, j]) for b, j in rows])

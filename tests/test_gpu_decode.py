@@ -62,6 +62,15 @@ def test_small_gqa_widths(lib, cuda, g):
     _decode_and_check(lib, w, cuda, n_cta=24)
 
 
+@pytest.mark.parametrize("n_cta", [2, 3, 7])
+def test_many_items_per_cta(lib, cuda, n_cta):
+    """Few CTAs over many short runs: a CTA holds more work items than fit in shared memory."""
+    w = synth.small(batch=24, N=150, H=4, H_q=8, H_p=2, L=1)
+    cache, _ = _decode_and_check(lib, w, cuda, n_cta=n_cta)
+    off, _ = lib.plan_items(cache.plan, 0)
+    assert np.diff(off).max() > 16
+
+
 def test_small_d256(lib, cuda):
     w = synth.small(d=256, H=8, H_q=16, H_p=4, batch=2, N=640)
     _decode_and_check(lib, w, cuda, n_cta=20)
@@ -89,11 +98,17 @@ def test_uniform_split_gives_same_result(lib, cuda):
         s, K, V, _ = run_layer(lib, w, 0, cache, cuda)
         q = synth.queries(w, 0, cuda)
         out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
-        cache.decode_layer(0, q, out)
+        lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+        cache.decode_layer(0, q, out, lse)
+        ref_out, ref_lse, _ = oracle_layer(w, 0, s, K, V, q, cache.pages["ntok"][0], N)
+        compare_out(out, lse, ref_out, ref_lse)
         outs.append(out.float().cpu())
-    # different split points change float32 summation order only
-    assert (outs[0] - outs[1]).abs().max() < 4e-3
-    assert (outs[0] - outs[2]).abs().max() < 4e-3
+    # different split points change the float32 summation order and the running
+    # max that P is rounded to bf16 against; the difference is absolute (not
+    # relative to |out|), so it is held to the same bar as the oracle comparison
+    for o in outs[1:]:
+        diff = (outs[0] - o).abs()
+        assert diff.max() <= 1e-2 and diff.mean() <= 1e-3
 
 
 def test_config1_full(lib, cuda):
