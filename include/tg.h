@@ -249,6 +249,28 @@ int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n
                        const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
                        int32_t *dev_status);
 
+/* tg_decode_attn_static_scratch -- tg_decode_attn without a caller workspace.
+ *   The pages have no counterpart of this call: it exists for callers that
+ *   cannot allocate device memory at call time (a serving process whose own
+ *   allocator has reserved the GPU heap up front, a plug-in running inside a
+ *   host framework that owns all device memory).  It computes exactly what
+ *   tg_decode_attn computes and takes the same arguments except the workspace:
+ *   its scratch is a fixed 4 MiB array inside this library, present on every
+ *   GPU that loads the library until the process exits.  Nothing is allocated
+ *   (no cudaMalloc, no cudaFree, no allocating library call).
+ *   - Plans whose workspace_bytes exceed 4 MiB are rejected with
+ *     TG_ERR_CAPACITY (use tg_decode_attn with a workspace then).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Each call clears the array's counters and status word on `stream`
+ *     before the kernel.  All calls share the one array, so calls whose
+ *     kernels may overlap on the GPU (different streams or host threads) race
+ *     on it and must be serialised by the caller. */
+int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
+                                  const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
+                                  const int64_t *pt_off, const int32_t *pt_ids, float scale,
+                                  uint16_t *out, float *lse, int32_t *dev_status, int64_t *cta_time);
+
 /* tg_check_status -- synchronously read a device status word (waits for the
  *   device).  Returns TG_OK when it is 0, TG_ERR_TIMEOUT when TG_STATUS_TIMEOUT
  *   is set, TG_ERR_DEVICE for any other bit; *host_status (may be NULL) gets

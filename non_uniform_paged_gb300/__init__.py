@@ -19,7 +19,7 @@ import numpy as np
 from . import _build
 
 __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
-           "tg_decode_attn", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
+           "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
@@ -41,6 +41,7 @@ _SIGS = {
     "tg_query_ncta": (_I, [_I, _I, _P]),
     "tg_plan_decode": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P]),
     "tg_decode_attn": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _L, _P, _P, _P, _P]),
+    "tg_decode_attn_static_scratch": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _P, _P, _P]),
     "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]),
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -208,6 +209,26 @@ def tg_decode_attn(plan_host: np.ndarray, plan_dev, layer: int, q, pool, pool_pa
                               workspace.numel() * workspace.element_size(), _dev(out, torch.bfloat16, "out"),
                               _dev(lse, torch.float32, "lse"), _dev(dev_status, torch.int32, "dev_status"),
                               _dev(cta_time, torch.int64, "cta_time")))
+
+
+def tg_decode_attn_static_scratch(plan_host: np.ndarray, plan_dev, layer: int, q, pool, pool_pages: int, pt_off,
+                                  pt_ids, scale: float, out, lse=None, dev_status=None, cta_time=None, stream=None):
+    """tg_decode_attn for callers that cannot allocate device memory when they call it.
+
+    Same arguments and result as tg_decode_attn minus the workspace: the scratch
+    is a fixed 4 MiB array inside libtg (tg.h: tg_decode_attn_static_scratch).
+    Calls that may overlap on the GPU share that array and must be serialised.
+    """
+    import torch
+    lib = load()
+    if not (isinstance(plan_host, np.ndarray) and plan_host.dtype == np.uint8 and plan_host.flags.c_contiguous):
+        raise TypeError("plan_host must be the contiguous uint8 array from tg_plan_decode")
+    _check(lib.tg_decode_attn_static_scratch(
+        _stream(stream), plan_host.ctypes.data, _dev(plan_dev, torch.uint8, "plan_dev"), int(layer),
+        _dev(q, torch.bfloat16, "q"), _dev(pool, torch.bfloat16, "pool"), int(pool_pages),
+        _dev(pt_off, torch.int64, "pt_off"), _dev(pt_ids, torch.int32, "pt_ids"), float(scale),
+        _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"),
+        _dev(dev_status, torch.int32, "dev_status"), _dev(cta_time, torch.int64, "cta_time")))
 
 
 def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok, pt_off, pt_ids, pool_pages,

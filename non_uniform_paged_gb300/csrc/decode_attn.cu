@@ -547,6 +547,131 @@ extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const v
   return tgi::ok();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of tg_decode_attn.
+//
+// Some callers cannot allocate device memory when they call us: a serving
+// process whose allocator reserved all GPU memory up front, or a plug-in that
+// runs inside a host framework that owns the device heap, gets an error (or
+// breaks the host's memory accounting) from cudaMalloc at request time.  This
+// entry point takes its scratch (merge counters, status word, split-KV
+// partials) from the fixed array below instead of a caller workspace.
+//
+// The array lives in this library's module on every GPU that loads it, until
+// the process exits.  Its device address is looked up once per device with
+// cudaGetSymbolAddress, on that device's first call; make that first call
+// before any stream capture.  Every call shares the array: the counters and
+// the status word are cleared (cudaMemsetAsync) at the start of each call, and
+// calls that overlap on the GPU (two streams, two host threads) race on it.
+constexpr int64_t kStaticScratchBytes = 4 << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {nullptr};
+
+int static_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: device %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return TG_OK;
+}
+}  // namespace
+
+extern "C" int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, const void *plan_dev,
+                                             int layer, const uint16_t *q, const uint16_t *pool,
+                                             int64_t pool_pages, const int64_t *pt_off, const int32_t *pt_ids,
+                                             float scale, uint16_t *out, float *lse, int32_t *dev_status,
+                                             int64_t *cta_time) {
+  if (!plan_host || !plan_dev || !q || !pool || !pt_off || !pt_ids || !out)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: NULL pointer argument");
+  const tg_plan_header *hd = static_cast<const tg_plan_header *>(plan_host);
+  if (hd->magic != TG_PLAN_MAGIC || hd->version != 1)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: plan_host is not a tg_plan_decode buffer");
+  if (layer < 0 || layer >= hd->L)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: layer %d of %d", layer, hd->L);
+  if (hd->workspace_bytes > kStaticScratchBytes)
+    return tgi::fail(TG_ERR_CAPACITY,
+                     "tg_decode_attn_static_scratch: the plan needs %lld bytes of scratch, more than the fixed "
+                     "%lld-byte array; use tg_decode_attn with a caller workspace",
+                     (long long)hd->workspace_bytes, (long long)kStaticScratchBytes);
+  if (!std::isfinite(scale)) return tgi::fail(TG_ERR_NONFINITE, "tg_decode_attn_static_scratch: scale is not finite");
+  if ((reinterpret_cast<uintptr_t>(pool) & 15) || (reinterpret_cast<uintptr_t>(plan_dev) & 15) ||
+      (reinterpret_cast<uintptr_t>(q) & 3))
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: pool/plan must be 16-byte aligned");
+  const int64_t rows = pool_pages * hd->H_p * 2 * hd->P;
+  if (pool_pages <= 0 || rows > INT32_MAX)
+    return tgi::fail(TG_ERR_CAPACITY, "tg_decode_attn_static_scratch: pool_pages=%lld gives %lld rows",
+                     (long long)pool_pages, (long long)rows);
+  const int g = hd->H_q / hd->H;
+  void *fn;
+  int threads, smem;
+  int rc = kernel_config(hd->d, g, &fn, &threads, &smem);
+  if (rc) return rc;
+  void *scratch = nullptr;
+  rc = static_scratch_address(&scratch);
+  if (rc) return rc;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: cuTensorMapEncodeTiled is unavailable");
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)hd->d, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)hd->d * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), gdim, gstride, box,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS)
+    return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  const tg_plan_layer *lt =
+      reinterpret_cast<const tg_plan_layer *>(static_cast<const uint8_t *>(plan_host) + hd->layers) + layer;
+  const uint8_t *pd = static_cast<const uint8_t *>(plan_dev);
+  const tgi::WorkspaceLayout wl = tgi::workspace_layout(hd->batch, hd->H, g, hd->d, hd->max_slots);
+  uint8_t *ws = static_cast<uint8_t *>(scratch);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the merge counters and the fallback status word must start at zero
+  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)wl.ml, st);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: memset: %s", cudaGetErrorString(e));
+  DecodeArgs args;
+  args.items = reinterpret_cast<const tg_work_item *>(pd + lt->items);
+  args.cta_off = reinterpret_cast<const int32_t *>(pd + lt->cta_off);
+  args.q = q;
+  args.out = out;
+  args.lse = lse;
+  args.pt_off = pt_off;
+  args.pt_ids = pt_ids;
+  args.pool_pages = pool_pages;
+  args.counters = reinterpret_cast<int32_t *>(ws + wl.counters);
+  args.ws_ml = reinterpret_cast<float *>(ws + wl.ml);
+  args.ws_o = reinterpret_cast<float *>(ws + wl.o);
+  args.status = dev_status ? dev_status : reinterpret_cast<int32_t *>(ws + wl.status);
+  args.cta_time = cta_time;
+  args.H = hd->H;
+  args.H_q = hd->H_q;
+  args.g = g;
+  args.G = hd->G;
+  args.H_p = hd->H_p;
+  args.P = hd->P;
+  args.scale_log2 = scale * kLog2e;
+  void *params[] = {&map, &args};
+  e = cudaLaunchKernel(fn, dim3(hd->N_CTA), dim3(threads), params, (size_t)smem, st);
+  if (e != cudaSuccess)
+    return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: launch failed: %s", cudaGetErrorString(e));
+  return tgi::ok();
+}
+
 extern "C" int tg_check_status(const int32_t *dev_status, int32_t *host_status) {
   if (!dev_status) return tgi::fail(TG_ERR_INVALID_ARG, "tg_check_status: NULL");
   int32_t v = 0;
