@@ -202,47 +202,32 @@ def run_reference(args, rank, world, device):
 
 # ------------------------------------------------------------------ GPU arm
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload 1-3 (ragged decode); default 2")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs)")
-    ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
-    rank, world, local = dist_setup()
-    device = torch.device(f"cuda:{local}") if torch.cuda.is_available() else torch.device("cpu")
-    if args.impl == "reference":
-        run_reference(args, rank, world, device)
-        return
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: the GPU arm needs CUDA")
-    torch.cuda.set_device(device)
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
-    import non_uniform_paged_gb300 as tg
+
+def compact_bytes(cache, layer) -> int:
+    """Algorithmic bytes of tg_compact_topk on one layer: scores read, kept K/V rows read and
+    written, and the zero-filled tail rows of each head's last page."""
+    w_d, P = cache.d, cache.P
+    ntok = cache.pages["ntok"][layer]
+    scores = int(cache.N.astype(np.int64).sum()) * cache.H * 4
+    kept = int(ntok.astype(np.int64).sum()) * 2 * w_d * 2 * 2
+    tail = int(((-ntok) % P).astype(np.int64).sum()) * 2 * w_d * 2
+    return scores + kept + tail
+
+
+def build_cache(w, device, n_cta=None, uniform=False):
     from non_uniform_paged_gb300.ragged import RaggedCache
-
-    w = synth.workload(args.config)
-    if args.layers or args.batch:
-        w = w.replace(L=args.layers or w.L, batch=args.batch or w.batch,
-                      name=f"{w.name}-override-L{args.layers or w.L}-b{args.batch or w.batch}")
+    import non_uniform_paged_gb300 as tg
     Bhat = synth.budgets_hat(w)
     N = synth.contexts(w)
     t0 = time.perf_counter()
     cache = RaggedCache(w.L, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, Bhat, N, cluster=w.cluster,
-                        n_cta=w.n_cta, device=device)
+                        n_cta=n_cta or w.n_cta, uniform_split=uniform, device=device)
     plan_s = time.perf_counter() - t0
-
-    # prefill side: compact every layer's retained tokens into the pages (timed separately)
-    comp_ms = []
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    comp_ms, comp_bytes = [], []
+    ev0, ev1 = _events(2)
     for layer in range(w.L):
         s = synth.scores(w, layer, device)
         K, V = synth.keys_values(w, layer, device)
@@ -251,26 +236,20 @@ def main():
         ev1.record()
         ev1.synchronize()
         comp_ms.append(ev0.elapsed_time(ev1))
+        comp_bytes.append(compact_bytes(cache, layer))
         del s, K, V
     torch.cuda.synchronize()
     tg.tg_check_status(cache.status)
+    rows = {"plan_host_s": plan_s, "compact_topk_ms_per_layer": statistics.mean(comp_ms),
+            "compact_topk_gbs": sum(comp_bytes) / (sum(comp_ms) * 1e-3) / 1e9,
+            "pages": cache.n_pages, "pages_monolithic": cache.pages["n_pages_monolithic"]}
+    return cache, rows, N
 
-    q = torch.stack([synth.queries(w, l, device) for l in range(w.L)])        # [L][batch][H_q][d]
-    out = torch.empty((w.L, w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=device)
-    lse = torch.empty((w.L, w.batch, w.H_q), dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream()
 
-    def step():
-        for l in range(w.L):
-            cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    tg.tg_check_status(cache.status)
-
-    # CTA skew (max/mean CTA busy time) of isolated launches, static split map vs a
-    # uniform split of the CTAs over the groups (untimed; same pool, own plan)
+def cta_skew(w, cache, q, out, lse, stream, Bhat, N, device):
+    """Max/mean CTA busy time of isolated launches: static split map vs a uniform split."""
+    import non_uniform_paged_gb300 as tg
+    from non_uniform_paged_gb300.ragged import RaggedCache
     uni = RaggedCache(w.L, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, Bhat, N, cluster=w.cluster,
                       n_cta=cache.n_cta, uniform_split=True, device=device, alloc_pool=False)
     skew = {}
@@ -278,7 +257,7 @@ def main():
         cta_time = torch.zeros((w.L, 2 * c.n_cta), dtype=torch.int64, device=device)
         ms = []
         for l in range(w.L):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0, e1 = _events(2)
             torch.cuda.synchronize()
             e0.record(stream)
             c.decode_layer(l, q[l], out[l], lse[l], cta_time=cta_time[l], stream=stream, pool=cache.pool)
@@ -291,44 +270,92 @@ def main():
         skew[name] = {"max_over_mean_busy": float(per_layer.max()), "mean_over_layers": float(per_layer.mean()),
                       "isolated_launch_us_mean": 1e3 * statistics.mean(ms)}
     tg.tg_check_status(cache.status)
-    del uni
+    return skew, uni
 
-    # timed region: K steps, one event after every launch
-    n_ev = args.steps * w.L + 1
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+
+def bench_ragged(args, w, rank, world, local, device):
+    """Configs 1-3: one decode step = tg_decode_attn on every layer of a compacted ragged cache."""
+    import non_uniform_paged_gb300 as tg
+    cache, rows, N = build_cache(w, device)
+    Bhat = synth.budgets_hat(w)
+    q = torch.stack([synth.queries(w, l, device) for l in range(w.L)])        # [L][batch][H_q][d]
+    out = torch.empty((w.L, w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.L, w.batch, w.H_q), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    step_bytes = cache.algorithmic_bytes()
+    small = step_bytes < 4 * 129e6      # a whole step fits in L2: flush it between iterations
+
+    def step(c=cache):
+        for l in range(w.L):
+            c.decode_layer(l, q[l], out[l], lse[l], stream=stream, pool=cache.pool)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    tg.tg_check_status(cache.status)
+    skew, uni = cta_skew(w, cache, q, out, lse, stream, Bhat, N, device)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if small else None
+    n_ev = args.steps * (w.L + 1) if small else args.steps * w.L + 1
+    evs = _events(n_ev)
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    evs[0].record(stream)
-    k = 1
-    for _ in range(args.steps):
-        for l in range(w.L):
-            cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
+    launch_ms = []
+    if small:
+        # each iteration: write a buffer 4x the L2 size, then time the decode launches alone
+        k = 0
+        for _ in range(args.steps):
+            flush.fill_(1)
             evs[k].record(stream)
-            k += 1
-    torch.cuda.synchronize()
+            for l in range(w.L):
+                cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
+                evs[k + 1 + l].record(stream)
+            k += w.L + 1
+        torch.cuda.synchronize()
+        for it in range(args.steps):
+            base = it * (w.L + 1)
+            launch_ms += [evs[base + l].elapsed_time(evs[base + l + 1]) for l in range(w.L)]
+        total_ms = sum(launch_ms)
+    else:
+        evs[0].record(stream)
+        k = 1
+        for _ in range(args.steps):
+            for l in range(w.L):
+                cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
+                evs[k].record(stream)
+                k += 1
+        torch.cuda.synchronize()
+        total_ms = evs[0].elapsed_time(evs[-1])
+        launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n_ev - 1)]
     clk = clocks.stop()
     barrier(world)
-    total_ms = evs[0].elapsed_time(evs[-1])
-    launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n_ev - 1)]
     tg.tg_check_status(cache.status)
     ms_step = max_over_ranks(total_ms / args.steps, world, device)
 
-    step_bytes = cache.algorithmic_bytes()
+    # the same step under the uniform split (no flush; for the skew comparison)
+    u_steps = max(3, args.steps // 4)
+    a, b = _events(2)
+    a.record(stream)
+    for _ in range(u_steps):
+        step(uni)
+    b.record(stream)
+    torch.cuda.synchronize()
+    uniform_ms = a.elapsed_time(b) / u_steps
+    skew["uniform"]["ms_per_step_back_to_back"] = uniform_ms
+    del uni
+
     step_tokens = cache.retained_tokens()
     all_bytes = sum_over_ranks(step_bytes, world, device)
     all_tokens = sum_over_ranks(step_tokens, world, device)
     gbs = all_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
-
-    # roofline of the dominant (only) kernel: average bytes per launch / average launch duration
     bytes_per_launch = step_bytes / w.L
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
 
-    # e2e through the public API with host buffers: H2D of q, decode, D2H of out + lse every step
     e2e = None
     if not args.no_e2e:
         q_h = q.cpu().pin_memory()
@@ -346,7 +373,7 @@ def main():
             e2e_step()
         torch.cuda.synchronize()
         barrier(world)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = _events(2)
         a.record(stream)
         for _ in range(e_steps):
             e2e_step()
@@ -356,7 +383,8 @@ def main():
         e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, world, device)
         e2e = {"value": all_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": q.numel() * q.element_size(),
-               "d2h_bytes_per_step": out.numel() * out.element_size() + lse.numel() * lse.element_size()}
+               "d2h_bytes_per_step": out.numel() * out.element_size() + lse.numel() * lse.element_size(),
+               "l2": "no flush (host copies inside the step)"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -365,35 +393,228 @@ def main():
                "tokens_per_s": nt / secs,
                "sample": f"{heads} random (layer, request, KV head) runs of this workload, "
                          f"{nt} retained tokens, {secs:.1f} s of float64 numpy attention on one core"}
-
     if rank != 0:
         return
     realised_rho = step_tokens / (w.L * w.batch * w.H * float(np.mean(N)))
+    l2 = (f"L2 flushed before every timed iteration (512 MB write); each step reads {step_bytes / 1e6:.1f} MB"
+          if small else f"no flush: each launch reads {bytes_per_launch / 1e6:.0f} MB, each step "
+                        f"{step_bytes / 1e9:.1f} GB, both far above the 129 MB L2")
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "layers": w.L, "batch": w.batch, "context": int(w.N), "H_q": w.H_q,
                    "H_kv": w.H, "head_dim": w.d, "page": w.P, "H_p": w.H_p, "alpha": w.alpha,
-                   "clustering": w.cluster, "realised_retention": realised_rho, "n_cta": cache.n_cta,
-                   "l2": f"no flush: each launch reads {bytes_per_launch / 1e6:.0f} MB, each step "
-                         f"{step_bytes / 1e9:.1f} GB, both far above the 129 MB L2"},
+                   "clustering": w.cluster, "realised_retention": realised_rho, "n_cta": cache.n_cta, "l2": l2},
         "pct_of_hbm_peak": 100.0 * gbs / peak,
         "retained_kv_tokens_per_s": all_tokens / (ms_step * 1e-3),
         "us_per_step": 1e3 * ms_step,
         "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "ragged_decode_kernel<128>",
+                     "kernel": f"ragged_decode_kernel<{w.d}>",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": 1e3 * avg_launch_ms},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * w.L,
         "clocks": clk,
-        "rows": {"plan_host_s": plan_s, "compact_topk_ms_per_layer": statistics.mean(comp_ms),
-                 "pages": cache.n_pages, "pages_monolithic": cache.pages["n_pages_monolithic"]},
+        "rows": rows,
     }
     print(json.dumps(line), flush=True)
+
+
+def bench_sparse(args, w, rank, world, local, device):
+    """Config 4: per layer, Quest page score + top-K (tg_page_score_topk) then decode over the
+    selected pages (tg_decode_attn), for each K; and dense decode over all pages."""
+    import non_uniform_paged_gb300 as tg
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    P, n_pages = w.P, w.N // w.P
+    pools, mms = [], []
+    for layer in range(w.L):
+        K, V = synth.keys_values(w, layer, device)
+        mms.append(build_minmax(K, P))
+        pools.append(torch.stack([K.view(w.batch, w.H, n_pages, P, w.d), V.view(w.batch, w.H, n_pages, P, w.d)],
+                                 dim=3).contiguous())
+        del K, V
+    q = torch.stack([synth.queries(w, l, device) for l in range(w.L)])
+    out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = peaks()
+    results = {}
+    for K_sel in list(w.topk_pages) + [n_pages]:
+        dec = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K_sel, device=device)
+        dense = K_sel == n_pages
+        if dense:  # all pages, no scoring: the page lists are every page of each head
+            dec.pt_ids.copy_(torch.arange(w.batch * w.H * n_pages, dtype=torch.int32, device=device))
+
+        def step():
+            for l in range(w.L):
+                if not dense:
+                    dec.select(q[l], mms[l], stream=stream)
+                dec.attend(q[l], pools[l], out, stream=stream)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        tg.tg_check_status(dec.status)
+        steps = max(3, args.steps // 10)
+        # per-kernel durations: events around every launch
+        evs = _events(steps * w.L * 3)
+        k = 0
+        for _ in range(steps):
+            for l in range(w.L):
+                evs[k].record(stream)
+                if not dense:
+                    dec.select(q[l], mms[l], stream=stream)
+                evs[k + 1].record(stream)
+                dec.attend(q[l], pools[l], out, stream=stream)
+                evs[k + 2].record(stream)
+                k += 3
+        torch.cuda.synchronize()
+        sel_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(0, k, 3)]
+        att_ms = [evs[i + 1].elapsed_time(evs[i + 2]) for i in range(0, k, 3)]
+        a, b = _events(2)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_step = a.elapsed_time(b) / steps
+        mm_bytes = 0 if dense else w.batch * w.H * n_pages * 2 * w.d * 2
+        kv_bytes = w.batch * w.H * K_sel * P * 2 * w.d * 2 + w.batch * w.H * K_sel * 4 + 2 * w.batch * w.H_q * w.d * 2
+        step_bytes = w.L * (mm_bytes + kv_bytes)
+        results["dense" if dense else f"K{K_sel}"] = {
+            "ms_per_step": ms_step, "gbs": step_bytes / (ms_step * 1e-3) / 1e9,
+            "pct_of_hbm_peak": 100 * step_bytes / (ms_step * 1e-3) / 1e9 / peak,
+            "score_topk_us": 1e3 * statistics.mean(sel_ms) if not dense else 0.0,
+            "score_topk_gbs": (mm_bytes / (statistics.mean(sel_ms) * 1e-3) / 1e9) if not dense else None,
+            "decode_us": 1e3 * statistics.mean(att_ms),
+            "decode_gbs": kv_bytes / (statistics.mean(att_ms) * 1e-3) / 1e9,
+            "bytes_per_step": step_bytes}
+        del dec
+    if rank != 0:
+        return
+    best = results[f"K{w.topk_pages[0]}"]
+    line = {"metric": METRIC, "value": best["gbs"], "unit": "GB/s", "n_gpus": world, "steps": args.steps // 10,
+            "warmup": args.warmup, "ms_per_step": best["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.L, "batch": w.batch, "context": w.N, "pages": n_pages,
+                       "topk_pages": list(w.topk_pages), "l2": "no flush: MinMax 102 MB + selected K/V per layer, "
+                                                            "52 GB dense cache rotated over 32 layers"},
+            "pct_of_hbm_peak": best["pct_of_hbm_peak"],
+            "sparse_vs_dense_speedup": {k: results["dense"]["ms_per_step"] / v["ms_per_step"]
+                                        for k, v in results.items() if k != "dense"},
+            "variants": results, "peak": peak, "peak_kind": peak_kind}
+    print(json.dumps(line), flush=True)
+
+
+def bench_layerwise(args, w, rank, world, local, device):
+    """Config 5 (d=256, ~220 GB of pages in total): one layer resident at a time.  For each
+    H_p, every layer is compacted into a one-layer pool and its decode launch is timed; the
+    step time is the sum over layers."""
+    import non_uniform_paged_gb300 as tg
+    from non_uniform_paged_gb300.ragged import RaggedCache
+    Bhat_all = synth.budgets_hat(w)
+    N = synth.contexts(w)
+    layers = range(w.L if not args.layers else args.layers)
+    peak, peak_kind = peaks()
+    sweep = {}
+    for H_p in (1, 2, 4, 8):
+        wl = w.replace(H_p=H_p)
+        total_ms, total_bytes, pages, mono, skews = 0.0, 0, 0, 0, []
+        pool = None
+        for layer in layers:
+            c = RaggedCache(1, wl.batch, wl.H, wl.H_q, wl.d, wl.P, H_p, wl.alpha, Bhat_all[layer:layer + 1], N,
+                            cluster=wl.cluster, device=device, alloc_pool=False)
+            need = c.n_pages * H_p * 2 * wl.P * wl.d
+            if pool is None or pool.numel() < need:
+                del pool
+                torch.cuda.empty_cache()
+                pool = torch.empty(int(need * 1.1), dtype=torch.bfloat16, device=device)
+            c.pool = pool
+            s = synth.scores(wl, layer, device)
+            K, V = synth.keys_values(wl, layer, device)
+            c.compact_layer(0, s, K, V)
+            del s, K, V
+            q = synth.queries(wl, layer, device)
+            out = torch.empty((wl.batch, wl.H_q, wl.d), dtype=torch.bfloat16, device=device)
+            for _ in range(args.warmup):
+                c.decode_layer(0, q, out)
+            reps = 5
+            ct = torch.zeros(2 * c.n_cta, dtype=torch.int64, device=device)
+            a, b = _events(2)
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                c.decode_layer(0, q, out)
+            b.record()
+            torch.cuda.synchronize()
+            c.decode_layer(0, q, out, cta_time=ct)
+            torch.cuda.synchronize()
+            tg.tg_check_status(c.status)
+            ctn = ct.cpu().numpy().astype(np.float64)
+            busy = ctn[1::2] - ctn[0::2]
+            skews.append(busy.max() / busy.mean())
+            total_ms += a.elapsed_time(b) / reps
+            total_bytes += c.algorithmic_bytes()
+            pages += c.n_pages
+            mono += c.pages["n_pages_monolithic"]
+        scale = w.L / len(layers)
+        sweep[f"H_p={H_p}"] = {"ms_per_step": total_ms * scale, "gbs": total_bytes / (total_ms * 1e-3) / 1e9,
+                               "pct_of_hbm_peak": 100 * total_bytes / (total_ms * 1e-3) / 1e9 / peak,
+                               "pool_gb": pages * H_p * 2 * w.P * w.d * 2 * scale / 1e9,
+                               "monolithic_pool_gb": mono * w.H * 2 * w.P * w.d * 2 * scale / 1e9,
+                               "cta_skew_max": float(max(skews)), "cta_skew_mean": float(np.mean(skews)),
+                               "layers_timed": len(layers)}
+        del pool
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return
+    main_v = sweep["H_p=4"]
+    line = {"metric": METRIC, "value": main_v["gbs"], "unit": "GB/s", "n_gpus": world, "steps": 5,
+            "warmup": args.warmup, "ms_per_step": main_v["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.L, "batch": w.batch, "head_dim": w.d, "alpha": w.alpha,
+                       "clustering": True, "timing": "one layer resident at a time; per-layer launches summed",
+                       "l2": "no flush: each launch reads several GB"},
+            "pct_of_hbm_peak": main_v["pct_of_hbm_peak"], "H_p_sweep": sweep, "peak": peak, "peak_kind": peak_kind}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload 1-5; default 2 (the headline)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    device = torch.device(f"cuda:{local}") if torch.cuda.is_available() else torch.device("cpu")
+    if args.impl == "reference":
+        run_reference(args, rank, world, device)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: the GPU arm needs CUDA")
+    torch.cuda.set_device(device)
+    w = synth.workload(args.config)
+    if args.config == 5:
+        bench_layerwise(args, w, rank, world, local, device)
+        return
+    if args.layers or args.batch:
+        w = w.replace(L=args.layers or w.L, batch=args.batch or w.batch,
+                      name=f"{w.name}-override-L{args.layers or w.L}-b{args.batch or w.batch}")
+    if args.config == 4:
+        bench_sparse(args, w, rank, world, local, device)
+    else:
+        bench_ragged(args, w, rank, world, local, device)
 
 
 if __name__ == "__main__":
