@@ -194,7 +194,13 @@ int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, int d, int 
  *   out   device bf16 [batch][H_q][d];  lse device float32 [batch][H_q] (may be NULL)
  *   dev_status device int32, OR-ed with TG_STATUS_* (may be NULL)
  *   cta_time device int64 [2*N_CTA] (may be NULL): %globaltimer ns at each
- *         CTA's start and end, for CTA skew = max/mean of (end - start). */
+ *         CTA's start and end, for CTA skew = max/mean of (end - start).
+ * Launch: programmatic dependent launch.  The kernel lets the next kernel in
+ *   the stream start as its CTAs finish, and it may itself start while the
+ *   previous tg_decode_attn launch in the stream is finishing: before waiting
+ *   for that launch it reads the plan, page tables, pool and q (never written
+ *   by a decode launch); it waits before it touches the workspace, out or lse.
+ *   Kernels other than tg_decode_attn complete before it starts, as usual. */
 int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
                    const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
                    const int64_t *pt_off, const int32_t *pt_ids, float scale,

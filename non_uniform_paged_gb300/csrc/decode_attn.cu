@@ -126,6 +126,10 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   uint64_t t_start = 0;
   if (tid == 0) t_start = globaltimer_ns();
 
+  // the next kernel in the stream may start as this grid's CTAs finish (programmatic
+  // dependent launch); it waits for this grid before touching shared workspace or outputs
+  griddep_launch_dependents();
+
   // ---------------- this CTA's work items and their page-table bases, one parallel round trip
   const int i_begin = a.cta_off[cta];
   const int n_items = a.cta_off[cta + 1] - i_begin;
@@ -312,6 +316,10 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
         }
       }
     }
+
+    // the workspace (merge counters, partials) and the outputs may still be in use by
+    // the previous decode launch in the stream: wait for it before the first write
+    if (ii == 0) griddep_wait();
 
     // ---- merge the warps' states of this item in shared memory
 #pragma unroll
@@ -541,8 +549,17 @@ extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const v
   // without a caller status word, faults are recorded in the workspace's own
   if (!dev_status) args.status = reinterpret_cast<int32_t *>(ws + wl.status);
   void *params[] = {&map, &args};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(hd->N_CTA), dim3(threads), params, (size_t)smem,
-                                   reinterpret_cast<cudaStream_t>(stream));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(hd->N_CTA);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, params);
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn: launch failed: %s", cudaGetErrorString(e));
   return tgi::ok();
 }

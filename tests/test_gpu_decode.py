@@ -149,3 +149,26 @@ def test_bad_page_id_is_reported(lib, cuda):
     with pytest.raises(lib.TGError):
         lib.tg_check_status(cache.status)
     assert int(cache.status.item()) & lib.STATUS_BAD_PAGE
+
+
+def test_back_to_back_layers_overlap_safely(lib, cuda):
+    """All layers launched back to back with no host sync, twice: consecutive launches
+    overlap (programmatic dependent launch) and share one workspace, and every layer's
+    output still matches the oracle."""
+    w = synth.small(L=6, batch=3, N=900, H=8, H_q=32, H_p=4)
+    cache, N = _cache(lib, w, cuda, n_cta=64)
+    inputs = [run_layer(lib, w, l, cache, cuda) for l in range(w.L)]
+    q = torch.stack([synth.queries(w, l, cuda) for l in range(w.L)])
+    out = torch.empty((w.L, w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((w.L, w.batch, w.H_q), dtype=torch.float32, device=cuda)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        for l in range(w.L):
+            cache.decode_layer(l, q[l], out[l], lse[l])
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(cache.status) == 0
+        for l in range(w.L):
+            s, K, V, _ = inputs[l]
+            ref_out, ref_lse, _ = oracle_layer(w, l, s, K, V, q[l], cache.pages["ntok"][l], N)
+            compare_out(out[l], lse[l], ref_out, ref_lse)
