@@ -48,9 +48,17 @@ __device__ __forceinline__ void block_radix_select(int count, int k, GetKey get,
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < count; i += NT) {
-      const uint32_t key = get(i);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    // histogram of the next digit among keys that match the prefix so far; lanes of a
+    // warp with the same digit add once (the leading digits of real scores coincide)
+    for (int base = 0; base < count; base += NT) {
+      const int i = base + threadIdx.x;
+      uint32_t dg = 256u;  // no digit
+      if (i < count) {
+        const uint32_t key = get(i);
+        if ((key & mask) == prefix) dg = (key >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+      if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
     }
     __syncthreads();
     if (warp == 0) {

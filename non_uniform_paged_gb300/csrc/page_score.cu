@@ -29,8 +29,17 @@ namespace {
 
 using namespace tgk;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kMaxPages = 16384;
+constexpr int kChunkPages = 32;                      // pages per bulk copy
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // give up a copy wait after 2 s
+
+template <int D>
+struct ScoreCfg {
+  static constexpr int NS = D == 256 ? 3 : 4;        // ring stages
+  static constexpr int CHUNK = kChunkPages * 2 * D * 2;  // bytes per stage
+  static int smem_bytes(int n_pages) { return NS * CHUNK + NS * 8 + n_pages * 4; }
+};
 
 struct ScoreArgs {
   const uint16_t *q, *minmax;
@@ -41,90 +50,207 @@ struct ScoreArgs {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// One CTA per (request, KV head).  Thread 0 streams the row's MinMax vectors
+// (contiguous, n_pages x 2 x d bf16) through an NS-stage shared-memory ring with
+// 1-D bulk copies; every half warp scores pages out of shared memory.
 template <int D, int GQ>
-__global__ void __launch_bounds__(kThreads) page_score_topk_kernel(const ScoreArgs a) {
-  constexpr int W = D / 16;      // elements per slice
-  constexpr int WV = W / 8;      // 16-byte vectors per slice
-  constexpr int NWARP = kThreads / 32;
-  constexpr int kUnroll = D == 256 ? 2 : 4;  // pages per half warp in flight (register budget)
-  extern __shared__ uint32_t keys[];  // [n_pages]
+__global__ void __launch_bounds__(kThreads, 3) page_score_topk_kernel(const ScoreArgs a) {
+  using CF = ScoreCfg<D>;
+  constexpr int W = D / 16;  // elements per slice
+  constexpr int WV = W / 8;  // 16-byte vectors per slice
+  constexpr int NS = CF::NS, CHUNK = CF::CHUNK;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *ring = smem;                                           // [NS][CHUNK]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NS * CHUNK);  // [NS]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(bars + NS);        // [n_pages]
   __shared__ int hist[256];
   __shared__ int scan[33];
   __shared__ int sel_scratch[4];
   __shared__ int nan_flag;
 
   const int row = blockIdx.x, b = row / a.H, h = row % a.H;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int half = lane >> 4, j = lane & 15;
-  if (threadIdx.x == 0) nan_flag = 0;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int hw = tid >> 4, j = lane & 15;  // half warp 0..15, slice j
+  if (tid == 0) {
+    nan_flag = 0;
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+  }
+  fence_barrier_init();
+  __syncthreads();
+
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(a.minmax + (size_t)row * a.n_pages * 2 * D);
+  const int nc = (a.n_pages + kChunkPages - 1) / kChunkPages;
+  auto chunk_bytes = [&](int c) { return min(kChunkPages, a.n_pages - c * kChunkPages) * 2 * D * 2; };
+  auto issue = [&](int c) {  // thread 0
+    uint64_t *bar = &bars[c % NS];
+    mbar_arrive_expect_tx(bar, (uint32_t)chunk_bytes(c));
+    bulk_load(ring + (c % NS) * CHUNK, src + (size_t)c * CHUNK, (uint32_t)chunk_bytes(c), bar);
+  };
+  if (tid == 0)
+    for (int c = 0; c < NS && c < nc; ++c) issue(c);
 
   // this lane's slice of the g query heads (heads past g contribute nothing)
   uint32_t qv[GQ][W / 2];
 #pragma unroll
   for (int i = 0; i < GQ; ++i) {
     const int qi = i < a.g ? i : 0;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.H * a.g + (size_t)h * a.g + qi) * D + j * W);
+    const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.H * a.g + (size_t)h * a.g + qi) * D + j * W);
 #pragma unroll
     for (int v = 0; v < WV; ++v) {
-      const uint4 x = src[v];
+      const uint4 x = qs[v];
       qv[i][4 * v] = x.x; qv[i][4 * v + 1] = x.y; qv[i][4 * v + 2] = x.z; qv[i][4 * v + 3] = x.w;
     }
   }
-  __syncthreads();
 
-  const uint16_t *mm_row = a.minmax + (size_t)row * a.n_pages * 2 * D;
+  // q+ = max(q, 0) and q- = min(q, 0) of this lane's slice, as float32, when they fit in registers
+  constexpr bool kSplitQ = GQ * W <= 32;
+  float qp[kSplitQ ? GQ : 1][kSplitQ ? W : 1], qm[kSplitQ ? GQ : 1][kSplitQ ? W : 1];
+  if constexpr (kSplitQ) {
+#pragma unroll
+    for (int i = 0; i < GQ; ++i)
+#pragma unroll
+      for (int e = 0; e < W; e += 2) {
+        const float lo = bf16_lo(qv[i][e / 2]), hi = bf16_hi(qv[i][e / 2]);
+        qp[i][e] = fmaxf(lo, 0.f);
+        qm[i][e] = fminf(lo, 0.f);
+        qp[i][e + 1] = fmaxf(hi, 0.f);
+        qm[i][e + 1] = fminf(hi, 0.f);
+      }
+  }
+
   bool nan_seen = false;
-  // the loop bound is the warp's base page so both halves iterate together (shuffles below)
-  for (int base = warp * 2; base < a.n_pages; base += NWARP * 2 * kUnroll) {
-    const int p0 = base + half;
-    uint4 mnv[kUnroll][WV], mxv[kUnroll][WV];
+  int c = 0;
+  bool failed = false;
+  for (; c < nc; ++c) {
+    const int s = c % NS;
+    const bool ok = mbar_wait(&bars[s], (uint32_t)((c / NS) & 1), kWaitLimitNs);
+    const int np = min(kChunkPages, a.n_pages - c * kChunkPages);
+    const uint8_t *stage = ring + s * CHUNK;
+    if constexpr (kSplitQ) {
+      // this half warp scores pages hw and hw + 16 of the chunk together (two independent
+      // sets of accumulator chains); pages past np read stale shared memory and are dropped
+      const int pa = hw, pb = hw + 16;
+      const uint4 *ra = reinterpret_cast<const uint4 *>(stage + pa * 4 * D + j * W * 2);
+      const uint4 *rb = reinterpret_cast<const uint4 *>(stage + pb * 4 * D + j * W * 2);
+      uint4 mna[WV], mxa[WV], mnb[WV], mxb[WV];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int p = p0 + u * NWARP * 2;
-      for (int v = 0; v < WV; ++v) mnv[u][v] = mxv[u][v] = make_uint4(0, 0, 0, 0);
-      if (p < a.n_pages) {
-        const uint4 *mn = reinterpret_cast<const uint4 *>(mm_row + (size_t)p * 2 * D + j * W);
-        const uint4 *mx = reinterpret_cast<const uint4 *>(mm_row + (size_t)p * 2 * D + D + j * W);
+      for (int v = 0; v < WV; ++v) {
+        mna[v] = ra[v];
+        mxa[v] = ra[v + D / 8];  // the max row follows the min row: 2*D bytes = D/8 vectors
+        mnb[v] = rb[v];
+        mxb[v] = rb[v + D / 8];
+      }
+      // e_d = max(q_d mn_d, q_d mx_d) = q+_d mx_d + q-_d mn_d (mn <= mx, one product is 0):
+      // two FMAs per element add exactly what mul-max-add adds, in the same order
+      float acca[GQ], accb[GQ];
 #pragma unroll
-        for (int v = 0; v < WV; ++v) {
-          mnv[u][v] = __ldcs(mn + v);
-          mxv[u][v] = __ldcs(mx + v);
+      for (int i = 0; i < GQ; ++i) acca[i] = accb[i] = 0.f;
+#pragma unroll
+      for (int v = 0; v < WV; ++v) {
+        const uint32_t wna[4] = {mna[v].x, mna[v].y, mna[v].z, mna[v].w};
+        const uint32_t wxa[4] = {mxa[v].x, mxa[v].y, mxa[v].z, mxa[v].w};
+        const uint32_t wnb[4] = {mnb[v].x, mnb[v].y, mnb[v].z, mnb[v].w};
+        const uint32_t wxb[4] = {mxb[v].x, mxb[v].y, mxb[v].z, mxb[v].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int el = 8 * v + 2 * e;
+          const float na0 = bf16_lo(wna[e]), na1 = bf16_hi(wna[e]), xa0 = bf16_lo(wxa[e]), xa1 = bf16_hi(wxa[e]);
+          const float nb0 = bf16_lo(wnb[e]), nb1 = bf16_hi(wnb[e]), xb0 = bf16_lo(wxb[e]), xb1 = bf16_hi(wxb[e]);
+#pragma unroll
+          for (int i = 0; i < GQ; ++i) {
+            acca[i] = fmaf(qp[i][el], xa0, acca[i]);
+            accb[i] = fmaf(qp[i][el], xb0, accb[i]);
+            acca[i] = fmaf(qm[i][el], na0, acca[i]);
+            accb[i] = fmaf(qm[i][el], nb0, accb[i]);
+            acca[i] = fmaf(qp[i][el + 1], xa1, acca[i]);
+            accb[i] = fmaf(qp[i][el + 1], xb1, accb[i]);
+            acca[i] = fmaf(qm[i][el + 1], na1, acca[i]);
+            accb[i] = fmaf(qm[i][el + 1], nb1, accb[i]);
+          }
         }
       }
-    }
+      float besta = -INFINITY, bestb = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int p = p0 + u * NWARP * 2;  // uniform within the half warp
+      for (int i = 0; i < GQ; ++i) {
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+          acca[i] = __fadd_rn(acca[i], __shfl_xor_sync(0xffffffffu, acca[i], off));
+          accb[i] = __fadd_rn(accb[i], __shfl_xor_sync(0xffffffffu, accb[i], off));
+        }
+        if (i < a.g) {
+          besta = i == 0 ? acca[i] : fmaxf(besta, acca[i]);
+          bestb = i == 0 ? accb[i] : fmaxf(bestb, accb[i]);
+        }
+      }
+      if (j == 0 && ok) {
+        if (pa < np) {
+          nan_seen |= is_nan(besta);
+          keys[c * kChunkPages + pa] = float_key(besta);
+        }
+        if (pb < np) {
+          nan_seen |= is_nan(bestb);
+          keys[c * kChunkPages + pb] = float_key(bestb);
+        }
+      }
+    } else {
+#pragma unroll
+    for (int pl0 = 0; pl0 < kChunkPages; pl0 += 16) {  // both halves of a warp take 2 pages each
+      const int pl = pl0 + hw;
+      const bool valid = ok && pl < np;
+      uint4 mnv[WV], mxv[WV];
+#pragma unroll
+      for (int v = 0; v < WV; ++v) {
+        mnv[v] = valid ? reinterpret_cast<const uint4 *>(stage + pl * 4 * D + j * W * 2)[v] : make_uint4(0, 0, 0, 0);
+        mxv[v] = valid ? reinterpret_cast<const uint4 *>(stage + pl * 4 * D + 2 * D + j * W * 2)[v] : make_uint4(0, 0, 0, 0);
+      }
       float best = -INFINITY;
 #pragma unroll
       for (int i = 0; i < GQ; ++i) {
         float acc = 0.f;
 #pragma unroll
         for (int v = 0; v < WV; ++v) {
-          const uint32_t mnw[4] = {mnv[u][v].x, mnv[u][v].y, mnv[u][v].z, mnv[u][v].w};
-          const uint32_t mxw[4] = {mxv[u][v].x, mxv[u][v].y, mxv[u][v].z, mxv[u][v].w};
+          const uint32_t mnw[4] = {mnv[v].x, mnv[v].y, mnv[v].z, mnv[v].w};
+          const uint32_t mxw[4] = {mxv[v].x, mxv[v].y, mxv[v].z, mxv[v].w};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t qq = qv[i][4 * v + c];
-            const float e_lo = fmaxf(__fmul_rn(bf16_lo(qq), bf16_lo(mnw[c])), __fmul_rn(bf16_lo(qq), bf16_lo(mxw[c])));
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t qq = qv[i][4 * v + e];
+            const float e_lo = fmaxf(__fmul_rn(bf16_lo(qq), bf16_lo(mnw[e])), __fmul_rn(bf16_lo(qq), bf16_lo(mxw[e])));
             acc = __fadd_rn(acc, e_lo);
-            const float e_hi = fmaxf(__fmul_rn(bf16_hi(qq), bf16_hi(mnw[c])), __fmul_rn(bf16_hi(qq), bf16_hi(mxw[c])));
+            const float e_hi = fmaxf(__fmul_rn(bf16_hi(qq), bf16_hi(mnw[e])), __fmul_rn(bf16_hi(qq), bf16_hi(mxw[e])));
             acc = __fadd_rn(acc, e_hi);
           }
         }
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
         if (i < a.g) {
-          nan_seen |= is_nan(acc);
+          nan_seen |= valid && is_nan(acc);
           best = i == 0 ? acc : fmaxf(best, acc);
         }
       }
-      if (j == 0 && p < a.n_pages) keys[p] = float_key(best);
+      if (j == 0 && valid) keys[c * kChunkPages + pl] = float_key(best);
     }
+    }
+    // every thread is done with stage s; thread 0 refills it
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    if (tid == 0 && c + NS < nc) {
+      fence_proxy_async_smem();
+      issue(c + NS);
+    }
+  }
+  if (failed) {  // a copy wait gave up: report, drain our own copies in flight, leave
+    if (tid == 0) {
+      report(a.status, TG_STATUS_TIMEOUT);
+      for (int t = c; t < nc && t < c + NS; ++t)
+        if (!mbar_wait(&bars[t % NS], (uint32_t)((t / NS) & 1), kWaitLimitNs)) break;
+    }
+    return;
   }
   if (nan_seen) nan_flag = 1;
   __syncthreads();
-  if (nan_flag && threadIdx.x == 0) report(a.status, TG_STATUS_NONFINITE);
+  if (nan_flag && tid == 0) report(a.status, TG_STATUS_NONFINITE);
 
   uint32_t T;
   int need_eq;
@@ -132,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) page_score_topk_kernel(const ScoreAr
 
   int taken = 0, eq_seen = 0;
   for (int c0 = 0; c0 < a.n_pages && taken < a.K; c0 += kThreads) {
-    const int p = c0 + threadIdx.x;
+    const int p = c0 + tid;
     const uint32_t key = p < a.n_pages ? keys[p] : 0u;
     const bool gt = p < a.n_pages && key > T, eq = p < a.n_pages && key == T;
     int eq_total, sel_total;
@@ -151,10 +277,10 @@ __global__ void __launch_bounds__(kThreads) page_score_topk_kernel(const ScoreAr
 template <int D, int GQ>
 cudaError_t launch_score(const ScoreArgs &a, int rows, cudaStream_t s) {
   auto fn = page_score_topk_kernel<D, GQ>;
-  const int smem = a.n_pages * 4;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxPages * 4);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ScoreCfg<D>::smem_bytes(kMaxPages));
   if (e != cudaSuccess) return e;
-  fn<<<rows, kThreads, smem, s>>>(a);
+  fn<<<rows, kThreads, ScoreCfg<D>::smem_bytes(a.n_pages), s>>>(a);
   return cudaGetLastError();
 }
 
