@@ -392,21 +392,64 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
         __syncthreads();
         if (*flag) {  // the last CTA of this run merges every partial
           __threadfence();
-          for (int e = tid; e < a.g * D; e += NT) {
-            const int hd = e / D, dd = e % D;
-            float M = -INFINITY;
-            for (int p = 0; p < it.nparts; ++p)
-              M = fmaxf(M, __ldcg(&a.ws_ml[((size_t)(it.slot0 + p) * a.g + hd) * 2]));
-            float Ls = 0.f, O = 0.f;
-            for (int p = 0; p < it.nparts; ++p) {
-              const size_t sp = (size_t)(it.slot0 + p) * a.g + hd;
-              const float f = ex2(__ldcg(&a.ws_ml[sp * 2]) - M);
-              Ls += __ldcg(&a.ws_ml[sp * 2 + 1]) * f;
-              O += __ldcg(&a.ws_o[sp * D + dd]) * f;
+          const int np = it.nparts, g = a.g;
+          const float *pml = a.ws_ml + (size_t)it.slot0 * g * 2;  // [nparts][g][2]
+          const float *po = a.ws_o + (size_t)it.slot0 * g * D;     // [nparts][g][D]
+          if (np <= NW * ostride) {
+            // factors 2^(m_p - M) of every part go to the (now free) merge buffer; per head,
+            // one warp gathers M and L with its lanes striding over the parts (independent loads)
+            float *fac = comb_o;  // [nparts][g]
+            for (int hh = warp; hh < g; hh += NW) {
+              float M = -INFINITY;
+              for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(pml + ((size_t)p * g + hh) * 2));
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+              float Ls = 0.f;
+              for (int p = lane; p < np; p += 32) {
+                const float f = ex2(__ldcg(pml + ((size_t)p * g + hh) * 2) - M);
+                fac[p * g + hh] = f;
+                Ls += __ldcg(pml + ((size_t)p * g + hh) * 2 + 1) * f;
+              }
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+              if (lane == 0) {
+                comb_m[hh] = M;
+                comb_l[hh] = Ls;
+              }
             }
-            __nv_bfloat16 v = __float2bfloat16_rn(O / Ls);
-            a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
-            if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (M + log2f(Ls)) * kLn2;
+            __syncthreads();
+            // O = sum_p o_p 2^(m_p - M), parts in order, eight loads in flight per thread
+            for (int e = tid; e < g * D; e += NT) {
+              const int hd = e / D, dd = e % D;
+              float O = 0.f;
+              int p = 0;
+              for (; p + 8 <= np; p += 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(p + u) * g * D + e);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) O += v[u] * fac[(p + u) * g + hd];
+              }
+              for (; p < np; ++p) O += __ldcg(po + (size_t)p * g * D + e) * fac[p * g + hd];
+              __nv_bfloat16 v = __float2bfloat16_rn(O / comb_l[hd]);
+              a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
+              if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (comb_m[hd] + log2f(comb_l[hd])) * kLn2;
+            }
+          } else {  // more parts than the buffer holds factors for: straight loops
+            for (int e = tid; e < g * D; e += NT) {
+              const int hd = e / D, dd = e % D;
+              float M = -INFINITY;
+              for (int p = 0; p < np; ++p) M = fmaxf(M, __ldcg(pml + ((size_t)p * g + hd) * 2));
+              float Ls = 0.f, O = 0.f;
+              for (int p = 0; p < np; ++p) {
+                const float f = ex2(__ldcg(pml + ((size_t)p * g + hd) * 2) - M);
+                Ls += __ldcg(pml + ((size_t)p * g + hd) * 2 + 1) * f;
+                O += __ldcg(po + (size_t)p * g * D + e) * f;
+              }
+              __nv_bfloat16 v = __float2bfloat16_rn(O / Ls);
+              a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
+              if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (M + log2f(Ls)) * kLn2;
+            }
           }
           if (tid == 0) atomicExch(&a.counters[it.b * a.H + it.h], 0);
         }

@@ -172,3 +172,13 @@ def test_back_to_back_layers_overlap_safely(lib, cuda):
             s, K, V, _ = inputs[l]
             ref_out, ref_lse, _ = oracle_layer(w, l, s, K, V, q[l], cache.pages["ntok"][l], N)
             compare_out(out[l], lse[l], ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("n_cta", [300, 8000])
+def test_runs_split_into_very_many_parts(lib, cuda, n_cta):
+    """One run shared by hundreds (fast merge) or thousands (fallback merge) of CTAs."""
+    w = synth.small(L=1, batch=1, H=4, H_q=8, H_p=2, N=2500, ctx_dist="fixed",
+                    budget_dist="ones", budget_args=())
+    cache, _ = _decode_and_check(lib, w, cuda, n_cta=n_cta)
+    _, items = lib.plan_items(cache.plan, 0)
+    assert items["nparts"].max() > (1056 if n_cta == 8000 else 50)
