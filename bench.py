@@ -285,9 +285,9 @@ def bench_ragged(args, w, rank, world, local, device):
     step_bytes = cache.algorithmic_bytes()
     small = step_bytes < 4 * 129e6      # a whole step fits in L2: flush it between iterations
 
-    def step(c=cache):
+    def step(c=cache, st=None):
         for l in range(w.L):
-            c.decode_layer(l, q[l], out[l], lse[l], stream=stream, pool=cache.pool)
+            c.decode_layer(l, q[l], out[l], lse[l], stream=st or torch.cuda.current_stream(), pool=cache.pool)
 
     for _ in range(args.warmup):
         step()
@@ -297,7 +297,8 @@ def bench_ragged(args, w, rank, world, local, device):
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device) if small else None
     n_ev = args.steps * (w.L + 1) if small else 2
-    evs = _events(n_ev)
+    # events recorded inside a captured graph must be 'external' to become timing nodes
+    evs = [torch.cuda.Event(enable_timing=True, external=small) for _ in range(n_ev)]
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -305,15 +306,27 @@ def bench_ragged(args, w, rank, world, local, device):
     time.sleep(0.3)
     launch_ms = []
     if small:
-        # each iteration: write a buffer 4x the L2 size, then time the decode launches alone
-        k = 0
-        for _ in range(args.steps):
-            flush.fill_(1)
-            evs[k].record(stream)
-            for l in range(w.L):
-                cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
-                evs[k + 1 + l].record(stream)
-            k += w.L + 1
+        # each iteration: write a buffer 4x the L2 size, then time the decode launches alone.
+        # The iterations are captured in one CUDA graph and replayed, so the device time of a
+        # launch is not stretched by the host's submission latency (tens of us per call).
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                flush.fill_(1)
+                step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            k = 0
+            for _ in range(args.steps):
+                flush.fill_(1)
+                evs[k].record(side)
+                for l in range(w.L):
+                    cache.decode_layer(l, q[l], out[l], lse[l], stream=side)
+                    evs[k + 1 + l].record(side)
+                k += w.L + 1
+        graph.replay()
         torch.cuda.synchronize()
         for it in range(args.steps):
             base = it * (w.L + 1)
@@ -397,7 +410,8 @@ def bench_ragged(args, w, rank, world, local, device):
     if rank != 0:
         return
     realised_rho = step_tokens / (w.L * w.batch * w.H * float(np.mean(N)))
-    l2 = (f"L2 flushed before every timed iteration (512 MB write); each step reads {step_bytes / 1e6:.1f} MB"
+    l2 = (f"L2 flushed before every timed iteration (512 MB write); each step reads {step_bytes / 1e6:.1f} MB; "
+          f"iterations replayed from one CUDA graph, each decode launch timed by its own event pair"
           if small else f"no flush: each launch reads {bytes_per_launch / 1e6:.0f} MB, each step "
                         f"{step_bytes / 1e9:.1f} GB, both far above the 129 MB L2")
     line = {
