@@ -6,28 +6,33 @@
 // ready) and 3.2 Ragged Paging (each H_p-head group writes into its own pages
 // of H_p x 2 x P x d elements).
 //
-// One CTA per (request, KV head) row:
+// C CTAs per (request, KV head) row (C chosen so the grid fills the GPU); CTA j
+// owns tokens [j N / C, (j+1) N / C) and talks to no other CTA:
 //  1. exact top-n by an MSB-first radix select over order-preserving keys of
-//     the float32 scores (cached in shared memory when they fit), giving the
-//     n-th largest key T and how many keys equal to T to keep;
-//  2. one ascending sweep that keeps key > T, plus the lowest-indexed keys
-//     equal to T, numbers them with a block scan and copies their K and V rows
-//     (16-byte vector loads/stores, one row per 16-thread group at d=128) to
-//     page k/P, row k%P of the head's block inside its group page;
-//  3. zero-fills the rows of the head's last page past n, so a decode kernel
-//     may read whole tiles.
+//     the float32 scores (every CTA of the row finds the same n-th largest key
+//     T and how many keys equal to T to keep; the scores stay in L2);
+//  2. block-wide counts of the kept keys before its chunk give the chunk's
+//     first output position;
+//  3. one ascending sweep of its chunk keeps key > T, plus the lowest-indexed
+//     keys equal to T, numbers them with a block scan and copies their K and V
+//     rows (16-byte vectors) to page k/P, row k%P of the head's block inside
+//     its group page;
+//  4. the row's last CTA zero-fills the rows of the head's last page past n,
+//     so a decode kernel may read whole tiles.
 #include "block_select.cuh"
 #include "ptx.cuh"
 #include "tg_internal.h"
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 namespace {
 
 using namespace tgk;
 
 constexpr int kThreads = 1024;
-constexpr int kSmemKeys = 40960;  // rows up to this length keep their keys in shared memory
+constexpr int kSmemKeys = 24576;  // rows up to this length keep their keys in shared memory (2 CTAs/SM)
 
 struct CompactArgs {
   const int32_t *N;
@@ -41,9 +46,10 @@ struct CompactArgs {
   int32_t *kept_idx;
   int32_t *status;
   int H, H_p, G, P, d, Nmax;
+  int parts;  // CTAs per row
 };
 
-__global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const CompactArgs a) {
   extern __shared__ uint32_t cache[];  // kSmemKeys keys when the row fits, else unused
   __shared__ int hist[256];
   __shared__ int scan[33];
@@ -51,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
   __shared__ int tok_list[kThreads];
   __shared__ int err_flag;
 
-  const int row = blockIdx.x, b = row / a.H, h = row % a.H;
+  const int row = blockIdx.x / a.parts, part = blockIdx.x % a.parts, b = row / a.H, h = row % a.H;
   const int Nb = a.N[b], n = a.ntok[row];
   if (threadIdx.x == 0) err_flag = 0;
   __syncthreads();
@@ -90,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
   }
   if (nan_seen) err_flag = 1;
   __syncthreads();
-  if (err_flag && threadIdx.x == 0) report(a.status, TG_STATUS_NONFINITE);
+  if (err_flag && threadIdx.x == 0 && part == 0) report(a.status, TG_STATUS_NONFINITE);
   auto key_of = [&](int t) -> uint32_t { return cached ? cache[t] : float_key(srow[t]); };
 
   uint32_t T;
@@ -99,11 +105,20 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
 
   const int d16 = a.d / 8;  // 16-byte chunks per row
   const size_t src_row0 = (size_t)row * a.Nmax;
-  int taken = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < Nb && taken < n; c0 += kThreads) {
+  const int c_begin = (int)((int64_t)part * Nb / a.parts), c_end = (int)((int64_t)(part + 1) * Nb / a.parts);
+  // keys kept before this chunk: all of them above T, and the first need_eq equal to T
+  int gt_before = 0, eq_before = 0;
+  for (int c0 = 0; c0 < c_begin; c0 += kThreads) {
     const int t = c0 + threadIdx.x;
-    const uint32_t key = t < Nb ? key_of(t) : 0u;
-    const bool gt = t < Nb && key > T, eq = t < Nb && key == T;
+    const uint32_t key = t < c_begin ? key_of(t) : 0u;
+    gt_before += __syncthreads_count(t < c_begin && key > T);
+    eq_before += __syncthreads_count(t < c_begin && key == T);
+  }
+  int taken = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
+  for (int c0 = c_begin; c0 < c_end && taken < n; c0 += kThreads) {
+    const int t = c0 + threadIdx.x;
+    const uint32_t key = t < c_end ? key_of(t) : 0u;
+    const bool gt = t < c_end && key > T, eq = t < c_end && key == T;
     int eq_total, sel_total;
     const int eq_rank = eq_seen + block_excl_count<kThreads>(eq, scan, eq_total);
     const bool sel = gt || (eq && eq_rank < need_eq);
@@ -133,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
 
   // zero the rows of the last page past n (K and V blocks)
   const int rem = n % a.P;
-  if (rem) {
+  if (rem && part == a.parts - 1) {
     const int32_t page = a.pt_ids[base + (n - 1) / a.P];
     if (page >= 0 && (int64_t)page < a.pool_pages) {
       const int rows = a.P - rem;
@@ -167,9 +182,20 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   a.pt_off = pt_off; a.pt_ids = pt_ids; a.pool_pages = pool_pages; a.pool = pool; a.kept_idx = kept_idx;
   a.status = dev_status; a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
   const int smem = (Nmax <= kSmemKeys ? Nmax : 0) * (int)sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
   if (e == cudaSuccess) {
-    compact_topk_kernel<<<batch * H, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    // enough CTAs per row for about two resident 1024-thread CTAs per SM, at most 16,
+    // and chunks of at least 2048 tokens
+    const int rows = batch * H;
+    int parts = (2 * sms + rows - 1) / rows;
+    parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
+    a.parts = parts;
+    const int64_t grid = (int64_t)rows * parts;
+    if (grid > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
+    compact_topk_kernel<<<(unsigned)grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: %s", cudaGetErrorString(e));
