@@ -35,6 +35,23 @@ METRIC = "decode-attn achieved HBM GB/s (% of GB300 peak) and retained KV tokens
 FALLBACK_HBM_GBS = 6800.0
 
 
+def decode_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, while the kernel
+    sources are unchanged since the capture (else None)."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", "ragged_decode_cfg2_dram.md")).read()
+        vals = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("traffic_", "kernel_")))
+        h = hashlib.sha256()
+        for f in ("non_uniform_paged_gb300/csrc/decode_attn.cu", "non_uniform_paged_gb300/csrc/ptx.cuh"):
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != vals["kernel_sources_sha256"].strip():
+            return None
+        return float(vals["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -426,7 +443,10 @@ def bench_ragged(args, w, rank, world, local, device):
         "us_per_step": 1e3 * ms_step,
         "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak,
+                     "traffic": decode_traffic() if w.name == synth.workload(2).name else None,
+                     "traffic_source": "profiles/ragged_decode_cfg2_dram.md (ncu, full size)",
+                     "peak_kind": peak_kind,
                      "kernel": f"ragged_decode_kernel<{w.d}>",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": 1e3 * avg_launch_ms},
         "cpu_baseline": cpu,
