@@ -244,16 +244,30 @@ int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d,
  *   score(b,h,p) = max over the g query heads j of sum_d max(q_jd mn_pd, q_jd mx_pd).
  * Reading: float32 arithmetic in one fixed order (d cut into 16 slices summed
  *   left to right, then partial sums added pairwise (j, j+8), (j, j+4), (j, j+2),
- *   (j, j+1)); ties to the lower page; output ascending.  NaN -> TG_STATUS_NONFINITE.
+ *   (j, j+1)); ties to the lower page; output ascending.  A NaN sum in any
+ *   query head sets TG_STATUS_NONFINITE (the selection is then unspecified).
  * Arguments (device): q bf16 [batch][H*g][d]; minmax bf16 [batch][H][n_pages][2][d];
  *   sel int32 [batch][H][K] (output, page indices 0..n_pages-1);
  *   pt_ids int32 [batch][H][K] (output, may be NULL): (b*H + h)*n_pages + sel,
  *   i.e. the ids of the selected pages in a dense pool [batch][H][n_pages] of
- *   H_p = 1 pages, ready as the page lists of tg_decode_attn.
- *   Host sizes: d in {128, 256}, 1 <= g <= 8, 1 <= K <= n_pages <= 16384. */
+ *   H_p = 1 pages, ready as the page lists of tg_decode_attn;
+ *   workspace: scratch of at least tg_page_score_workspace bytes (the page
+ *   scores); no initial contents needed; one call at a time per workspace.
+ *   q, minmax and workspace 16-byte aligned.
+ *   Host sizes: d in {128, 256}, 1 <= g <= 8, 1 <= K <= n_pages <= 16384.
+ * Launch: two kernels (scores over all pages, then one top-K per head), both
+ *   with programmatic dependent launch: the first may start while the previous
+ *   kernel in the stream (a tg_decode_attn of the previous layer) finishes,
+ *   reading q and minmax and writing only the workspace; it completes only after
+ *   that kernel.  The second waits for the first, writes sel and pt_ids, and
+ *   does not let the next kernel start early. */
 int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                        const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
-                       int32_t *dev_status);
+                       void *workspace, int64_t workspace_bytes, int32_t *dev_status);
+
+/* tg_page_score_workspace -- bytes of workspace tg_page_score_topk needs for
+ *   batch x H rows of n_pages pages (host only). */
+int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *workspace_bytes);
 
 /* tg_decode_attn_static_scratch -- tg_decode_attn without a caller workspace.
  *   The pages have no counterpart of this call: it exists for callers that

@@ -20,6 +20,7 @@ from . import _build
 
 __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
+           "tg_page_score_workspace",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
@@ -44,7 +45,8 @@ _SIGS = {
     "tg_decode_attn_static_scratch": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _P, _P, _P]),
     "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]),
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
-    "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P]),
+    "tg_page_score_workspace": (_I, [_I, _I, _I, _P]),
     "tg_check_status": (_I, [_P, _P]),
 }
 
@@ -253,13 +255,28 @@ def tg_build_minmax(batch, H, N, P, d, K, minmax, dev_status=None, stream=None):
                                _dev(minmax, torch.bfloat16, "minmax"), _dev(dev_status, torch.int32, "dev_status")))
 
 
-def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, dev_status=None, stream=None):
-    """Quest page bound + per-KV-head top-K pages (tg.h: tg_page_score_topk)."""
+def tg_page_score_workspace(batch, H, n_pages) -> int:
+    """Workspace bytes tg_page_score_topk needs (tg.h: tg_page_score_workspace)."""
+    lib = load()
+    v = ctypes.c_int64(0)
+    _check(lib.tg_page_score_workspace(batch, H, n_pages, ctypes.addressof(v)))
+    return v.value
+
+
+def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, workspace=None, dev_status=None,
+                       stream=None):
+    """Quest page bound + per-KV-head top-K pages (tg.h: tg_page_score_topk).  Without a
+    workspace, one of tg_page_score_workspace bytes is allocated for the call."""
     import torch
     lib = load()
+    need = tg_page_score_workspace(batch, H, n_pages)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(lib.tg_page_score_topk(_stream(stream), batch, H, g, d, n_pages, K, _dev(q, torch.bfloat16, "q"),
                                   _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
-                                  _dev(pt_ids, torch.int32, "pt_ids"), _dev(dev_status, torch.int32, "dev_status")))
+                                  _dev(pt_ids, torch.int32, "pt_ids"), _dev(workspace, torch.uint8, "workspace"),
+                                  workspace.numel() * workspace.element_size(),
+                                  _dev(dev_status, torch.int32, "dev_status")))
 
 
 def tg_check_status(dev_status) -> int:

@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   // dependent launch); it waits for this grid before touching shared workspace or outputs
   griddep_launch_dependents();
 
-  // ---------------- this CTA's work items and their page-table bases, one parallel round trip
+  // ---------------- this CTA's work items and their page-table bases, one parallel round trip.
+  // Page tables and q are read from L2 (ld.global.cg): the kernel before this one in the
+  // stream may have written them just before this grid started
   const int i_begin = a.cta_off[cta];
   const int n_items = a.cta_off[cta + 1] - i_begin;
   const bool items_in_smem = n_items <= kMaxItems;
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
     for (int i = tid; i < n_items; i += NT) {
       const tg_work_item it = a.items[i_begin + i];
       s_items[i] = it;
-      s_base[i] = a.pt_off[it.b * a.G + it.g];
+      s_base[i] = __ldcg(a.pt_off + it.b * a.G + it.g);
     }
   }
   if (lane == 0) {
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   __syncthreads();
   auto get_item = [&](int i) -> tg_work_item { return items_in_smem ? s_items[i] : a.items[i_begin + i]; };
   auto get_base = [&](int i, const tg_work_item &it) -> int64_t {
-    return items_in_smem ? s_base[i] : a.pt_off[it.b * a.G + it.g];
+    return items_in_smem ? s_base[i] : __ldcg(a.pt_off + it.b * a.G + it.g);
   };
   // tiles of item `it` that this warp takes: lo + warp, lo + warp + NW, ...
   auto warp_tiles = [&](const tg_work_item &it, int &lo) -> int {
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
       const int cnt = warp_tiles(it, lo);
       if (rem < cnt) {
         const int tok = 16 * (lo + warp + NW * rem);
-        page = a.pt_ids[get_base(i, it) + tok / a.P];
+        page = __ldcg(a.pt_ids + get_base(i, it) + tok / a.P);
         row_in_page = it.hpos * 2 * a.P + tok % a.P;  // first K row of the tile inside its page
         return;
       }
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
     const uint16_t *qrow = a.q + ((size_t)it.b * a.H_q + (size_t)it.h * a.g + gid) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qn[ks][0] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tig) : 0u;
-      qn[ks][1] = gid < a.g ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
+      qn[ks][0] = gid < a.g ? __ldcg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 2 * tig)) : 0u;
+      qn[ks][1] = gid < a.g ? __ldcg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
   };
   auto next_item_with_tiles = [&](int from) {

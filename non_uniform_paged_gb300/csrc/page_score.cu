@@ -11,285 +11,505 @@
 // Score of page p for KV head h: max over its g query heads j of
 //   sum_d max(q_jd * mn_pd, q_jd * mx_pd)
 // in float32, in one fixed order so the selection is reproducible: d is cut
-// into 16 slices of d/16, each summed left to right by one lane of a 16-lane
-// half warp; the 16 lane sums are then added by xor-shuffles 8, 4, 2, 1, i.e.
-// pairs (j, j+8), (j, j+4), (j, j+2), (j, j+1).  bf16 x bf16 products are exact
-// in float32 and no multiply is fused into an add.
+// into 16 slices of d/16, each summed left to right; the 16 slice sums are then
+// added pairwise (j, j+8), (j, j+4), (j, j+2), (j, j+1).  bf16 x bf16 products
+// are exact in float32, and since mn <= mx exactly one of q+ mx and q- mn is
+// nonzero (q+ = max(q, 0), q- = min(q, 0)), so two fused multiply-adds per
+// element add exactly what multiply-max-add adds.
 //
-// One CTA per (request, KV head): scores of all pages go to shared memory as
-// order-preserving keys, then an exact radix select finds the K-th largest
-// and an ascending sweep lists the winners (ties to the lower page).
+// Two kernels per call:
+//  * page_score_kernel: the (request, KV head, page) units of the whole call
+//    form one flat sequence (the MinMax rows are contiguous), split evenly over
+//    one persistent CTA per SM and, inside it, over its warps.  Each warp
+//    streams its contiguous range through its own ring of 1-D bulk copies; each
+//    half warp scores two pages at once, lane j owning slice j, with the two
+//    pages' chains packed into f32x2 FMAs.  The 16 slice sums are combined by an
+//    xor butterfly that also spreads the g heads over the lanes (every add is
+//    one of the fixed pairs; a + b == b + a in float32).  Scores go to the
+//    workspace as order-preserving keys.
+//  * page_select_warp_kernel (rows of up to 1024 pages: one warp per (request,
+//    KV head), keys in registers) or page_select_kernel (longer rows: one CTA,
+//    keys in shared memory): an exact radix select of the K-th largest key, then
+//    an ascending sweep (ties to the lower page).
 #include "block_select.cuh"
 #include "ptx.cuh"
 #include "tg_internal.h"
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 namespace {
 
 using namespace tgk;
 
-constexpr int kThreads = 256;
-constexpr int kMaxPages = 16384;
-constexpr int kChunkPages = 32;                      // pages per bulk copy
-constexpr uint64_t kWaitLimitNs = 2000000000ull;     // give up a copy wait after 2 s
+constexpr int kMaxPages = 16384;                  // pages per (request, KV head) the select holds
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up a copy wait after 2 s
+constexpr int kSelThreads = 256;
 
 template <int D>
 struct ScoreCfg {
-  static constexpr int NS = D == 256 ? 3 : 4;        // ring stages
-  static constexpr int CHUNK = kChunkPages * 2 * D * 2;  // bytes per stage
-  static int smem_bytes(int n_pages) { return NS * CHUNK + NS * 8 + n_pages * 4; }
+  static constexpr int NW = 8;                   // warps per CTA
+  static constexpr int PAGE = 4 * D;             // bytes of one page: min row, then max row (bf16)
+  static constexpr int SP = D == 128 ? 8 : 4;    // pages per stage; a half warp scores SP/2 of them
+  static constexpr int PPL = SP / 2;             // pages per lane (stage pages hw, hw+2, hw+4, ...)
+  static constexpr int R = 4;                    // stages per warp
+  static constexpr int STAGE = SP * PAGE;        // 4 KB
+  static constexpr int RING = NW * R * STAGE;    // 128 KB
+  static constexpr int SMEM = RING + NW * R * 8;
 };
 
 struct ScoreArgs {
   const uint16_t *q, *minmax;
-  int32_t *sel, *pt_ids, *status;
-  int H, g, n_pages, K;
+  uint32_t *keys;
+  int32_t *status;
+  int64_t units;  // rows * n_pages
+  int g, n_pages;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// One CTA per (request, KV head).  Thread 0 streams the row's MinMax vectors
-// (contiguous, n_pages x 2 x d bf16) through an NS-stage shared-memory ring with
-// 1-D bulk copies; every half warp scores pages out of shared memory.
-template <int D, int GQ>
-__global__ void __launch_bounds__(kThreads, 3) page_score_topk_kernel(const ScoreArgs a) {
-  using CF = ScoreCfg<D>;
-  constexpr int W = D / 16;  // elements per slice
-  constexpr int WV = W / 8;  // 16-byte vectors per slice
-  constexpr int NS = CF::NS, CHUNK = CF::CHUNK;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *ring = smem;                                           // [NS][CHUNK]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NS * CHUNK);  // [NS]
-  uint32_t *keys = reinterpret_cast<uint32_t *>(bars + NS);        // [n_pages]
-  __shared__ int hist[256];
-  __shared__ int scan[33];
-  __shared__ int sel_scratch[4];
-  __shared__ int nan_flag;
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &x, float &y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+// two independent IEEE fused multiply-adds, round to nearest: d.x = a.x b.x + d.x, d.y = a.y b.y + d.y
+__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
 
-  const int row = blockIdx.x, b = row / a.H, h = row % a.H;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int hw = tid >> 4, j = lane & 15;  // half warp 0..15, slice j
-  if (tid == 0) {
-    nan_flag = 0;
-    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
-  }
-  fence_barrier_init();
-  __syncthreads();
+__host__ __device__ constexpr int log2c(int n) { return n <= 1 ? 0 : 1 + log2c(n / 2); }
 
-  const uint8_t *src = reinterpret_cast<const uint8_t *>(a.minmax + (size_t)row * a.n_pages * 2 * D);
-  const int nc = (a.n_pages + kChunkPages - 1) / kChunkPages;
-  auto chunk_bytes = [&](int c) { return min(kChunkPages, a.n_pages - c * kChunkPages) * 2 * D * 2; };
-  auto issue = [&](int c) {  // thread 0
-    uint64_t *bar = &bars[c % NS];
-    mbar_arrive_expect_tx(bar, (uint32_t)chunk_bytes(c));
-    bulk_load(ring + (c % NS) * CHUNK, src + (size_t)c * CHUNK, (uint32_t)chunk_bytes(c), bar);
-  };
-  if (tid == 0)
-    for (int c = 0; c < NS && c < nc; ++c) issue(c);
-
-  // this lane's slice of the g query heads (heads past g contribute nothing)
-  uint32_t qv[GQ][W / 2];
+// Add the 16 slice sums of NV values over the 16 lanes of a half warp (lane j = slice j)
+// in the fixed pair order: xor levels 8, 4, 2, 1 add the pairs (j, j^o).  While a lane
+// holds more than one value, each level also halves what it keeps: it keeps one half of
+// its values, sends the other half to its partner and adds the partner's copy of the half
+// it kept (a + b == b + a in float32, so both lanes of a pair add the same two numbers).
+// After min(4, log2 NV) such levels the lane holds NV >> LS values, value r being number
+// base + r where base = sum over split levels k of (bit 8>>k of the lane) * NV >> (k+1).
+template <int NV>
+__device__ __forceinline__ void transpose_sum(float (&v)[NV], int lane) {
+  constexpr int LS = log2c(NV) < 4 ? log2c(NV) : 4;
 #pragma unroll
-  for (int i = 0; i < GQ; ++i) {
-    const int qi = i < a.g ? i : 0;
-    const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * a.H * a.g + (size_t)h * a.g + qi) * D + j * W);
+  for (int k = 0; k < 4; ++k) {
+    const int o = 8 >> k;
+    if (k < LS) {
+      const int h = NV >> (k + 1);
+      const bool up = lane & o;
 #pragma unroll
-    for (int v = 0; v < WV; ++v) {
-      const uint4 x = qs[v];
-      qv[i][4 * v] = x.x; qv[i][4 * v + 1] = x.y; qv[i][4 * v + 2] = x.z; qv[i][4 * v + 3] = x.w;
-    }
-  }
-
-  // q+ = max(q, 0) and q- = min(q, 0) of this lane's slice, as float32, when they fit in registers
-  constexpr bool kSplitQ = GQ * W <= 32;
-  float qp[kSplitQ ? GQ : 1][kSplitQ ? W : 1], qm[kSplitQ ? GQ : 1][kSplitQ ? W : 1];
-  if constexpr (kSplitQ) {
-#pragma unroll
-    for (int i = 0; i < GQ; ++i)
-#pragma unroll
-      for (int e = 0; e < W; e += 2) {
-        const float lo = bf16_lo(qv[i][e / 2]), hi = bf16_hi(qv[i][e / 2]);
-        qp[i][e] = fmaxf(lo, 0.f);
-        qm[i][e] = fminf(lo, 0.f);
-        qp[i][e + 1] = fmaxf(hi, 0.f);
-        qm[i][e + 1] = fminf(hi, 0.f);
-      }
-  }
-
-  bool nan_seen = false;
-  int c = 0;
-  bool failed = false;
-  for (; c < nc; ++c) {
-    const int s = c % NS;
-    const bool ok = mbar_wait(&bars[s], (uint32_t)((c / NS) & 1), kWaitLimitNs);
-    const int np = min(kChunkPages, a.n_pages - c * kChunkPages);
-    const uint8_t *stage = ring + s * CHUNK;
-    if constexpr (kSplitQ) {
-      // this half warp scores pages hw and hw + 16 of the chunk together (two independent
-      // sets of accumulator chains); pages past np read stale shared memory and are dropped
-      const int pa = hw, pb = hw + 16;
-      const uint4 *ra = reinterpret_cast<const uint4 *>(stage + pa * 4 * D + j * W * 2);
-      const uint4 *rb = reinterpret_cast<const uint4 *>(stage + pb * 4 * D + j * W * 2);
-      uint4 mna[WV], mxa[WV], mnb[WV], mxb[WV];
-#pragma unroll
-      for (int v = 0; v < WV; ++v) {
-        mna[v] = ra[v];
-        mxa[v] = ra[v + D / 8];  // the max row follows the min row: 2*D bytes = D/8 vectors
-        mnb[v] = rb[v];
-        mxb[v] = rb[v + D / 8];
-      }
-      // e_d = max(q_d mn_d, q_d mx_d) = q+_d mx_d + q-_d mn_d (mn <= mx, one product is 0):
-      // two FMAs per element add exactly what mul-max-add adds, in the same order
-      float acca[GQ], accb[GQ];
-#pragma unroll
-      for (int i = 0; i < GQ; ++i) acca[i] = accb[i] = 0.f;
-#pragma unroll
-      for (int v = 0; v < WV; ++v) {
-        const uint32_t wna[4] = {mna[v].x, mna[v].y, mna[v].z, mna[v].w};
-        const uint32_t wxa[4] = {mxa[v].x, mxa[v].y, mxa[v].z, mxa[v].w};
-        const uint32_t wnb[4] = {mnb[v].x, mnb[v].y, mnb[v].z, mnb[v].w};
-        const uint32_t wxb[4] = {mxb[v].x, mxb[v].y, mxb[v].z, mxb[v].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int el = 8 * v + 2 * e;
-          const float na0 = bf16_lo(wna[e]), na1 = bf16_hi(wna[e]), xa0 = bf16_lo(wxa[e]), xa1 = bf16_hi(wxa[e]);
-          const float nb0 = bf16_lo(wnb[e]), nb1 = bf16_hi(wnb[e]), xb0 = bf16_lo(wxb[e]), xb1 = bf16_hi(wxb[e]);
-#pragma unroll
-          for (int i = 0; i < GQ; ++i) {
-            acca[i] = fmaf(qp[i][el], xa0, acca[i]);
-            accb[i] = fmaf(qp[i][el], xb0, accb[i]);
-            acca[i] = fmaf(qm[i][el], na0, acca[i]);
-            accb[i] = fmaf(qm[i][el], nb0, accb[i]);
-            acca[i] = fmaf(qp[i][el + 1], xa1, acca[i]);
-            accb[i] = fmaf(qp[i][el + 1], xb1, accb[i]);
-            acca[i] = fmaf(qm[i][el + 1], na1, acca[i]);
-            accb[i] = fmaf(qm[i][el + 1], nb1, accb[i]);
-          }
-        }
-      }
-      float besta = -INFINITY, bestb = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < GQ; ++i) {
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-          acca[i] = __fadd_rn(acca[i], __shfl_xor_sync(0xffffffffu, acca[i], off));
-          accb[i] = __fadd_rn(accb[i], __shfl_xor_sync(0xffffffffu, accb[i], off));
-        }
-        if (i < a.g) {
-          besta = i == 0 ? acca[i] : fmaxf(besta, acca[i]);
-          bestb = i == 0 ? accb[i] : fmaxf(bestb, accb[i]);
-        }
-      }
-      if (j == 0 && ok) {
-        if (pa < np) {
-          nan_seen |= is_nan(besta);
-          keys[c * kChunkPages + pa] = float_key(besta);
-        }
-        if (pb < np) {
-          nan_seen |= is_nan(bestb);
-          keys[c * kChunkPages + pb] = float_key(bestb);
+      for (int t = 0; t < NV / 2; ++t) {
+        if (t < h) {
+          const float send = up ? v[t] : v[t + h];
+          const float keep = up ? v[t + h] : v[t];
+          v[t] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
         }
       }
     } else {
 #pragma unroll
-    for (int pl0 = 0; pl0 < kChunkPages; pl0 += 16) {  // both halves of a warp take 2 pages each
-      const int pl = pl0 + hw;
-      const bool valid = ok && pl < np;
-      uint4 mnv[WV], mxv[WV];
+      for (int t = 0; t < (NV >> LS); ++t) v[t] = __fadd_rn(v[t], __shfl_xor_sync(0xffffffffu, v[t], o));
+    }
+  }
+}
+
+template <int D, int GQ>
+__global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(const ScoreArgs a) {
+  using CF = ScoreCfg<D>;
+  constexpr int NW = CF::NW, SP = CF::SP, PPL = CF::PPL, R = CF::R, PAGE = CF::PAGE, STAGE = CF::STAGE;
+  constexpr int W = D / 16;   // elements per slice
+  constexpr int WV = W / 8;   // 16-byte vectors per slice
+  constexpr bool kPack = GQ * W <= 32;  // q+ and q- as duplicated f32x2 pairs fit in registers
+  // values per lane after the slice sums: NV = PPL pages x GQ heads, value number slot * GQ + head
+  constexpr int NV = PPL * GQ;
+  constexpr int LS = log2c(NV) < 4 ? log2c(NV) : 4;  // split levels of transpose_sum
+  constexpr int NR = NV >> LS;                       // values a lane holds afterwards
+  static_assert(NR <= GQ && GQ % NR == 0, "a lane's values after the sum are heads of one page");
+  // lane bits that index heads (split levels of weight < GQ) or that hold copies (levels past LS);
+  // a lane with none of them set writes the page's key
+  constexpr int kHeadLevels = log2c(GQ / NR);
+  int wmask = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (k >= LS - kHeadLevels) wmask |= 8 >> k;
+  static_assert(SP == 2 * PPL && PPL % 2 == 0, "pages are scored in f32x2 pairs");
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = lane >> 4, j = lane & 15;
+  uint8_t *wring = smem + warp * R * STAGE;                                     // [R][STAGE]
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + CF::RING) + warp * R;   // [R]
+
+  // the select kernel may be scheduled now; it waits for this grid before reading keys
+  griddep_launch_dependents();
+
+  // this warp's units [u0, u1)
+  const int64_t c0 = (int64_t)blockIdx.x * a.units / gridDim.x;
+  const int64_t c1 = (int64_t)(blockIdx.x + 1) * a.units / gridDim.x;
+  const int64_t u0 = c0 + warp * (c1 - c0) / NW, u1 = c0 + (warp + 1) * (c1 - c0) / NW;
+  const int nst = (int)((u1 - u0 + SP - 1) / SP);
+  if (lane < R) mbar_init(&wbar[lane], 1);
+  fence_barrier_init();
+  __syncwarp();
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(a.minmax);
+  auto issue = [&](int st) {  // lane 0: stage st of this warp
+    const int64_t us = u0 + (int64_t)st * SP;
+    const uint32_t bytes = (uint32_t)(min((int64_t)SP, u1 - us) * PAGE);
+    uint64_t *bar = &wbar[st % R];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(wring + (st % R) * STAGE, src + us * PAGE, bytes, bar);
+  };
+  if (lane == 0)
+    for (int st = 0; st < R && st < nst; ++st) issue(st);
+  int issued = min(R, nst);
+
+  // query slice of the current row: packed (q, q) pairs of q+ and q-, or raw bf16 words
+  uint64_t qp2[kPack ? GQ : 1][kPack ? W : 1], qm2[kPack ? GQ : 1][kPack ? W : 1];
+  uint32_t qv[kPack ? 1 : GQ][kPack ? 1 : W / 2];
+  int64_t row = u0 / a.n_pages;
+  int64_t row_lo = row * a.n_pages, row_hi = row_lo + a.n_pages;
+  bool q_nan = false;  // a NaN in this lane's query slice (q+ and q- would hide it)
+  auto load_q = [&]() {
+    q_nan = false;
+#pragma unroll
+    for (int i = 0; i < GQ; ++i) {
+      const int qi = i < a.g ? i : 0;  // heads past g repeat head 0: the max is unchanged
+      const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + ((size_t)row * a.g + qi) * D + j * W);
 #pragma unroll
       for (int v = 0; v < WV; ++v) {
-        mnv[v] = valid ? reinterpret_cast<const uint4 *>(stage + pl * 4 * D + j * W * 2)[v] : make_uint4(0, 0, 0, 0);
-        mxv[v] = valid ? reinterpret_cast<const uint4 *>(stage + pl * 4 * D + 2 * D + j * W * 2)[v] : make_uint4(0, 0, 0, 0);
-      }
-      float best = -INFINITY;
+        const uint4 x = __ldcg(qs + v);
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int i = 0; i < GQ; ++i) {
-        float acc = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          q_nan |= i < a.g && (is_nan(bf16_lo(w4[e])) || is_nan(bf16_hi(w4[e])));
+          if constexpr (kPack) {
+            const float lo = bf16_lo(w4[e]), hi = bf16_hi(w4[e]);
+            qp2[i][8 * v + 2 * e] = pack2(fmaxf(lo, 0.f), fmaxf(lo, 0.f));
+            qm2[i][8 * v + 2 * e] = pack2(fminf(lo, 0.f), fminf(lo, 0.f));
+            qp2[i][8 * v + 2 * e + 1] = pack2(fmaxf(hi, 0.f), fmaxf(hi, 0.f));
+            qm2[i][8 * v + 2 * e + 1] = pack2(fminf(hi, 0.f), fminf(hi, 0.f));
+          } else {
+            qv[i][4 * v + e] = w4[e];
+          }
+        }
+      }
+    }
+  };
+  if (nst > 0) load_q();
+
+  // page slot of this lane's values after transpose_sum (only meaningful for writers)
+  int base = 0;
+#pragma unroll
+  for (int k = 0; k < LS; ++k)
+    if (lane & (8 >> k)) base += NV >> (k + 1);
+  const int my_slot = base / GQ;
+  const bool writer = (lane & wmask) == 0;
+
+  bool nan_seen = false, dead = false;
+  int st = 0;
+  for (; st < nst; ++st) {
+    bool ok = mbar_wait(&wbar[st % R], (uint32_t)((st / R) & 1), kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      if (lane == 0) report(a.status, TG_STATUS_TIMEOUT);
+      dead = true;
+      break;
+    }
+    const uint8_t *stage = wring + (st % R) * STAGE;
+    const int64_t us = u0 + (int64_t)st * SP;
+    const int cnt = (int)min((int64_t)SP, u1 - us);
+    // slot s of this lane is stage page hw + 2s; pages past cnt read stale shared memory
+    // and are never written
+    uint4 mn[PPL][WV], mx[PPL][WV];
+#pragma unroll
+    for (int sl = 0; sl < PPL; ++sl) {
+      const uint4 *rp = reinterpret_cast<const uint4 *>(stage + (hw + 2 * sl) * PAGE + j * W * 2);
+#pragma unroll
+      for (int v = 0; v < WV; ++v) {
+        mn[sl][v] = rp[v];
+        mx[sl][v] = rp[v + D / 8];  // the max row follows the min row: 2*D bytes = D/8 vectors
+      }
+    }
+    constexpr uint32_t kAll = (1u << SP) - 1u;
+    uint32_t done = kAll & ~((1u << cnt) - 1u);
+    while (done != kAll) {
+      // one row at a time (a stage straddles a row end only rarely)
+      const int first = __ffs(~done & kAll) - 1;
+      if (us + first >= row_hi) {
+        while (us + first >= row_hi) {
+          ++row;
+          row_lo = row_hi;
+          row_hi += a.n_pages;
+        }
+        load_q();
+      }
+      const int lo = (int)max(row_lo - us, (int64_t)0), hi = (int)min(row_hi - us, (int64_t)SP);
+      const uint32_t mine = ((1u << hi) - 1u) & ~((1u << lo) - 1u) & ~done;
+
+      float val[NV];  // slot * GQ + head
+      if constexpr (kPack) {
+        uint64_t acc[PPL / 2][GQ];  // (slot 2k, slot 2k+1) of head i
+#pragma unroll
+        for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+          for (int i = 0; i < GQ; ++i) acc[k][i] = 0ull;
 #pragma unroll
         for (int v = 0; v < WV; ++v) {
-          const uint32_t mnw[4] = {mnv[v].x, mnv[v].y, mnv[v].z, mnv[v].w};
-          const uint32_t mxw[4] = {mxv[v].x, mxv[v].y, mxv[v].z, mxv[v].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint32_t qq = qv[i][4 * v + e];
-            const float e_lo = fmaxf(__fmul_rn(bf16_lo(qq), bf16_lo(mnw[e])), __fmul_rn(bf16_lo(qq), bf16_lo(mxw[e])));
-            acc = __fadd_rn(acc, e_lo);
-            const float e_hi = fmaxf(__fmul_rn(bf16_hi(qq), bf16_hi(mnw[e])), __fmul_rn(bf16_hi(qq), bf16_hi(mxw[e])));
-            acc = __fadd_rn(acc, e_hi);
+            const int el = 8 * v + 2 * e;
+#pragma unroll
+            for (int k = 0; k < PPL / 2; ++k) {
+              const uint32_t wx0 = (&mx[2 * k][v].x)[e], wx1 = (&mx[2 * k + 1][v].x)[e];
+              const uint32_t wn0 = (&mn[2 * k][v].x)[e], wn1 = (&mn[2 * k + 1][v].x)[e];
+              const uint64_t x0 = pack2(bf16_lo(wx0), bf16_lo(wx1)), n0 = pack2(bf16_lo(wn0), bf16_lo(wn1));
+              const uint64_t x1 = pack2(bf16_hi(wx0), bf16_hi(wx1)), n1 = pack2(bf16_hi(wn0), bf16_hi(wn1));
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) {
+                ffma2(acc[k][i], qp2[i][el], x0);
+                ffma2(acc[k][i], qm2[i][el], n0);
+                ffma2(acc[k][i], qp2[i][el + 1], x1);
+                ffma2(acc[k][i], qm2[i][el + 1], n1);
+              }
+            }
           }
         }
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-        if (i < a.g) {
-          nan_seen |= valid && is_nan(acc);
-          best = i == 0 ? acc : fmaxf(best, acc);
+        for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+          for (int i = 0; i < GQ; ++i) unpack2(acc[k][i], val[(2 * k) * GQ + i], val[(2 * k + 1) * GQ + i]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < NV; ++t) val[t] = 0.f;
+#pragma unroll
+        for (int v = 0; v < WV; ++v) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+#pragma unroll
+            for (int sl = 0; sl < PPL; ++sl) {
+              const uint32_t wn = (&mn[sl][v].x)[e], wx = (&mx[sl][v].x)[e];
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) {
+                const uint32_t qq = qv[i][4 * v + e];
+                const float q0 = bf16_lo(qq), q1 = bf16_hi(qq);
+                float &acc = val[sl * GQ + i];
+                acc = __fadd_rn(acc, fmaxf(__fmul_rn(q0, bf16_lo(wn)), __fmul_rn(q0, bf16_lo(wx))));
+                acc = __fadd_rn(acc, fmaxf(__fmul_rn(q1, bf16_hi(wn)), __fmul_rn(q1, bf16_hi(wx))));
+              }
+            }
+          }
         }
       }
-      if (j == 0 && valid) keys[c * kChunkPages + pl] = float_key(best);
+      transpose_sum<NV>(val, lane);
+      // val[0 .. NR-1]: heads (base % GQ) .. of page slot my_slot; max over the page's heads
+      float best = val[0];
+      bool nan_here = is_nan(val[0]);
+#pragma unroll
+      for (int r = 1; r < NR; ++r) {
+        best = fmaxf(best, val[r]);
+        nan_here |= is_nan(val[r]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k >= LS - kHeadLevels && k < LS) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 8 >> k));
+      const int po = hw + 2 * my_slot;  // stage page of this lane's values
+      const bool own = (mine >> po) & 1u;
+      nan_seen |= (own && nan_here) || (mine && q_nan);
+      if (writer && own) a.keys[us + po] = float_key(best);
+      done |= mine;
     }
-    }
-    // every thread is done with stage s; thread 0 refills it
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    if (tid == 0 && c + NS < nc) {
-      fence_proxy_async_smem();
-      issue(c + NS);
+    __syncwarp();
+    if (issued < nst) {
+      if (lane == 0) {
+        fence_proxy_async_smem();  // our reads of this stage come before the refill
+        issue(issued);
+      }
+      ++issued;
     }
   }
-  if (failed) {  // a copy wait gave up: report, drain our own copies in flight, leave
-    if (tid == 0) {
-      report(a.status, TG_STATUS_TIMEOUT);
-      for (int t = c; t < nc && t < c + NS; ++t)
-        if (!mbar_wait(&bars[t % NS], (uint32_t)((t / NS) & 1), kWaitLimitNs)) break;
-    }
-    return;
+  if (dead && lane == 0) {  // drain this warp's copies still in flight
+    for (int t = st; t < issued; ++t)
+      if (!mbar_wait(&wbar[t % R], (uint32_t)((t / R) & 1), kWaitLimitNs)) break;
   }
-  if (nan_seen) nan_flag = 1;
-  __syncthreads();
-  if (nan_flag && tid == 0) report(a.status, TG_STATUS_NONFINITE);
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) report(a.status, TG_STATUS_NONFINITE);
+  // complete only after the kernel before this one in the stream: the select kernel
+  // that follows waits for this grid, and it overwrites page lists that kernel may read
+  griddep_wait();
+}
 
+// One CTA per (request, KV head): top-K of the row's keys, ascending, ties to the lower page.
+__global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t *keys, int n_pages, int K,
+                                                                  int32_t *sel, int32_t *pt_ids) {
+  extern __shared__ uint32_t skeys[];  // [n_pages]
+  __shared__ int hist[256];
+  __shared__ int scan[33];
+  __shared__ int sel_scratch[4];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  // the keys are written by the score kernel just before this one
+  griddep_wait();
+  const uint32_t *rk = keys + (size_t)row * n_pages;
+  for (int i = tid; i < n_pages; i += kSelThreads) skeys[i] = __ldcg(rk + i);
+  __syncthreads();
   uint32_t T;
   int need_eq;
-  block_radix_select<kThreads>(a.n_pages, a.K, [&](int i) { return keys[i]; }, hist, sel_scratch, T, need_eq);
-
+  block_radix_select<kSelThreads>(n_pages, K, [&](int i) { return skeys[i]; }, hist, sel_scratch, T, need_eq);
   int taken = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < a.n_pages && taken < a.K; c0 += kThreads) {
+  for (int c0 = 0; c0 < n_pages && taken < K; c0 += kSelThreads) {
     const int p = c0 + tid;
-    const uint32_t key = p < a.n_pages ? keys[p] : 0u;
-    const bool gt = p < a.n_pages && key > T, eq = p < a.n_pages && key == T;
+    const uint32_t key = p < n_pages ? skeys[p] : 0u;
+    const bool gt = p < n_pages && key > T, eq = p < n_pages && key == T;
     int eq_total, sel_total;
-    const int eq_rank = eq_seen + block_excl_count<kThreads>(eq, scan, eq_total);
-    const bool sel = gt || (eq && eq_rank < need_eq);
-    const int k = taken + block_excl_count<kThreads>(sel, scan, sel_total);
-    if (sel) {
-      a.sel[(size_t)row * a.K + k] = p;
-      if (a.pt_ids) a.pt_ids[(size_t)row * a.K + k] = row * a.n_pages + p;
+    const int eq_rank = eq_seen + block_excl_count<kSelThreads>(eq, scan, eq_total);
+    const bool take = gt || (eq && eq_rank < need_eq);
+    const int k = taken + block_excl_count<kSelThreads>(take, scan, sel_total);
+    if (take) {
+      sel[(size_t)row * K + k] = p;
+      if (pt_ids) pt_ids[(size_t)row * K + k] = row * n_pages + p;
     }
     taken += sel_total;
     eq_seen += eq_total;
   }
 }
 
+// One warp per (request, KV head) for rows of at most 32 x KPL pages: the row's keys sit in
+// registers (lane l holds pages l, l+32, ...; missing pages hold key 0, which no candidate
+// below reaches).  The K-th largest key T is built bit by bit from the top: a bit stays set
+// when at least K keys are >= the prefix with it (a warp-wide count per bit; the bits on
+// which all keys agree are taken as they are).  A ballot sweep then lists the winners in
+// ascending page order: every key > T, and the lowest pages among the keys == T.
+constexpr int kWarpKeysMax = 32;
+constexpr int kSelWarps = 4;
+
+template <int KPL>
+__global__ void __launch_bounds__(kSelWarps * 32) page_select_warp_kernel(const uint32_t *keys, int rows,
+                                                                          int n_pages, int K, int32_t *sel,
+                                                                          int32_t *pt_ids) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kSelWarps + warp;
+  // the keys are written by the score kernel just before this one
+  griddep_wait();
+  if (row >= rows) return;
+  const uint32_t *rk = keys + (size_t)row * n_pages;
+  uint32_t key[KPL];
+  uint32_t k_and = 0xffffffffu, k_or = 0u;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool valid = 32 * i + lane < n_pages;
+    key[i] = valid ? __ldcg(rk + 32 * i + lane) : 0u;
+    k_and &= valid ? key[i] : 0xffffffffu;
+    k_or |= key[i];
+  }
+  k_and = __reduce_and_sync(0xffffffffu, k_and);
+  k_or = __reduce_or_sync(0xffffffffu, k_or);
+  // number of keys >= c, for c >= 1 (missing pages hold 0): four independent partial counts
+  auto count_ge = [&](uint32_t c) {
+    int n[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) n[i & 3] += key[i] >= c;
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)(n[0] + n[1] + n[2] + n[3]));
+  };
+  uint32_t T = k_and;  // all keys agree above the top differing bit (and T == k_and if they all agree)
+  const uint32_t differ = k_and ^ k_or;
+  if (differ) {
+    const int top = 31 - __clz(differ);
+    T = top == 31 ? 0u : T & ~((2u << top) - 1u);
+#pragma unroll 1
+    for (int bit = top; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      if (count_ge(cand) >= K) T = cand;
+    }
+  }
+  const int need_eq = K - (T == 0xffffffffu ? 0 : count_ge(T + 1));  // keys equal to T to take
+  const uint32_t lt = (1u << lane) - 1u;
+  int taken = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool eq = key[i] == T && 32 * i + lane < n_pages;
+    const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+    const bool take = key[i] > T || (eq && eq_seen + __popc(beq & lt) < need_eq);
+    const uint32_t btake = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int pos = taken + __popc(btake & lt);
+      const int p = 32 * i + lane;
+      sel[(size_t)row * K + pos] = p;
+      if (pt_ids) pt_ids[(size_t)row * K + pos] = row * n_pages + p;
+    }
+    taken += __popc(btake);
+    eq_seen += __popc(beq);
+  }
+}
+
+cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  return at;
+}
+
 template <int D, int GQ>
-cudaError_t launch_score(const ScoreArgs &a, int rows, cudaStream_t s) {
-  auto fn = page_score_topk_kernel<D, GQ>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       ScoreCfg<D>::smem_bytes(kMaxPages));
+cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s) {
+  using CF = ScoreCfg<D>;
+  auto fn = page_score_kernel<D, GQ>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, CF::NW * 32, CF::SMEM);
   if (e != cudaSuccess) return e;
-  fn<<<rows, kThreads, ScoreCfg<D>::smem_bytes(a.n_pages), s>>>(a);
-  return cudaGetLastError();
+  // one wave of persistent CTAs; no more CTAs than give each warp a full stage
+  const int64_t want = (a.units + CF::NW * CF::SP - 1) / (CF::NW * CF::SP);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)std::max(1, per_sm) * sms, want));
+  // may start while the previous kernel in the stream finishes (it reads only q and MinMax
+  // before that kernel is done, and writes only keys, which no other kernel reads then)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(CF::NW * 32);
+  cfg.dynamicSmemBytes = (size_t)CF::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 template <int D>
-cudaError_t launch_score_d(const ScoreArgs &a, int rows, cudaStream_t s) {
-  if (a.g <= 1) return launch_score<D, 1>(a, rows, s);
-  if (a.g <= 2) return launch_score<D, 2>(a, rows, s);
-  if (a.g <= 4) return launch_score<D, 4>(a, rows, s);
-  return launch_score<D, 8>(a, rows, s);
+cudaError_t launch_score_d(const ScoreArgs &a, cudaStream_t s) {
+  if (a.g <= 1) return launch_score<D, 1>(a, s);
+  if (a.g <= 2) return launch_score<D, 2>(a, s);
+  if (a.g <= 4) return launch_score<D, 4>(a, s);
+  return launch_score<D, 8>(a, s);
+}
+
+cudaError_t launch_select(const uint32_t *keys, int rows, int n_pages, int K, int32_t *sel, int32_t *pt_ids,
+                          cudaStream_t s) {
+  // launched early behind the score kernel; it waits for it before reading the keys.  It
+  // does not let the next kernel start early, so a decode launch that reads the page
+  // lists written here always sees them complete
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (n_pages <= 32 * kWarpKeysMax) {
+    cfg.gridDim = dim3((rows + kSelWarps - 1) / kSelWarps);
+    cfg.blockDim = dim3(kSelWarps * 32);
+    const int kpl = (n_pages + 31) / 32;
+    if (kpl <= 4) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<4>, keys, rows, n_pages, K, sel, pt_ids);
+    if (kpl <= 8) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<8>, keys, rows, n_pages, K, sel, pt_ids);
+    if (kpl <= 16) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<16>, keys, rows, n_pages, K, sel, pt_ids);
+    if (kpl <= 20) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<20>, keys, rows, n_pages, K, sel, pt_ids);
+    return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<32>, keys, rows, n_pages, K, sel, pt_ids);
+  }
+  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxPages * 4);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = (size_t)n_pages * 4;
+  return cudaLaunchKernelEx(&cfg, page_select_kernel, keys, n_pages, K, sel, pt_ids);
 }
 
 // minmax[b][h][p][0][:] = min over the page's valid keys, [1][:] = max (exact in bf16)
@@ -319,23 +539,34 @@ __global__ void build_minmax_kernel(const uint16_t *K, uint16_t *mm, int N, int 
 
 }  // namespace
 
+extern "C" int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *workspace_bytes) {
+  if (!workspace_bytes) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_workspace: NULL workspace_bytes");
+  if (batch < 0 || H <= 0 || n_pages < 1) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_workspace: bad sizes");
+  *workspace_bytes = tgi::align_up((int64_t)batch * H * n_pages * 4, 256);
+  return tgi::ok();
+}
+
 extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                                   const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
-                                  int32_t *dev_status) {
+                                  void *workspace, int64_t workspace_bytes, int32_t *dev_status) {
   if (batch < 0 || H <= 0 || g < 1 || g > 8) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: bad batch/H/g");
   if (d != 128 && d != 256) return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: d=%d (128 or 256)", d);
   if (n_pages < 1 || n_pages > kMaxPages || K < 1 || K > n_pages)
     return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: need 1 <= K=%d <= n_pages=%d <= %d", K, n_pages, kMaxPages);
   if (batch == 0) return tgi::ok();
-  if (!q || !minmax || !sel) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: NULL q/minmax/sel");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(minmax)) & 15)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: q and minmax must be 16-byte aligned");
+  if (!q || !minmax || !sel || !workspace)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: NULL q/minmax/sel/workspace");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(minmax) | reinterpret_cast<uintptr_t>(workspace)) & 15)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: q, minmax and workspace must be 16-byte aligned");
   if ((int64_t)batch * H * n_pages > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: page ids overflow int32");
-  ScoreArgs a{q, minmax, sel, pt_ids, dev_status, H, g, n_pages, K};
+  const int64_t need = (int64_t)batch * H * n_pages * 4;
+  if (workspace_bytes < need)
+    return tgi::fail(TG_ERR_CAPACITY, "tg_page_score_topk: workspace %lld < %lld bytes", (long long)workspace_bytes,
+                     (long long)need);
+  ScoreArgs a{q, minmax, static_cast<uint32_t *>(workspace), dev_status, (int64_t)batch * H * n_pages, g, n_pages};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (d == 128) e = launch_score_d<128>(a, batch * H, s);
-  else e = launch_score_d<256>(a, batch * H, s);
+  cudaError_t e = d == 128 ? launch_score_d<128>(a, s) : launch_score_d<256>(a, s);
+  if (e == cudaSuccess) e = launch_select(a.keys, batch * H, n_pages, K, sel, pt_ids, s);
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_page_score_topk: %s", cudaGetErrorString(e));
   return tgi::ok();
 }

@@ -22,7 +22,7 @@ import numpy as np
 import torch
 
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
-               tg_compact_topk, tg_build_minmax, tg_page_score_topk)
+               tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace)
 
 BYTES_BF16 = 2
 
@@ -109,11 +109,12 @@ class SparseDecoder:
         self.pt_off = torch.arange(0, batch * H * K + 1, K, dtype=torch.int64, device=dev)
         self.sel = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
         self.pt_ids = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
+        self.score_ws = torch.empty(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(d)
 
     def select(self, q, minmax, stream=None):
         tg_page_score_topk(self.batch, self.H, self.g, self.d, self.n_pages, self.K, q, minmax, self.sel,
-                           pt_ids=self.pt_ids, dev_status=self.status, stream=stream)
+                           pt_ids=self.pt_ids, workspace=self.score_ws, dev_status=self.status, stream=stream)
 
     def attend(self, q, pool, out, lse=None, cta_time=None, stream=None):
         tg_decode_attn(self.plan, self.plan_dev, 0, q, pool, self.batch * self.H * self.n_pages, self.pt_off,

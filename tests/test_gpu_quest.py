@@ -70,7 +70,7 @@ def _select_case(lib, cuda, batch, H, g, d, n_pages, K, seed=0, ties=False):
     assert np.array_equal(ids.cpu().numpy(), rows * n_pages + ref)
 
 
-@pytest.mark.parametrize("g,d", [(4, 128), (2, 256), (1, 128), (3, 128), (8, 128)])
+@pytest.mark.parametrize("g,d", [(4, 128), (2, 256), (1, 128), (3, 128), (8, 128), (4, 256), (8, 256)])
 @pytest.mark.parametrize("n_pages,K", [(625, 64), (625, 128), (37, 37), (1000, 1), (2049, 300)])
 def test_page_topk_exact(lib, cuda, g, d, n_pages, K):
     _select_case(lib, cuda, 2, 2, g, d, n_pages, K, seed=n_pages + K + g)
@@ -83,6 +83,58 @@ def test_page_topk_ties(lib, cuda, K):
 
 def test_page_topk_max_pages(lib, cuda):
     _select_case(lib, cuda, 1, 1, 4, 128, 16384, 2048, seed=3)
+
+
+@pytest.mark.parametrize("n_pages,K", [(1024, 1000), (1025, 64), (1024, 1)])
+def test_page_topk_select_paths(lib, cuda, n_pages, K):
+    """Rows at the limit of the warp-per-row select (1024 pages) and just past it."""
+    _select_case(lib, cuda, 3, 2, 4, 128, n_pages, K, seed=n_pages + K)
+
+
+@pytest.mark.parametrize("n_pages,K", [(1, 1), (2, 1), (3, 2), (5, 5), (7, 3)])
+def test_page_topk_tiny_rows(lib, cuda, n_pages, K):
+    """Rows shorter than a scoring group of four pages: one group spans several rows."""
+    _select_case(lib, cuda, 7, 5, 4, 128, n_pages, K, seed=n_pages * 10 + K)
+
+
+def test_page_topk_many_rows(lib, cuda):
+    """Hundreds of rows cut at arbitrary points by the even split over the CTAs' warps."""
+    _select_case(lib, cuda, 37, 9, 2, 128, 101, 17, seed=5)
+
+
+def test_page_topk_workspace_checks(lib, cuda):
+    batch, H, n_pages, K = 2, 3, 50, 5
+    need = lib.tg_page_score_workspace(batch, H, n_pages)
+    assert need >= batch * H * n_pages * 4
+    q = torch.zeros((batch, H * 2, 128), dtype=torch.bfloat16, device=cuda)
+    mm = torch.zeros((batch, H, n_pages, 2, 128), dtype=torch.bfloat16, device=cuda)
+    sel = torch.empty((batch, H, K), dtype=torch.int32, device=cuda)
+    small = torch.empty(batch * H * n_pages * 4 - 16, dtype=torch.uint8, device=cuda)
+    with pytest.raises(lib.TGError) as e:
+        lib.tg_page_score_topk(batch, H, 2, 128, n_pages, K, q, mm, sel, workspace=small)
+    assert "workspace" in str(e.value)
+
+
+def test_page_topk_nan_sets_status(lib, cuda):
+    """A NaN in one query head makes that head's sums NaN: the call reports NONFINITE."""
+    batch, H, g, d, n_pages, K = 2, 2, 4, 128, 40, 8
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(1)
+    q = torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16)
+    q[1, 2, 5] = float("nan")  # request 1, KV head 0, query head 2
+    mm = torch.randn((batch, H, n_pages, 2, d), generator=gen, device=cuda).to(torch.bfloat16)
+    mm = torch.stack([torch.minimum(mm[:, :, :, 0], mm[:, :, :, 1]),
+                      torch.maximum(mm[:, :, :, 0], mm[:, :, :, 1])], 3).contiguous()
+    sel = torch.empty((batch, H, K), dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    lib.tg_page_score_topk(batch, H, g, d, n_pages, K, q, mm, sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & lib.STATUS_NONFINITE
+    # the rows without a NaN still select exactly
+    q_h, mm_h = q.float().cpu().numpy(), mm.float().cpu().numpy()
+    for b, h in [(0, 0), (0, 1), (1, 1)]:
+        ref = ofx.top_pages(ofx.page_scores(q_h[b, h * g:(h + 1) * g], mm_h[b, h, :, 0], mm_h[b, h, :, 1]), K)
+        assert np.array_equal(sel[b, h].cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("K", [4, 10, 25])
