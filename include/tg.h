@@ -251,16 +251,20 @@ int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d,
  *   pt_ids int32 [batch][H][K] (output, may be NULL): (b*H + h)*n_pages + sel,
  *   i.e. the ids of the selected pages in a dense pool [batch][H][n_pages] of
  *   H_p = 1 pages, ready as the page lists of tg_decode_attn;
- *   workspace: scratch of at least tg_page_score_workspace bytes (the page
- *   scores); no initial contents needed; one call at a time per workspace.
- *   q, minmax and workspace 16-byte aligned.
+ *   workspace: scratch of at least tg_page_score_workspace bytes (page scores and
+ *   one page counter per (request, KV head)); zero-filled before the first call.
+ *   Each call returns the counters to zero, so one workspace serves every later
+ *   call on the same stream; concurrent calls need separate workspaces.  After a
+ *   TG_STATUS_TIMEOUT, zero it again.  q, minmax and workspace 16-byte aligned.
  *   Host sizes: d in {128, 256}, 1 <= g <= 8, 1 <= K <= n_pages <= 16384.
- * Launch: two kernels (scores over all pages, then one top-K per head), both
- *   with programmatic dependent launch: the first may start while the previous
- *   kernel in the stream (a tg_decode_attn of the previous layer) finishes,
- *   reading q and minmax and writing only the workspace; it completes only after
- *   that kernel.  The second waits for the first, writes sel and pt_ids, and
- *   does not let the next kernel start early. */
+ * Launch: the score kernel streams every page of the call, evenly split over
+ *   one CTA per SM.  With n_pages <= 1024 the warp that scores the last page of
+ *   a (request, KV head) selects its top K in the same kernel; longer rows are
+ *   selected by a second kernel.  Programmatic dependent launch: the call may
+ *   start while the previous kernel in the stream (a tg_decode_attn of the
+ *   previous layer) finishes, reading q and minmax and writing only the
+ *   workspace; it waits for that kernel before writing sel and pt_ids, and it
+ *   does not let the next kernel start before sel and pt_ids are complete. */
 int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                        const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
                        void *workspace, int64_t workspace_bytes, int32_t *dev_status);

@@ -266,12 +266,11 @@ def tg_page_score_workspace(batch, H, n_pages) -> int:
 def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, workspace=None, dev_status=None,
                        stream=None):
     """Quest page bound + per-KV-head top-K pages (tg.h: tg_page_score_topk).  Without a
-    workspace, one of tg_page_score_workspace bytes is allocated for the call."""
+    workspace, a zero-filled one of tg_page_score_workspace bytes is allocated for the call."""
     import torch
     lib = load()
-    need = tg_page_score_workspace(batch, H, n_pages)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=q.device)
     _check(lib.tg_page_score_topk(_stream(stream), batch, H, g, d, n_pages, K, _dev(q, torch.bfloat16, "q"),
                                   _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
                                   _dev(pt_ids, torch.int32, "pt_ids"), _dev(workspace, torch.uint8, "workspace"),

@@ -61,10 +61,13 @@ struct ScoreCfg {
 
 struct ScoreArgs {
   const uint16_t *q, *minmax;
-  uint32_t *keys;
+  uint32_t *keys;      // [rows][n_pages] scores as keys (workspace)
+  int32_t *row_cnt;    // [rows] pages scored so far (workspace, zero between calls)
+  int32_t *sel, *pt_ids;
   int32_t *status;
-  int64_t units;  // rows * n_pages
-  int g, n_pages;
+  int64_t units;       // rows * n_pages
+  int g, n_pages, K;
+  int fused;           // the warp that completes a row selects its top K (n_pages <= 1024)
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -101,19 +104,94 @@ __device__ __forceinline__ void transpose_sum(float (&v)[NV], int lane) {
     if (k < LS) {
       const int h = NV >> (k + 1);
       const bool up = lane & o;
+      float recv[NV / 2 > 0 ? NV / 2 : 1];
 #pragma unroll
-      for (int t = 0; t < NV / 2; ++t) {
-        if (t < h) {
-          const float send = up ? v[t] : v[t + h];
-          const float keep = up ? v[t + h] : v[t];
-          v[t] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
-        }
-      }
+      for (int t = 0; t < NV / 2; ++t)  // all shuffles of the level first, then the adds
+        if (t < h) recv[t] = __shfl_xor_sync(0xffffffffu, up ? v[t] : v[t + h], o);
+#pragma unroll
+      for (int t = 0; t < NV / 2; ++t)
+        if (t < h) v[t] = __fadd_rn(up ? v[t + h] : v[t], recv[t]);
     } else {
+      float recv[NV >> LS];
 #pragma unroll
-      for (int t = 0; t < (NV >> LS); ++t) v[t] = __fadd_rn(v[t], __shfl_xor_sync(0xffffffffu, v[t], o));
+      for (int t = 0; t < (NV >> LS); ++t) recv[t] = __shfl_xor_sync(0xffffffffu, v[t], o);
+#pragma unroll
+      for (int t = 0; t < (NV >> LS); ++t) v[t] = __fadd_rn(v[t], recv[t]);
     }
   }
+}
+
+// Top K of one (request, KV head) row of at most 32 x KPL pages, by one warp.  The row's keys
+// sit in registers (lane l holds pages l, l+32, ...; missing pages hold key 0, which no
+// candidate below reaches).  The K-th largest key T is built bit by bit from the top: a bit
+// stays set when at least K keys are >= the prefix with it (a warp-wide count per bit; the
+// bits on which all keys agree are taken as they are).  A ballot sweep then lists the winners
+// in ascending page order: every key > T, and the lowest pages among the keys == T.
+constexpr int kWarpKeysMax = 32;
+constexpr int kRowQueue = 64;  // completed rows a score CTA queues for its warps to select
+
+template <int KPL>
+__device__ __noinline__ void warp_select_row(const uint32_t *rk, int n_pages, int K, int64_t row, int32_t *sel,
+                                             int32_t *pt_ids) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[KPL];
+  uint32_t k_and = 0xffffffffu, k_or = 0u;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool valid = 32 * i + lane < n_pages;
+    key[i] = valid ? __ldcg(rk + 32 * i + lane) : 0u;
+    k_and &= valid ? key[i] : 0xffffffffu;
+    k_or |= key[i];
+  }
+  k_and = __reduce_and_sync(0xffffffffu, k_and);
+  k_or = __reduce_or_sync(0xffffffffu, k_or);
+  // number of keys >= c, for c >= 1 (missing pages hold 0): four independent partial counts
+  auto count_ge = [&](uint32_t c) {
+    int n[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) n[i & 3] += key[i] >= c;
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)(n[0] + n[1] + n[2] + n[3]));
+  };
+  uint32_t T = k_and;  // all keys agree above the top differing bit (and T == k_and if they all agree)
+  const uint32_t differ = k_and ^ k_or;
+  if (differ) {
+    const int top = 31 - __clz(differ);
+    T = top == 31 ? 0u : T & ~((2u << top) - 1u);
+#pragma unroll 1
+    for (int bit = top; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      if (count_ge(cand) >= K) T = cand;
+    }
+  }
+  const int need_eq = K - (T == 0xffffffffu ? 0 : count_ge(T + 1));  // keys equal to T to take
+  const uint32_t lt = (1u << lane) - 1u;
+  int taken = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool eq = key[i] == T && 32 * i + lane < n_pages;
+    const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+    const bool take = key[i] > T || (eq && eq_seen + __popc(beq & lt) < need_eq);
+    const uint32_t btake = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int pos = taken + __popc(btake & lt);
+      const int p = 32 * i + lane;
+      sel[(size_t)row * K + pos] = p;
+      if (pt_ids) pt_ids[(size_t)row * K + pos] = (int32_t)(row * n_pages + p);
+    }
+    taken += __popc(btake);
+    eq_seen += __popc(beq);
+  }
+}
+
+// the KPL bucket for n_pages <= 32 * kWarpKeysMax
+__device__ __forceinline__ void warp_select(const uint32_t *rk, int n_pages, int K, int64_t row, int32_t *sel,
+                                            int32_t *pt_ids) {
+  const int kpl = (n_pages + 31) / 32;
+  if (kpl <= 4) warp_select_row<4>(rk, n_pages, K, row, sel, pt_ids);
+  else if (kpl <= 8) warp_select_row<8>(rk, n_pages, K, row, sel, pt_ids);
+  else if (kpl <= 16) warp_select_row<16>(rk, n_pages, K, row, sel, pt_ids);
+  else if (kpl <= 24) warp_select_row<24>(rk, n_pages, K, row, sel, pt_ids);
+  else warp_select_row<32>(rk, n_pages, K, row, sel, pt_ids);
 }
 
 template <int D, int GQ>
@@ -138,13 +216,22 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
   static_assert(SP == 2 * PPL && PPL % 2 == 0, "pages are scored in f32x2 pairs");
 
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int64_t s_rows[kRowQueue];  // rows completed by this CTA's warps, to select
+  __shared__ int s_nrows, s_more;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hw = lane >> 4, j = lane & 15;
+  if (threadIdx.x == 0) {
+    s_nrows = 0;
+    s_more = 0;
+  }
+  __syncthreads();
   uint8_t *wring = smem + warp * R * STAGE;                                     // [R][STAGE]
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + CF::RING) + warp * R;   // [R]
 
-  // the select kernel may be scheduled now; it waits for this grid before reading keys
-  griddep_launch_dependents();
+  // with a separate select kernel next, it may be scheduled now (it waits for this grid
+  // before reading keys); with the select fused in, the next kernel (a decode reading the
+  // page lists before it waits) starts only when this grid is done
+  if (!a.fused) griddep_launch_dependents();
 
   // this warp's units [u0, u1)
   const int64_t c0 = (int64_t)blockIdx.x * a.units / gridDim.x;
@@ -233,22 +320,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
         mx[sl][v] = rp[v + D / 8];  // the max row follows the min row: 2*D bytes = D/8 vectors
       }
     }
-    constexpr uint32_t kAll = (1u << SP) - 1u;
-    uint32_t done = kAll & ~((1u << cnt) - 1u);
-    while (done != kAll) {
-      // one row at a time (a stage straddles a row end only rarely)
-      const int first = __ffs(~done & kAll) - 1;
-      if (us + first >= row_hi) {
-        while (us + first >= row_hi) {
-          ++row;
-          row_lo = row_hi;
-          row_hi += a.n_pages;
-        }
-        load_q();
-      }
-      const int lo = (int)max(row_lo - us, (int64_t)0), hi = (int)min(row_hi - us, (int64_t)SP);
-      const uint32_t mine = ((1u << hi) - 1u) & ~((1u << lo) - 1u) & ~done;
-
+    // score the stage pages in `mine` against the current row's query (all of them lie in it)
+    auto score_pages = [&](const uint32_t mine) {
       float val[NV];  // slot * GQ + head
       if constexpr (kPack) {
         uint64_t acc[PPL / 2][GQ];  // (slot 2k, slot 2k+1) of head i
@@ -261,20 +334,33 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int el = 8 * v + 2 * e;
+            uint64_t x0[PPL / 2], n0[PPL / 2], x1[PPL / 2], n1[PPL / 2];
 #pragma unroll
             for (int k = 0; k < PPL / 2; ++k) {
               const uint32_t wx0 = (&mx[2 * k][v].x)[e], wx1 = (&mx[2 * k + 1][v].x)[e];
               const uint32_t wn0 = (&mn[2 * k][v].x)[e], wn1 = (&mn[2 * k + 1][v].x)[e];
-              const uint64_t x0 = pack2(bf16_lo(wx0), bf16_lo(wx1)), n0 = pack2(bf16_lo(wn0), bf16_lo(wn1));
-              const uint64_t x1 = pack2(bf16_hi(wx0), bf16_hi(wx1)), n1 = pack2(bf16_hi(wn0), bf16_hi(wn1));
-#pragma unroll
-              for (int i = 0; i < GQ; ++i) {
-                ffma2(acc[k][i], qp2[i][el], x0);
-                ffma2(acc[k][i], qm2[i][el], n0);
-                ffma2(acc[k][i], qp2[i][el + 1], x1);
-                ffma2(acc[k][i], qm2[i][el + 1], n1);
-              }
+              x0[k] = pack2(bf16_lo(wx0), bf16_lo(wx1));
+              n0[k] = pack2(bf16_lo(wn0), bf16_lo(wn1));
+              x1[k] = pack2(bf16_hi(wx0), bf16_hi(wx1));
+              n1[k] = pack2(bf16_hi(wn0), bf16_hi(wn1));
             }
+            // four rounds over every (pair, head) chain: consecutive FMAs are independent
+#pragma unroll
+            for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) ffma2(acc[k][i], qp2[i][el], x0[k]);
+#pragma unroll
+            for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) ffma2(acc[k][i], qm2[i][el], n0[k]);
+#pragma unroll
+            for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) ffma2(acc[k][i], qp2[i][el + 1], x1[k]);
+#pragma unroll
+            for (int k = 0; k < PPL / 2; ++k)
+#pragma unroll
+              for (int i = 0; i < GQ; ++i) ffma2(acc[k][i], qm2[i][el + 1], n1[k]);
           }
         }
 #pragma unroll
@@ -319,7 +405,28 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
       const bool own = (mine >> po) & 1u;
       nan_seen |= (own && nan_here) || (mine && q_nan);
       if (writer && own) a.keys[us + po] = float_key(best);
-      done |= mine;
+    };
+    constexpr uint32_t kAll = (1u << SP) - 1u;
+    if (cnt == SP && us >= row_lo && us + SP <= row_hi) {
+      score_pages(kAll);  // the common case: a full stage inside the current row
+    } else {
+      uint32_t done = kAll & ~((1u << cnt) - 1u);
+      while (done != kAll) {
+        // one row at a time (a stage straddles a row end only rarely)
+        const int first = __ffs(~done & kAll) - 1;
+        if (us + first >= row_hi) {
+          while (us + first >= row_hi) {
+            ++row;
+            row_lo = row_hi;
+            row_hi += a.n_pages;
+          }
+          load_q();
+        }
+        const int lo = (int)max(row_lo - us, (int64_t)0), hi = (int)min(row_hi - us, (int64_t)SP);
+        const uint32_t mine = ((1u << hi) - 1u) & ~((1u << lo) - 1u) & ~done;
+        score_pages(mine);
+        done |= mine;
+      }
     }
     __syncwarp();
     if (issued < nst) {
@@ -335,8 +442,56 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
       if (!mbar_wait(&wbar[t % R], (uint32_t)((t / R) & 1), kWaitLimitNs)) break;
   }
   if (__any_sync(0xffffffffu, nan_seen) && lane == 0) report(a.status, TG_STATUS_NONFINITE);
-  // complete only after the kernel before this one in the stream: the select kernel
-  // that follows waits for this grid, and it overwrites page lists that kernel may read
+
+  // ---- rows this warp scored: add their page counts.  A row whose count reaches n_pages
+  // is complete (its keys are all in L2): the CTA queues it, and once all its warps are
+  // done streaming, they share the queued selections, one row per warp at a time
+  if (a.fused) {
+    if (nst > 0 && !dead) {
+      __threadfence();  // this lane's key stores before the count
+      __syncwarp();
+      const int64_t r_first = u0 / a.n_pages, r_last = (u1 - 1) / a.n_pages;
+      for (int64_t r = r_first; r <= r_last; ++r) {
+        const int64_t lo = max(u0, r * a.n_pages), hi = min(u1, (r + 1) * a.n_pages);
+        if (lane == 0 && atomicAdd(&a.row_cnt[r], (int)(hi - lo)) + (int)(hi - lo) == a.n_pages) {
+          const int at = atomicAdd(&s_nrows, 1);
+          if (at < kRowQueue) s_rows[at] = r;
+          else s_more = 1;  // more rows than the queue holds: the overflow is found below
+        }
+      }
+    }
+    __syncthreads();
+    const int nq = min(s_nrows, kRowQueue);
+    if (nq > 0) {
+      __threadfence();   // the other CTAs' key stores, ordered by their counts
+      griddep_wait();    // the previous kernel (a decode) may still read sel / pt_ids
+      for (int i = warp; i < nq; i += NW) {
+        const int64_t r = s_rows[i];
+        warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, r, a.sel, a.pt_ids);
+        if (lane == 0) a.row_cnt[r] = 0;
+      }
+    }
+    if (s_more && nst > 0 && !dead) {  // rare: rescan this warp's rows for completed ones not queued
+      const int64_t r_first = u0 / a.n_pages, r_last = (u1 - 1) / a.n_pages;
+      for (int64_t r = r_first; r <= r_last; ++r) {
+        int mine_row = 0;
+        if (lane == 0 && atomicAdd(&a.row_cnt[r], 0) == a.n_pages) {
+          mine_row = 1;
+          for (int i = 0; i < nq; ++i) mine_row &= s_rows[i] != r;
+          // claim it: only one warp of this CTA may select a row left out of the queue
+          if (mine_row) mine_row = atomicCAS(&a.row_cnt[r], a.n_pages, -1) == a.n_pages;
+        }
+        if (__shfl_sync(0xffffffffu, mine_row, 0)) {
+          __threadfence();
+          griddep_wait();
+          warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, r, a.sel, a.pt_ids);
+          if (lane == 0) a.row_cnt[r] = 0;
+        }
+      }
+    }
+  }
+  // complete only after the kernel before this one in the stream: the kernel that
+  // follows may overwrite page lists that kernel reads
   griddep_wait();
 }
 
@@ -371,74 +526,6 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t
     }
     taken += sel_total;
     eq_seen += eq_total;
-  }
-}
-
-// One warp per (request, KV head) for rows of at most 32 x KPL pages: the row's keys sit in
-// registers (lane l holds pages l, l+32, ...; missing pages hold key 0, which no candidate
-// below reaches).  The K-th largest key T is built bit by bit from the top: a bit stays set
-// when at least K keys are >= the prefix with it (a warp-wide count per bit; the bits on
-// which all keys agree are taken as they are).  A ballot sweep then lists the winners in
-// ascending page order: every key > T, and the lowest pages among the keys == T.
-constexpr int kWarpKeysMax = 32;
-constexpr int kSelWarps = 4;
-
-template <int KPL>
-__global__ void __launch_bounds__(kSelWarps * 32) page_select_warp_kernel(const uint32_t *keys, int rows,
-                                                                          int n_pages, int K, int32_t *sel,
-                                                                          int32_t *pt_ids) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kSelWarps + warp;
-  // the keys are written by the score kernel just before this one
-  griddep_wait();
-  if (row >= rows) return;
-  const uint32_t *rk = keys + (size_t)row * n_pages;
-  uint32_t key[KPL];
-  uint32_t k_and = 0xffffffffu, k_or = 0u;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const bool valid = 32 * i + lane < n_pages;
-    key[i] = valid ? __ldcg(rk + 32 * i + lane) : 0u;
-    k_and &= valid ? key[i] : 0xffffffffu;
-    k_or |= key[i];
-  }
-  k_and = __reduce_and_sync(0xffffffffu, k_and);
-  k_or = __reduce_or_sync(0xffffffffu, k_or);
-  // number of keys >= c, for c >= 1 (missing pages hold 0): four independent partial counts
-  auto count_ge = [&](uint32_t c) {
-    int n[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) n[i & 3] += key[i] >= c;
-    return (int)__reduce_add_sync(0xffffffffu, (unsigned)(n[0] + n[1] + n[2] + n[3]));
-  };
-  uint32_t T = k_and;  // all keys agree above the top differing bit (and T == k_and if they all agree)
-  const uint32_t differ = k_and ^ k_or;
-  if (differ) {
-    const int top = 31 - __clz(differ);
-    T = top == 31 ? 0u : T & ~((2u << top) - 1u);
-#pragma unroll 1
-    for (int bit = top; bit >= 0; --bit) {
-      const uint32_t cand = T | (1u << bit);
-      if (count_ge(cand) >= K) T = cand;
-    }
-  }
-  const int need_eq = K - (T == 0xffffffffu ? 0 : count_ge(T + 1));  // keys equal to T to take
-  const uint32_t lt = (1u << lane) - 1u;
-  int taken = 0, eq_seen = 0;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const bool eq = key[i] == T && 32 * i + lane < n_pages;
-    const uint32_t beq = __ballot_sync(0xffffffffu, eq);
-    const bool take = key[i] > T || (eq && eq_seen + __popc(beq & lt) < need_eq);
-    const uint32_t btake = __ballot_sync(0xffffffffu, take);
-    if (take) {
-      const int pos = taken + __popc(btake & lt);
-      const int p = 32 * i + lane;
-      sel[(size_t)row * K + pos] = p;
-      if (pt_ids) pt_ids[(size_t)row * K + pos] = row * n_pages + p;
-    }
-    taken += __popc(btake);
-    eq_seen += __popc(beq);
   }
 }
 
@@ -485,6 +572,9 @@ cudaError_t launch_score_d(const ScoreArgs &a, cudaStream_t s) {
 
 cudaError_t launch_select(const uint32_t *keys, int rows, int n_pages, int K, int32_t *sel, int32_t *pt_ids,
                           cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxPages * 4);
+  if (e != cudaSuccess) return e;
   // launched early behind the score kernel; it waits for it before reading the keys.  It
   // does not let the next kernel start early, so a decode launch that reads the page
   // lists written here always sees them complete
@@ -493,19 +583,6 @@ cudaError_t launch_select(const uint32_t *keys, int rows, int n_pages, int K, in
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (n_pages <= 32 * kWarpKeysMax) {
-    cfg.gridDim = dim3((rows + kSelWarps - 1) / kSelWarps);
-    cfg.blockDim = dim3(kSelWarps * 32);
-    const int kpl = (n_pages + 31) / 32;
-    if (kpl <= 4) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<4>, keys, rows, n_pages, K, sel, pt_ids);
-    if (kpl <= 8) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<8>, keys, rows, n_pages, K, sel, pt_ids);
-    if (kpl <= 16) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<16>, keys, rows, n_pages, K, sel, pt_ids);
-    if (kpl <= 20) return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<20>, keys, rows, n_pages, K, sel, pt_ids);
-    return cudaLaunchKernelEx(&cfg, page_select_warp_kernel<32>, keys, rows, n_pages, K, sel, pt_ids);
-  }
-  cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxPages * 4);
-  if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(rows);
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = (size_t)n_pages * 4;
@@ -542,7 +619,8 @@ __global__ void build_minmax_kernel(const uint16_t *K, uint16_t *mm, int N, int 
 extern "C" int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *workspace_bytes) {
   if (!workspace_bytes) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_workspace: NULL workspace_bytes");
   if (batch < 0 || H <= 0 || n_pages < 1) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_workspace: bad sizes");
-  *workspace_bytes = tgi::align_up((int64_t)batch * H * n_pages * 4, 256);
+  // page keys, then one page counter per (request, KV head)
+  *workspace_bytes = tgi::align_up((int64_t)batch * H * n_pages * 4, 256) + tgi::align_up((int64_t)batch * H * 4, 256);
   return tgi::ok();
 }
 
@@ -559,14 +637,28 @@ extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, i
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(minmax) | reinterpret_cast<uintptr_t>(workspace)) & 15)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: q, minmax and workspace must be 16-byte aligned");
   if ((int64_t)batch * H * n_pages > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: page ids overflow int32");
-  const int64_t need = (int64_t)batch * H * n_pages * 4;
+  const int64_t keys_bytes = tgi::align_up((int64_t)batch * H * n_pages * 4, 256);
+  const int64_t need = keys_bytes + tgi::align_up((int64_t)batch * H * 4, 256);
   if (workspace_bytes < need)
     return tgi::fail(TG_ERR_CAPACITY, "tg_page_score_topk: workspace %lld < %lld bytes", (long long)workspace_bytes,
                      (long long)need);
-  ScoreArgs a{q, minmax, static_cast<uint32_t *>(workspace), dev_status, (int64_t)batch * H * n_pages, g, n_pages};
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  ScoreArgs a;
+  a.q = q;
+  a.minmax = minmax;
+  a.keys = reinterpret_cast<uint32_t *>(ws);
+  a.row_cnt = reinterpret_cast<int32_t *>(ws + keys_bytes);
+  a.sel = sel;
+  a.pt_ids = pt_ids;
+  a.status = dev_status;
+  a.units = (int64_t)batch * H * n_pages;
+  a.g = g;
+  a.n_pages = n_pages;
+  a.K = K;
+  a.fused = n_pages <= 32 * kWarpKeysMax;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = d == 128 ? launch_score_d<128>(a, s) : launch_score_d<256>(a, s);
-  if (e == cudaSuccess) e = launch_select(a.keys, batch * H, n_pages, K, sel, pt_ids, s);
+  if (e == cudaSuccess && !a.fused) e = launch_select(a.keys, batch * H, n_pages, K, sel, pt_ids, s);
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_page_score_topk: %s", cudaGetErrorString(e));
   return tgi::ok();
 }

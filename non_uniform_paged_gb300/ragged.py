@@ -109,7 +109,7 @@ class SparseDecoder:
         self.pt_off = torch.arange(0, batch * H * K + 1, K, dtype=torch.int64, device=dev)
         self.sel = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
         self.pt_ids = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
-        self.score_ws = torch.empty(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=dev)
+        self.score_ws = torch.zeros(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(d)
 
     def select(self, q, minmax, stream=None):

@@ -97,6 +97,13 @@ def test_page_topk_tiny_rows(lib, cuda, n_pages, K):
     _select_case(lib, cuda, 7, 5, 4, 128, n_pages, K, seed=n_pages * 10 + K)
 
 
+@pytest.mark.parametrize("n_pages,K", [(1, 1), (2, 1)])
+def test_page_topk_more_rows_than_a_cta_queues(lib, cuda, n_pages, K):
+    """Tens of thousands of one- or two-page rows: each CTA completes far more rows than
+    its selection queue holds, so the overflow rescan selects the rest."""
+    _select_case(lib, cuda, 700, 30, 1, 128, n_pages, K, seed=11 + n_pages)
+
+
 def test_page_topk_many_rows(lib, cuda):
     """Hundreds of rows cut at arbitrary points by the even split over the CTAs' warps."""
     _select_case(lib, cuda, 37, 9, 2, 128, 101, 17, seed=5)
@@ -113,6 +120,28 @@ def test_page_topk_workspace_checks(lib, cuda):
     with pytest.raises(lib.TGError) as e:
         lib.tg_page_score_topk(batch, H, 2, 128, n_pages, K, q, mm, sel, workspace=small)
     assert "workspace" in str(e.value)
+
+
+@pytest.mark.parametrize("n_pages", [625, 3000])
+def test_page_topk_workspace_reused(lib, cuda, n_pages):
+    """Consecutive calls on one workspace (the per-row page counters return to zero)."""
+    batch, H, g, d, K = 5, 3, 4, 128, 40
+    ws = torch.zeros(lib.tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=cuda)
+    gen = torch.Generator(device=cuda)
+    for call in range(3):
+        gen.manual_seed(100 + call)
+        q = torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16)
+        mm = torch.randn((batch, H, n_pages, 2, d), generator=gen, device=cuda).to(torch.bfloat16)
+        mm = torch.stack([torch.minimum(mm[:, :, :, 0], mm[:, :, :, 1]),
+                          torch.maximum(mm[:, :, :, 0], mm[:, :, :, 1])], 3).contiguous()
+        sel = torch.full((batch, H, K), -1, dtype=torch.int32, device=cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        lib.tg_page_score_topk(batch, H, g, d, n_pages, K, q, mm, sel, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(status) == 0
+        q_h, mm_h = q.float().cpu().numpy(), mm.float().cpu().numpy()
+        ref = ofx.select_pages(q_h, mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
+        assert np.array_equal(sel.cpu().numpy(), ref), call
 
 
 def test_page_topk_nan_sets_status(lib, cuda):
