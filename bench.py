@@ -527,6 +527,7 @@ def bench_sparse(args, w, rank, world, local, device):
             "decode_gbs": kv_bytes / (statistics.mean(att_ms) * 1e-3) / 1e9,
             "bytes_per_step": step_bytes}
         del dec
+    rerank = bench_rerank(args, w, q, mms, pools, out, stream, results, device)
     if rank != 0:
         return
     best = results[f"K{w.topk_pages[0]}"]
@@ -539,8 +540,67 @@ def bench_sparse(args, w, rank, world, local, device):
             "pct_of_hbm_peak": best["pct_of_hbm_peak"],
             "sparse_vs_dense_speedup": {k: results["dense"]["ms_per_step"] / v["ms_per_step"]
                                         for k, v in results.items() if k != "dense"},
-            "variants": results, "peak": peak, "peak_kind": peak_kind}
+            "variants": results, "rerank": rerank, "peak": peak, "peak_kind": peak_kind}
     print(json.dumps(line), flush=True)
+
+
+def bench_rerank(args, w, q, mms, pools, out, stream, results, device):
+    """Stability-aware rerank at K = topk_pages[0]: 25% of the (layer, KV head) pairs are
+    unstable (seeded permutation) and re-ranked every step, the stable ones every 16 steps
+    (all requests together, or one request phase per step).  Times whole 16-step windows
+    (score launches only for the rows due, none for a layer with no rows due) against the
+    every-step full rerank and against decode with no scoring at all."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, RerankSchedule
+    K_sel, n_pages, period = w.topk_pages[0], w.N // w.P, 16
+    pairs = np.random.default_rng(w.seed + 77).permutation(w.L * w.H)[:(w.L * w.H) // 4]
+    unstable = np.zeros((w.L, w.H), np.uint8)
+    unstable.flat[pairs] = 1
+    dec = SparseDecoder(w.batch, w.H, w.H_q, w.d, w.P, n_pages, K_sel, device=device, layers=w.L)
+    for l in range(w.L):  # every layer starts from a full selection
+        dec.select(q[l], mms[l], stream=stream, layer=l)
+    out_rr = {"unstable_pairs": int(unstable.sum()), "pairs": w.L * w.H, "period": period,
+              "every_step_ms": results[f"K{K_sel}"]["ms_per_step"]}
+    windows = max(2, args.steps // 100)
+
+    def timed(fn):
+        for t in range(period):
+            fn(t)
+        torch.cuda.synchronize()
+        a, b = _events(2)
+        a.record(stream)
+        for t in range(windows * period):
+            fn(t)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (windows * period)
+
+    def decode_only(t):
+        for l in range(w.L):
+            dec.attend(q[l], pools[l], out, stream=stream, layer=l)
+    out_rr["decode_only_ms"] = timed(decode_only)
+    for stagger in (0, 1):
+        sched = RerankSchedule(unstable, w.batch, period=period, stagger=stagger, device=device)
+
+        def step(t):
+            for l in range(w.L):
+                rows, n = sched.rows(l, t)
+                dec.select_rows(q[l], mms[l], rows, n, stream=stream, layer=l)
+                dec.attend(q[l], pools[l], out, stream=stream, layer=l)
+        ms = timed(step)
+        rows_per_step = float(sched.counts.sum()) / period
+        out_rr[f"stagger{stagger}"] = {
+            "ms_per_step": ms,
+            "scored_rows_per_step": rows_per_step,
+            "scored_fraction": rows_per_step / (w.L * w.batch * w.H),
+            "score_launches_per_step": float((sched.counts > 0).sum()) / period,
+            "speedup_vs_every_step": out_rr["every_step_ms"] / ms,
+            "scoring_ms_per_step": ms - out_rr["decode_only_ms"],
+            "scoring_speedup_vs_every_step": (out_rr["every_step_ms"] - out_rr["decode_only_ms"])
+                                             / max(1e-9, ms - out_rr["decode_only_ms"])}
+    tg_check = __import__("non_uniform_paged_gb300").tg_check_status
+    tg_check(dec.status)
+    del dec
+    return out_rr
 
 
 def bench_layerwise(args, w, rank, world, local, device):

@@ -127,12 +127,22 @@ int tg_query_ncta(int d, int g, int *N_CTA);
  *   tg_plan_header | tg_plan_layer[L] | per layer: int32 cta_off[N_CTA+1], tg_work_item[]
  * (every section 16-byte aligned; offsets are in bytes from the buffer start). */
 #define TG_PLAN_MAGIC 0x31504754u /* "TGP1" */
+#define TG_PLAN_VERSION 2
+
+/* Plan flag: each tg_decode_attn launch of this plan waits for the previous
+ * kernel in the stream to complete before it reads q, pt_off or pt_ids (it
+ * still starts early and reads the plan).  Set it when that kernel writes them
+ * and lets the next kernel start early, as tg_page_score_topk does with
+ * TG_SCORE_LET_NEXT_START. */
+#define TG_PLAN_WAIT_TABLES 0x1u
 
 typedef struct tg_plan_header {
   uint32_t magic;
   int32_t version;
   int32_t L, batch, H, H_q, H_p, P, d, G, N_CTA;
   int32_t max_slots;       /* most partial slots any layer uses */
+  uint32_t flags;          /* TG_PLAN_* (tg_plan_set_flags); 0 from tg_plan_decode */
+  int32_t reserved;
   int64_t plan_bytes;      /* size of the whole buffer */
   int64_t workspace_bytes; /* device workspace tg_decode_attn needs */
   int64_t layers;          /* byte offset of tg_plan_layer[L] */
@@ -165,6 +175,10 @@ typedef struct tg_work_item {
 int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, int d, int N_CTA,
                    const int32_t *S, const int32_t *head_order, const int32_t *ntok,
                    void *plan, int64_t plan_cap, int64_t *plan_bytes, int64_t *workspace_bytes);
+
+/* tg_plan_set_flags -- set the TG_PLAN_* flags of a plan (host buffer; the
+ *   device copy needs no update: only the host launch reads them). */
+int tg_plan_set_flags(void *plan_host, uint32_t flags);
 
 /* ------------------------------------------------------------- a5 + a6 ---
  * tg_decode_attn -- split-KV flash decoding of one layer over the ragged pool,
@@ -200,7 +214,9 @@ int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, int d, int 
  *   previous tg_decode_attn launch in the stream is finishing: before waiting
  *   for that launch it reads the plan, page tables, pool and q (never written
  *   by a decode launch); it waits before it touches the workspace, out or lse.
- *   Kernels other than tg_decode_attn complete before it starts, as usual. */
+ *   Other kernels complete before it starts, unless they let it start early
+ *   (tg_page_score_topk with TG_SCORE_LET_NEXT_START): the plan must then carry
+ *   TG_PLAN_WAIT_TABLES, and the launch waits before it reads q and the tables. */
 int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
                    const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
                    const int64_t *pt_off, const int32_t *pt_ids, float scale,
@@ -263,11 +279,39 @@ int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d,
  *   selected by a second kernel.  Programmatic dependent launch: the call may
  *   start while the previous kernel in the stream (a tg_decode_attn of the
  *   previous layer) finishes, reading q and minmax and writing only the
- *   workspace; it waits for that kernel before writing sel and pt_ids, and it
- *   does not let the next kernel start before sel and pt_ids are complete. */
+ *   workspace; it waits for that kernel before writing sel and pt_ids.
+ *   flags: 0, or TG_SCORE_LET_NEXT_START to let the next kernel in the stream
+ *   start before sel and pt_ids are complete; that kernel must then wait for
+ *   this one before reading them (tg_decode_attn with a plan flagged
+ *   TG_PLAN_WAIT_TABLES does).  Without the flag the next kernel starts only
+ *   when sel and pt_ids are complete. */
+#define TG_SCORE_LET_NEXT_START 0x1u
 int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                        const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
-                       void *workspace, int64_t workspace_bytes, int32_t *dev_status);
+                       void *workspace, int64_t workspace_bytes, uint32_t flags, int32_t *dev_status);
+
+/* tg_page_score_topk_rows -- tg_page_score_topk restricted to a list of rows.
+ *   [FlexiCache] "Stability-aware rerank frequency": only the heads due for a
+ *   rerank are scored; every other row keeps its previous sel / pt_ids.
+ *   rows: device int32 [n_rows], distinct row numbers b*H + h in [0, batch*H)
+ *   (an entry outside that range sets TG_STATUS_BAD_INPUT and is skipped).
+ *   n_rows = 0 launches nothing.  Everything else as tg_page_score_topk, with
+ *   sel / pt_ids still indexed by row (only the listed rows are written). */
+int tg_page_score_topk_rows(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
+                            int n_rows, const int32_t *rows, const uint16_t *q, const uint16_t *minmax,
+                            int32_t *sel, int32_t *pt_ids, void *workspace, int64_t workspace_bytes,
+                            uint32_t flags, int32_t *dev_status);
+
+/* tg_rerank_rows -- the rows of one layer due for a rerank at a decode step (host).
+ *   [FlexiCache] "Core method" (stable heads re-ranked every 16 steps, unstable
+ *   heads every step; all-stable layers skip scoring).
+ *   unstable uint8 [L][H] (1 = unstable).  Row b*H + h is listed when head h of
+ *   the layer is unstable, or when (step + b*stagger) % period == 0 (stagger 0:
+ *   every request's stable heads together, so an all-stable layer has no rows at
+ *   15 of 16 steps; stagger 1: one request phase per step).  rows (host, capacity
+ *   batch*H) in (b, h) order; *n_rows = the count (0: skip the layer). */
+int tg_rerank_rows(int L, int batch, int H, const uint8_t *unstable, int layer, int step, int period,
+                   int stagger, int32_t *rows, int32_t *n_rows);
 
 /* tg_page_score_workspace -- bytes of workspace tg_page_score_topk needs for
  *   batch x H rows of n_pages pages (host only). */

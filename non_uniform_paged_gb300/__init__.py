@@ -20,11 +20,14 @@ from . import _build
 
 __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
-           "tg_page_score_workspace",
+           "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
+           "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
 STATUS_NONFINITE, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_INPUT = 0x1, 0x2, 0x4, 0x8
+PLAN_WAIT_TABLES = 0x1       # tg.h TG_PLAN_WAIT_TABLES
+SCORE_LET_NEXT_START = 0x1   # tg.h TG_SCORE_LET_NEXT_START
 PLAN_MAGIC = 0x31504754
 
 _lib: Optional[ctypes.CDLL] = None
@@ -45,8 +48,12 @@ _SIGS = {
     "tg_decode_attn_static_scratch": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _P, _P, _P]),
     "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]),
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
-    "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, _P]),
+    "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, ctypes.c_uint32, _P]),
+    "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
     "tg_page_score_workspace": (_I, [_I, _I, _I, _P]),
+    "tg_page_score_topk_rows": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _L, ctypes.c_uint32,
+                                     _P]),
+    "tg_rerank_rows": (_I, [_I, _I, _I, _P, _I, _I, _I, _I, _P, _P]),
     "tg_check_status": (_I, [_P, _P]),
 }
 
@@ -168,7 +175,8 @@ def tg_plan_decode(S, head_order, ntok, H_q: int, H_p: int, P: int, d: int):
 
 _HEADER_DTYPE = np.dtype([("magic", "<u4"), ("version", "<i4"), ("L", "<i4"), ("batch", "<i4"), ("H", "<i4"),
                           ("H_q", "<i4"), ("H_p", "<i4"), ("P", "<i4"), ("d", "<i4"), ("G", "<i4"),
-                          ("N_CTA", "<i4"), ("max_slots", "<i4"), ("plan_bytes", "<i8"),
+                          ("N_CTA", "<i4"), ("max_slots", "<i4"), ("flags", "<u4"), ("reserved", "<i4"),
+                          ("plan_bytes", "<i8"),
                           ("workspace_bytes", "<i8"), ("layers", "<i8")])
 _LAYER_DTYPE = np.dtype([("cta_off", "<i8"), ("items", "<i8"), ("n_items", "<i4"), ("n_slots", "<i4")])
 WORK_ITEM_DTYPE = np.dtype([("b", "<i4"), ("h", "<i4"), ("hpos", "<i4"), ("g", "<i4"), ("t0", "<i4"),
@@ -255,6 +263,14 @@ def tg_build_minmax(batch, H, N, P, d, K, minmax, dev_status=None, stream=None):
                                _dev(minmax, torch.bfloat16, "minmax"), _dev(dev_status, torch.int32, "dev_status")))
 
 
+def tg_plan_set_flags(plan: np.ndarray, flags: int) -> None:
+    """Set a plan's TG_PLAN_* flags in its host buffer (tg.h: tg_plan_set_flags)."""
+    lib = load()
+    if not (isinstance(plan, np.ndarray) and plan.dtype == np.uint8 and plan.flags["C_CONTIGUOUS"]):
+        raise TypeError("plan must be the contiguous uint8 array tg_plan_decode returned")
+    _check(lib.tg_plan_set_flags(plan.ctypes.data, int(flags)))
+
+
 def tg_page_score_workspace(batch, H, n_pages) -> int:
     """Workspace bytes tg_page_score_topk needs (tg.h: tg_page_score_workspace)."""
     lib = load()
@@ -264,7 +280,7 @@ def tg_page_score_workspace(batch, H, n_pages) -> int:
 
 
 def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, workspace=None, dev_status=None,
-                       stream=None):
+                       stream=None, flags=0):
     """Quest page bound + per-KV-head top-K pages (tg.h: tg_page_score_topk).  Without a
     workspace, a zero-filled one of tg_page_score_workspace bytes is allocated for the call."""
     import torch
@@ -274,8 +290,37 @@ def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, 
     _check(lib.tg_page_score_topk(_stream(stream), batch, H, g, d, n_pages, K, _dev(q, torch.bfloat16, "q"),
                                   _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
                                   _dev(pt_ids, torch.int32, "pt_ids"), _dev(workspace, torch.uint8, "workspace"),
-                                  workspace.numel() * workspace.element_size(),
+                                  workspace.numel() * workspace.element_size(), int(flags),
                                   _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows, n_rows, q, minmax, sel, pt_ids=None, workspace=None,
+                            dev_status=None, stream=None, flags=0):
+    """tg_page_score_topk over the listed rows only (tg.h: tg_page_score_topk_rows).  rows is a
+    device int32 tensor whose first n_rows entries are used."""
+    import torch
+    lib = load()
+    if workspace is None:
+        workspace = torch.zeros(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=q.device)
+    _check(lib.tg_page_score_topk_rows(_stream(stream), batch, H, g, d, n_pages, K, int(n_rows),
+                                       _dev(rows, torch.int32, "rows"), _dev(q, torch.bfloat16, "q"),
+                                       _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
+                                       _dev(pt_ids, torch.int32, "pt_ids"), _dev(workspace, torch.uint8, "workspace"),
+                                       workspace.numel() * workspace.element_size(), int(flags),
+                                       _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_rerank_rows(unstable, batch, layer, step, period=16, stagger=0) -> np.ndarray:
+    """Rows of one layer due for a rerank at a decode step (tg.h: tg_rerank_rows).
+    unstable: uint8/bool [L][H].  Returns int32 row numbers b*H + h."""
+    lib = load()
+    u = np.ascontiguousarray(np.asarray(unstable, dtype=np.uint8))
+    L, H = u.shape
+    rows = np.empty(max(1, batch * H), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib.tg_rerank_rows(L, batch, H, u.ctypes.data, layer, step, period, stagger, rows.ctypes.data,
+                              ctypes.addressof(n)))
+    return rows[:n.value].copy()
 
 
 def tg_check_status(dev_status) -> int:

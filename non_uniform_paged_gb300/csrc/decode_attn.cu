@@ -59,6 +59,7 @@ struct DecodeArgs {
   int64_t *cta_time;
   int H, H_q, g, G, H_p, P;
   float scale_log2;
+  int wait_tables;  // wait for the previous kernel before reading q, pt_off, pt_ids
 };
 
 template <int D>
@@ -136,13 +137,13 @@ __global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
   const int i_begin = a.cta_off[cta];
   const int n_items = a.cta_off[cta + 1] - i_begin;
   const bool items_in_smem = n_items <= kMaxItems;
-  if (items_in_smem) {
-    for (int i = tid; i < n_items; i += NT) {
-      const tg_work_item it = a.items[i_begin + i];
-      s_items[i] = it;
-      s_base[i] = __ldcg(a.pt_off + it.b * a.G + it.g);
-    }
-  }
+  if (items_in_smem)
+    for (int i = tid; i < n_items; i += NT) s_items[i] = a.items[i_begin + i];
+  // page tables written by the kernel just before this one (which let this grid start
+  // early): wait for it first
+  if (a.wait_tables) griddep_wait();
+  if (items_in_smem)
+    for (int i = tid; i < n_items; i += NT) s_base[i] = __ldcg(a.pt_off + s_items[i].b * a.G + s_items[i].g);
   if (lane == 0) {
     for (int s = 0; s < R; ++s) mbar_init(&bars[warp * R + s], 1);
   }
@@ -533,7 +534,7 @@ extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const v
   if (!plan_host || !plan_dev || !q || !pool || !pt_off || !pt_ids || !workspace || !out)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: NULL pointer argument");
   const tg_plan_header *hd = static_cast<const tg_plan_header *>(plan_host);
-  if (hd->magic != TG_PLAN_MAGIC || hd->version != 1)
+  if (hd->magic != TG_PLAN_MAGIC || hd->version != TG_PLAN_VERSION)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: plan_host is not a tg_plan_decode buffer");
   if (layer < 0 || layer >= hd->L) return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn: layer %d of %d", layer, hd->L);
   if (!std::isfinite(scale)) return tgi::fail(TG_ERR_NONFINITE, "tg_decode_attn: scale is not finite");
@@ -591,6 +592,7 @@ extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const v
   args.H_p = hd->H_p;
   args.P = hd->P;
   args.scale_log2 = scale * kLog2e;
+  args.wait_tables = (hd->flags & TG_PLAN_WAIT_TABLES) != 0;
   // without a caller status word, faults are recorded in the workspace's own
   if (!dev_status) args.status = reinterpret_cast<int32_t *>(ws + wl.status);
   void *params[] = {&map, &args};
@@ -660,7 +662,7 @@ extern "C" int tg_decode_attn_static_scratch(tg_stream_t stream, const void *pla
   if (!plan_host || !plan_dev || !q || !pool || !pt_off || !pt_ids || !out)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: NULL pointer argument");
   const tg_plan_header *hd = static_cast<const tg_plan_header *>(plan_host);
-  if (hd->magic != TG_PLAN_MAGIC || hd->version != 1)
+  if (hd->magic != TG_PLAN_MAGIC || hd->version != TG_PLAN_VERSION)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: plan_host is not a tg_plan_decode buffer");
   if (layer < 0 || layer >= hd->L)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: layer %d of %d", layer, hd->L);
@@ -727,6 +729,7 @@ extern "C" int tg_decode_attn_static_scratch(tg_stream_t stream, const void *pla
   args.H_p = hd->H_p;
   args.P = hd->P;
   args.scale_log2 = scale * kLog2e;
+  args.wait_tables = (hd->flags & TG_PLAN_WAIT_TABLES) != 0;
   void *params[] = {&map, &args};
   e = cudaLaunchKernel(fn, dim3(hd->N_CTA), dim3(threads), params, (size_t)smem, st);
   if (e != cudaSuccess)

@@ -65,9 +65,12 @@ struct ScoreArgs {
   int32_t *row_cnt;    // [rows] pages scored so far (workspace, zero between calls)
   int32_t *sel, *pt_ids;
   int32_t *status;
-  int64_t units;       // rows * n_pages
+  const int32_t *rows; // the (request, KV head) rows to score, in list order (NULL: all, in order)
+  int64_t total_rows;  // batch * H: listed rows outside [0, total_rows) are reported and skipped
+  int64_t units;       // listed rows * n_pages
   int g, n_pages, K;
   int fused;           // the warp that completes a row selects its top K (n_pages <= 1024)
+  int let_next;        // let the next kernel start early (it waits before reading sel / pt_ids)
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
   // with a separate select kernel next, it may be scheduled now (it waits for this grid
   // before reading keys); with the select fused in, the next kernel (a decode reading the
   // page lists before it waits) starts only when this grid is done
-  if (!a.fused) griddep_launch_dependents();
+  if (!a.fused || a.let_next) griddep_launch_dependents();
 
   // this warp's units [u0, u1)
   const int64_t c0 = (int64_t)blockIdx.x * a.units / gridDim.x;
@@ -242,12 +245,33 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
   fence_barrier_init();
   __syncwarp();
   const uint8_t *src = reinterpret_cast<const uint8_t *>(a.minmax);
-  auto issue = [&](int st) {  // lane 0: stage st of this warp
+  // row of list position lr (the rows of a listed call need not be adjacent in memory)
+  auto row_id = [&](int64_t lr) -> int64_t {
+    if (!a.rows) return lr;
+    const int64_t r = __ldcg(a.rows + lr);
+    return r >= 0 && r < a.total_rows ? r : -1;
+  };
+  auto issue = [&](int st) {  // lane 0: stage st of this warp, one bulk copy per row it touches
     const int64_t us = u0 + (int64_t)st * SP;
-    const uint32_t bytes = (uint32_t)(min((int64_t)SP, u1 - us) * PAGE);
+    const int cnt = (int)min((int64_t)SP, u1 - us);
     uint64_t *bar = &wbar[st % R];
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(wring + (st % R) * STAGE, src + us * PAGE, bytes, bar);
+    uint8_t *dst = wring + (st % R) * STAGE;
+    mbar_arrive_expect_tx(bar, (uint32_t)(cnt * PAGE));
+    if (!a.rows) {
+      bulk_load(dst, src + us * PAGE, (uint32_t)(cnt * PAGE), bar);
+      return;
+    }
+    for (int done = 0; done < cnt;) {
+      const int64_t u = us + done, lr = u / a.n_pages, pg = u - lr * a.n_pages;
+      const int seg = (int)min((int64_t)(cnt - done), a.n_pages - pg);
+      int64_t r = row_id(lr);
+      if (r < 0) {  // a listed row out of range: read row 0 instead, select nothing for it
+        report(a.status, TG_STATUS_BAD_INPUT);
+        r = 0;
+      }
+      bulk_load(dst + done * PAGE, src + (r * a.n_pages + pg) * PAGE, (uint32_t)(seg * PAGE), bar);
+      done += seg;
+    }
   };
   if (lane == 0)
     for (int st = 0; st < R && st < nst; ++st) issue(st);
@@ -264,7 +288,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
 #pragma unroll
     for (int i = 0; i < GQ; ++i) {
       const int qi = i < a.g ? i : 0;  // heads past g repeat head 0: the max is unchanged
-      const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + ((size_t)row * a.g + qi) * D + j * W);
+      const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + ((size_t)max(row_id(row), (int64_t)0) * a.g + qi) * D + j * W);
 #pragma unroll
       for (int v = 0; v < WV; ++v) {
         const uint4 x = __ldcg(qs + v);
@@ -467,7 +491,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
       griddep_wait();    // the previous kernel (a decode) may still read sel / pt_ids
       for (int i = warp; i < nq; i += NW) {
         const int64_t r = s_rows[i];
-        warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, r, a.sel, a.pt_ids);
+        const int64_t out = row_id(r);
+        if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids);
         if (lane == 0) a.row_cnt[r] = 0;
       }
     }
@@ -484,7 +509,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
         if (__shfl_sync(0xffffffffu, mine_row, 0)) {
           __threadfence();
           griddep_wait();
-          warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, r, a.sel, a.pt_ids);
+          const int64_t out = row_id(r);
+          if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids);
           if (lane == 0) a.row_cnt[r] = 0;
         }
       }
@@ -496,15 +522,18 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
 }
 
 // One CTA per (request, KV head): top-K of the row's keys, ascending, ties to the lower page.
-__global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t *keys, int n_pages, int K,
+__global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t *keys, const int32_t *rows,
+                                                                  int64_t total_rows, int n_pages, int K,
                                                                   int32_t *sel, int32_t *pt_ids) {
   extern __shared__ uint32_t skeys[];  // [n_pages]
   __shared__ int hist[256];
   __shared__ int scan[33];
   __shared__ int sel_scratch[4];
-  const int row = blockIdx.x, tid = threadIdx.x;
+  const int row = blockIdx.x, tid = threadIdx.x;  // list position
+  const int64_t out_row = rows ? (int64_t)__ldcg(rows + row) : row;  // checked by the score kernel
   // the keys are written by the score kernel just before this one
   griddep_wait();
+  if (out_row < 0 || out_row >= total_rows) return;
   const uint32_t *rk = keys + (size_t)row * n_pages;
   for (int i = tid; i < n_pages; i += kSelThreads) skeys[i] = __ldcg(rk + i);
   __syncthreads();
@@ -521,8 +550,8 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t
     const bool take = gt || (eq && eq_rank < need_eq);
     const int k = taken + block_excl_count<kSelThreads>(take, scan, sel_total);
     if (take) {
-      sel[(size_t)row * K + k] = p;
-      if (pt_ids) pt_ids[(size_t)row * K + k] = row * n_pages + p;
+      sel[(size_t)out_row * K + k] = p;
+      if (pt_ids) pt_ids[(size_t)out_row * K + k] = (int32_t)(out_row * n_pages + p);
     }
     taken += sel_total;
     eq_seen += eq_total;
@@ -570,8 +599,8 @@ cudaError_t launch_score_d(const ScoreArgs &a, cudaStream_t s) {
   return launch_score<D, 8>(a, s);
 }
 
-cudaError_t launch_select(const uint32_t *keys, int rows, int n_pages, int K, int32_t *sel, int32_t *pt_ids,
-                          cudaStream_t s) {
+cudaError_t launch_select(const uint32_t *keys, const int32_t *rows, int64_t total_rows, int n_rows, int n_pages,
+                          int K, int32_t *sel, int32_t *pt_ids, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxPages * 4);
   if (e != cudaSuccess) return e;
@@ -583,10 +612,10 @@ cudaError_t launch_select(const uint32_t *keys, int rows, int n_pages, int K, in
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(rows);
+  cfg.gridDim = dim3(n_rows);
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = (size_t)n_pages * 4;
-  return cudaLaunchKernelEx(&cfg, page_select_kernel, keys, n_pages, K, sel, pt_ids);
+  return cudaLaunchKernelEx(&cfg, page_select_kernel, keys, rows, total_rows, n_pages, K, sel, pt_ids);
 }
 
 // minmax[b][h][p][0][:] = min over the page's valid keys, [1][:] = max (exact in bf16)
@@ -624,24 +653,26 @@ extern "C" int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *w
   return tgi::ok();
 }
 
-extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
-                                  const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
-                                  void *workspace, int64_t workspace_bytes, int32_t *dev_status) {
-  if (batch < 0 || H <= 0 || g < 1 || g > 8) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: bad batch/H/g");
-  if (d != 128 && d != 256) return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: d=%d (128 or 256)", d);
+namespace {
+int score_topk(const char *fn, tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K, int n_rows,
+               const int32_t *rows, const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
+               void *workspace, int64_t workspace_bytes, uint32_t flags, int32_t *dev_status) {
+  if (flags & ~TG_SCORE_LET_NEXT_START) return tgi::fail(TG_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
+  if (batch < 0 || H <= 0 || g < 1 || g > 8) return tgi::fail(TG_ERR_INVALID_ARG, "%s: bad batch/H/g", fn);
+  if (d != 128 && d != 256) return tgi::fail(TG_ERR_SHAPE, "%s: d=%d (128 or 256)", fn, d);
   if (n_pages < 1 || n_pages > kMaxPages || K < 1 || K > n_pages)
-    return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: need 1 <= K=%d <= n_pages=%d <= %d", K, n_pages, kMaxPages);
-  if (batch == 0) return tgi::ok();
-  if (!q || !minmax || !sel || !workspace)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: NULL q/minmax/sel/workspace");
+    return tgi::fail(TG_ERR_SHAPE, "%s: need 1 <= K=%d <= n_pages=%d <= %d", fn, K, n_pages, kMaxPages);
+  if (n_rows < 0 || (int64_t)n_rows > (int64_t)batch * H)
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: n_rows=%d outside [0, batch*H]", fn, n_rows);
+  if (batch == 0 || n_rows == 0) return tgi::ok();
+  if (!q || !minmax || !sel || !workspace) return tgi::fail(TG_ERR_INVALID_ARG, "%s: NULL q/minmax/sel/workspace", fn);
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(minmax) | reinterpret_cast<uintptr_t>(workspace)) & 15)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk: q, minmax and workspace must be 16-byte aligned");
-  if ((int64_t)batch * H * n_pages > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_page_score_topk: page ids overflow int32");
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: q, minmax and workspace must be 16-byte aligned", fn);
+  if ((int64_t)batch * H * n_pages > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "%s: page ids overflow int32", fn);
   const int64_t keys_bytes = tgi::align_up((int64_t)batch * H * n_pages * 4, 256);
   const int64_t need = keys_bytes + tgi::align_up((int64_t)batch * H * 4, 256);
   if (workspace_bytes < need)
-    return tgi::fail(TG_ERR_CAPACITY, "tg_page_score_topk: workspace %lld < %lld bytes", (long long)workspace_bytes,
-                     (long long)need);
+    return tgi::fail(TG_ERR_CAPACITY, "%s: workspace %lld < %lld bytes", fn, (long long)workspace_bytes, (long long)need);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   ScoreArgs a;
   a.q = q;
@@ -651,16 +682,36 @@ extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, i
   a.sel = sel;
   a.pt_ids = pt_ids;
   a.status = dev_status;
-  a.units = (int64_t)batch * H * n_pages;
+  a.rows = rows;
+  a.total_rows = (int64_t)batch * H;
+  a.units = (int64_t)n_rows * n_pages;
   a.g = g;
   a.n_pages = n_pages;
   a.K = K;
   a.fused = n_pages <= 32 * kWarpKeysMax;
+  a.let_next = (flags & TG_SCORE_LET_NEXT_START) != 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = d == 128 ? launch_score_d<128>(a, s) : launch_score_d<256>(a, s);
-  if (e == cudaSuccess && !a.fused) e = launch_select(a.keys, batch * H, n_pages, K, sel, pt_ids, s);
-  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_page_score_topk: %s", cudaGetErrorString(e));
+  if (e == cudaSuccess && !a.fused) e = launch_select(a.keys, rows, a.total_rows, n_rows, n_pages, K, sel, pt_ids, s);
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return tgi::ok();
+}
+}  // namespace
+
+extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
+                                  const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
+                                  void *workspace, int64_t workspace_bytes, uint32_t flags, int32_t *dev_status) {
+  return score_topk("tg_page_score_topk", stream, batch, H, g, d, n_pages, K, batch * H, nullptr, q, minmax, sel,
+                    pt_ids, workspace, workspace_bytes, flags, dev_status);
+}
+
+extern "C" int tg_page_score_topk_rows(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
+                                       int n_rows, const int32_t *rows, const uint16_t *q, const uint16_t *minmax,
+                                       int32_t *sel, int32_t *pt_ids, void *workspace, int64_t workspace_bytes,
+                                       uint32_t flags, int32_t *dev_status) {
+  if (n_rows > 0 && !rows) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk_rows: NULL rows");
+  return score_topk("tg_page_score_topk_rows", stream, batch, H, g, d, n_pages, K, n_rows, rows, q, minmax, sel,
+                    pt_ids, workspace, workspace_bytes, flags, dev_status);
 }
 
 extern "C" int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d, const uint16_t *K,

@@ -305,7 +305,7 @@ extern "C" int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, 
   tg_plan_header hd;
   std::memset(&hd, 0, sizeof hd);
   hd.magic = TG_PLAN_MAGIC;
-  hd.version = 1;
+  hd.version = TG_PLAN_VERSION;
   hd.L = L; hd.batch = batch; hd.H = H; hd.H_q = H_q; hd.H_p = H_p; hd.P = P; hd.d = d; hd.G = G;
   hd.N_CTA = N_CTA;
   hd.max_slots = max_slots;
@@ -319,5 +319,37 @@ extern "C" int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, 
     if (!items[l].empty())
       std::memcpy(base + lt[l].items, items[l].data(), items[l].size() * sizeof(tg_work_item));
   }
+  return tgi::ok();
+}
+
+// ---------------------------------------------------------------------------
+// Stability-aware rerank schedule ("FlexiCache ... (MLSys 2026)", paper-review
+// page, "Core method / Tiered KV placement" and "Stability-aware rerank
+// frequency"): an unstable head is re-scored every decode step; a stable head
+// only every `period` steps, request b at the steps where (step + b * stagger)
+// % period == 0.  Rows are (b, h) -> b * H + h, listed by b then h.
+extern "C" int tg_rerank_rows(int L, int batch, int H, const uint8_t *unstable, int layer, int step, int period,
+                              int stagger, int32_t *rows, int32_t *n_rows) {
+  if (L <= 0 || batch < 0 || H <= 0 || period <= 0 || step < 0 || (stagger != 0 && stagger != 1))
+    return fail(TG_ERR_INVALID_ARG, "tg_rerank_rows: bad L/batch/H/step/period/stagger");
+  if (layer < 0 || layer >= L) return fail(TG_ERR_INVALID_ARG, "tg_rerank_rows: layer %d of %d", layer, L);
+  if (!unstable || !n_rows || (!rows && batch > 0)) return fail(TG_ERR_INVALID_ARG, "tg_rerank_rows: NULL argument");
+  int32_t n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const bool stable_due = ((int64_t)step + (int64_t)b * stagger) % period == 0;
+    for (int h = 0; h < H; ++h)
+      if (unstable[(size_t)layer * H + h] || stable_due) rows[n++] = b * H + h;
+  }
+  *n_rows = n;
+  return tgi::ok();
+}
+
+extern "C" int tg_plan_set_flags(void *plan_host, uint32_t flags) {
+  if (!plan_host) return fail(TG_ERR_INVALID_ARG, "tg_plan_set_flags: NULL plan");
+  tg_plan_header *hd = static_cast<tg_plan_header *>(plan_host);
+  if (hd->magic != TG_PLAN_MAGIC || hd->version != TG_PLAN_VERSION)
+    return fail(TG_ERR_INVALID_ARG, "tg_plan_set_flags: not a tg_plan_decode buffer");
+  if (flags & ~TG_PLAN_WAIT_TABLES) return fail(TG_ERR_INVALID_ARG, "tg_plan_set_flags: unknown flags 0x%x", flags);
+  hd->flags = flags;
   return tgi::ok();
 }

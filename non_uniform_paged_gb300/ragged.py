@@ -22,7 +22,9 @@ import numpy as np
 import torch
 
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
-               tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace)
+               tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
+               tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
+               SCORE_LET_NEXT_START)
 
 BYTES_BF16 = 2
 
@@ -90,11 +92,15 @@ class RaggedCache:
 
 
 class SparseDecoder:
-    """Top-K page sparse decode over a dense cache [batch][H][n_pages][2][P][d] (H_p = 1 tables)."""
+    """Top-K page sparse decode over a dense cache [batch][H][n_pages][2][P][d] (H_p = 1 tables).
 
-    def __init__(self, batch, H, H_q, d, P, n_pages, K, n_cta=None, device="cuda"):
+    One selection (sel / pt_ids) per layer, so a layer whose heads are not all re-ranked at a
+    step keeps the pages the others selected earlier (stability-aware rerank)."""
+
+    def __init__(self, batch, H, H_q, d, P, n_pages, K, n_cta=None, device="cuda", layers=1, overlap=False):
         self.batch, self.H, self.H_q, self.d, self.P, self.n_pages, self.K = batch, H, H_q, d, P, n_pages, K
         self.g = H_q // H
+        self.layers = layers
         dev = torch.device(device)
         self.n_cta = int(n_cta) if n_cta else tg_query_ncta(d, self.g)
         # every head attends K full pages: one plan serves every layer
@@ -103,35 +109,78 @@ class SparseDecoder:
         Phi = ntok.sum(axis=1).astype(np.int64)
         self.S = tg_split_map(Phi, self.n_cta)
         self.plan, self.workspace_bytes = tg_plan_decode(self.S, order, ntok, H_q, 1, P, d)
+        # overlap: the score call lets the decode launch start early; the decode then waits for
+        # the kernel before it before reading the page lists (the two flags go together).  Off by
+        # default: on GB300 it gains nothing after a score launch, and a decode that follows a
+        # decode (a layer with no rows to re-rank) then loses the decode-to-decode overlap
+        self.score_flags = SCORE_LET_NEXT_START if overlap else 0
+        if overlap:
+            tg_plan_set_flags(self.plan, PLAN_WAIT_TABLES)
         self.plan_dev = torch.from_numpy(self.plan).to(dev)
         self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.pt_off = torch.arange(0, batch * H * K + 1, K, dtype=torch.int64, device=dev)
-        self.sel = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
-        self.pt_ids = torch.empty(batch * H * K, dtype=torch.int32, device=dev)
+        self.sel = torch.empty((layers, batch * H * K), dtype=torch.int32, device=dev)
+        self.pt_ids = torch.empty((layers, batch * H * K), dtype=torch.int32, device=dev)
         self.score_ws = torch.zeros(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=dev)
         self.scale = 1.0 / math.sqrt(d)
 
-    def select(self, q, minmax, stream=None):
-        tg_page_score_topk(self.batch, self.H, self.g, self.d, self.n_pages, self.K, q, minmax, self.sel,
-                           pt_ids=self.pt_ids, workspace=self.score_ws, dev_status=self.status, stream=stream)
+    def select(self, q, minmax, stream=None, layer=0):
+        """Re-rank every (request, KV head) of a layer."""
+        tg_page_score_topk(self.batch, self.H, self.g, self.d, self.n_pages, self.K, q, minmax, self.sel[layer],
+                           pt_ids=self.pt_ids[layer], workspace=self.score_ws, dev_status=self.status, stream=stream,
+                           flags=self.score_flags)
 
-    def attend(self, q, pool, out, lse=None, cta_time=None, stream=None):
+    def select_rows(self, q, minmax, rows, n_rows, stream=None, layer=0):
+        """Re-rank only the listed rows b*H + h of a layer (device int32, first n_rows)."""
+        if n_rows == 0:
+            return
+        tg_page_score_topk_rows(self.batch, self.H, self.g, self.d, self.n_pages, self.K, rows, n_rows, q, minmax,
+                                self.sel[layer], pt_ids=self.pt_ids[layer], workspace=self.score_ws,
+                                dev_status=self.status, stream=stream, flags=self.score_flags)
+
+    def attend(self, q, pool, out, lse=None, cta_time=None, stream=None, layer=0):
         tg_decode_attn(self.plan, self.plan_dev, 0, q, pool, self.batch * self.H * self.n_pages, self.pt_off,
-                       self.pt_ids, self.scale, self.workspace, out, lse=lse, dev_status=self.status,
+                       self.pt_ids[layer], self.scale, self.workspace, out, lse=lse, dev_status=self.status,
                        cta_time=cta_time, stream=stream)
 
-    def step(self, q, minmax, pool, out, lse=None, stream=None):
-        self.select(q, minmax, stream=stream)
-        self.attend(q, pool, out, lse=lse, stream=stream)
+    def step(self, q, minmax, pool, out, lse=None, stream=None, layer=0):
+        self.select(q, minmax, stream=stream, layer=layer)
+        self.attend(q, pool, out, lse=lse, stream=stream, layer=layer)
 
-    def algorithmic_bytes(self) -> int:
-        """MinMax read + selected K/V pages + page ids + q and out, one layer."""
-        mm = self.batch * self.H * self.n_pages * 2 * self.d * BYTES_BF16
+    def algorithmic_bytes(self, scored_rows=None) -> int:
+        """MinMax read (of the scored rows; all by default) + selected K/V pages + page ids +
+        q and out, one layer."""
+        rows = self.batch * self.H if scored_rows is None else scored_rows
+        mm = rows * self.n_pages * 2 * self.d * BYTES_BF16
         kv = self.batch * self.H * self.K * self.P * 2 * self.d * BYTES_BF16
         ids = self.batch * self.H * self.K * 4
         qo = 2 * self.batch * self.H_q * self.d * BYTES_BF16
         return mm + kv + ids + qo
+
+
+class RerankSchedule:
+    """Device row lists of the stability-aware rerank ([FlexiCache] "Stability-aware rerank
+    frequency"): unstable heads every step, stable heads every `period` steps.  The schedule
+    repeats with the period, so the lists of steps 0 .. period-1 are built once (tg_rerank_rows)
+    and uploaded; rows(layer, step) returns (tensor, n) with n = 0 for a skipped layer."""
+
+    def __init__(self, unstable, batch, period=16, stagger=0, device="cuda"):
+        self.unstable = np.asarray(unstable, dtype=np.uint8)
+        self.L, self.H = self.unstable.shape
+        self.batch, self.period, self.stagger = batch, period, stagger
+        dev = torch.device(device)
+        self.lists = [[None] * period for _ in range(self.L)]
+        self.counts = np.zeros((self.L, period), dtype=np.int64)
+        for l in range(self.L):
+            for t in range(period):
+                r = tg_rerank_rows(self.unstable, batch, l, t, period, stagger)
+                self.counts[l, t] = r.size
+                self.lists[l][t] = torch.from_numpy(r if r.size else np.zeros(1, np.int32)).to(dev)
+
+    def rows(self, layer, step):
+        t = step % self.period
+        return self.lists[layer][t], int(self.counts[layer, t])
 
 
 def build_minmax(K, P, minmax=None, stream=None):

@@ -23,7 +23,13 @@ Readings (also listed in the design doc):
   two bf16 values is exact in float32, so only the additions round;
 * top-K keeps the K highest scores, ties to the lower page index, and lists
   the pages in ascending order; no page is forced in;
-* sparse decode = exact attention over the tokens of the selected pages.
+* sparse decode = exact attention over the tokens of the selected pages;
+* "Stability-aware rerank frequency": an unstable head is re-ranked at every
+  decode step, a stable head every `period` (16) steps.  Request b's stable
+  heads are due at the steps with (step + b * stagger) % period == 0
+  (stagger 0: all requests together, so an all-stable layer is skipped at the
+  other steps; stagger 1: one phase per request).  A head that is not due
+  keeps the pages it selected at its last rerank.
 """
 from __future__ import annotations
 
@@ -106,3 +112,39 @@ def page_tokens(pages: np.ndarray, P: int, N: int) -> np.ndarray:
     """Token indices covered by a list of pages (ascending pages -> ascending tokens)."""
     return np.concatenate([np.arange(p * P, min(N, (p + 1) * P)) for p in pages]) \
         if len(pages) else np.zeros(0, dtype=np.int64)
+
+
+def rerank_rows(unstable_layer, batch: int, step: int, period: int, stagger: int) -> list:
+    """Rows b*H + h of one layer due for a rerank at `step`, in (b, h) order."""
+    unstable_layer = [bool(u) for u in unstable_layer]
+    H = len(unstable_layer)
+    rows = []
+    for b in range(batch):
+        stable_due = (step + b * stagger) % period == 0
+        for h in range(H):
+            if unstable_layer[h] or stable_due:
+                rows.append(b * H + h)
+    return rows
+
+
+def stability_aware_selection(q_steps, mn_l, mx_l, K: int, unstable_layer, period: int, stagger: int):
+    """Selected pages of one layer after each decode step: list of int [batch][H][K].
+
+    q_steps[t] is the layer's query [batch][H_q][d] at step t; mn_l/mx_l are
+    [batch][H][n_pages][d].  Step 0 re-ranks every row (no earlier selection);
+    later steps re-rank only the rows rerank_rows lists, the others keep theirs.
+    """
+    mn_l = np.asarray(mn_l, dtype=np.float32)
+    mx_l = np.asarray(mx_l, dtype=np.float32)
+    batch, H = mn_l.shape[:2]
+    out, cur = [], None
+    for t, q in enumerate(q_steps):
+        q = np.asarray(q, dtype=np.float32)
+        g = q.shape[1] // H
+        due = range(batch * H) if cur is None else rerank_rows(unstable_layer, batch, t, period, stagger)
+        cur = np.zeros((batch, H, K), dtype=np.int64) if cur is None else cur.copy()
+        for r in due:
+            b, h = divmod(r, H)
+            cur[b, h] = top_pages(page_scores(q[b, h * g:(h + 1) * g], mn_l[b, h], mx_l[b, h]), K)
+        out.append(cur)
+    return out

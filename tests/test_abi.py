@@ -42,4 +42,4 @@ def test_version_and_error_string(lib):
 
 def test_struct_sizes_match_header(lib):
     assert lib.WORK_ITEM_DTYPE.itemsize == 48
-    assert lib._HEADER_DTYPE.itemsize == 72
+    assert lib._HEADER_DTYPE.itemsize == 80

@@ -144,6 +144,85 @@ def test_page_topk_workspace_reused(lib, cuda, n_pages):
         assert np.array_equal(sel.cpu().numpy(), ref), call
 
 
+def _random_rows_case(cuda, batch, H, g, d, n_pages, seed):
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(seed)
+    q = torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16)
+    mm = torch.randn((batch, H, n_pages, 2, d), generator=gen, device=cuda).to(torch.bfloat16)
+    mm = torch.stack([torch.minimum(mm[:, :, :, 0], mm[:, :, :, 1]),
+                      torch.maximum(mm[:, :, :, 0], mm[:, :, :, 1])], 3).contiguous()
+    return q, mm
+
+
+@pytest.mark.parametrize("n_pages,K", [(625, 64), (2049, 100), (3, 2)])
+def test_select_rows_only_touches_listed_rows(lib, cuda, n_pages, K):
+    """tg_page_score_topk_rows: the listed rows are exact, every other row keeps its values."""
+    batch, H, g, d = 6, 4, 4, 128
+    q, mm = _random_rows_case(cuda, batch, H, g, d, n_pages, seed=n_pages)
+    rng = np.random.default_rng(n_pages)
+    rows = np.sort(rng.choice(batch * H, size=9, replace=False)).astype(np.int32)
+    rows_dev = torch.from_numpy(np.concatenate([rows[::-1], [0, 0]]).astype(np.int32)).to(cuda)  # any order
+    sel = torch.full((batch, H, K), -7, dtype=torch.int32, device=cuda)
+    ids = torch.full((batch, H, K), -7, dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    lib.tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows_dev, rows.size, q, mm, sel, pt_ids=ids,
+                                dev_status=status)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(status) == 0
+    ref = ofx.select_pages(q.float().cpu().numpy(), mm.float().cpu().numpy()[:, :, :, 0],
+                           mm.float().cpu().numpy()[:, :, :, 1], K)
+    got, got_ids = sel.cpu().numpy(), ids.cpu().numpy()
+    for r in range(batch * H):
+        b, h = divmod(r, H)
+        if r in rows:
+            assert np.array_equal(got[b, h], ref[b, h]), r
+            assert np.array_equal(got_ids[b, h], r * n_pages + ref[b, h]), r
+        else:
+            assert (got[b, h] == -7).all() and (got_ids[b, h] == -7).all(), r
+
+
+def test_select_rows_bad_row_is_reported(lib, cuda):
+    batch, H, g, d, n_pages, K = 2, 3, 2, 128, 40, 5
+    q, mm = _random_rows_case(cuda, batch, H, g, d, n_pages, seed=3)
+    rows_dev = torch.tensor([1, 99, 4], dtype=torch.int32, device=cuda)
+    sel = torch.full((batch, H, K), -7, dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    lib.tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows_dev, 3, q, mm, sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & lib.STATUS_BAD_INPUT
+    ref = ofx.select_pages(q.float().cpu().numpy(), mm.float().cpu().numpy()[:, :, :, 0],
+                           mm.float().cpu().numpy()[:, :, :, 1], K)
+    for r in (1, 4):
+        assert np.array_equal(sel[r // H, r % H].cpu().numpy(), ref[r // H, r % H])
+
+
+@pytest.mark.parametrize("period,stagger", [(3, 0), (3, 1), (1, 0)])
+def test_stability_aware_rerank_steps(lib, cuda, period, stagger):
+    """Several decode steps with a new query each: unstable heads re-ranked every step, stable
+    heads every `period` steps; the selection after every step equals the oracle's."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, RerankSchedule
+    batch, H, g, d, n_pages, K, T, P = 4, 4, 2, 128, 50, 7, 7, 16
+    unstable = np.array([[1, 0, 0, 1]], np.uint8)
+    sched = RerankSchedule(unstable, batch, period=period, stagger=stagger, device=cuda)
+    dec = SparseDecoder(batch, H, H * g, d, P, n_pages, K, n_cta=16, device=cuda)
+    _, mm = _random_rows_case(cuda, batch, H, g, d, n_pages, seed=9)
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(10)
+    qs = [torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16) for _ in range(T)]
+    mm_h = mm.float().cpu().numpy()
+    ref = ofx.stability_aware_selection([q.float().cpu().numpy() for q in qs], mm_h[:, :, :, 0],
+                                        mm_h[:, :, :, 1], K, unstable[0], period, stagger)
+    for t in range(T):
+        if t == 0:
+            dec.select(qs[t], mm)
+        else:
+            rows, n = sched.rows(0, t)
+            dec.select_rows(qs[t], mm, rows, n)
+        torch.cuda.synchronize()
+        assert np.array_equal(dec.sel.view(batch, H, K).cpu().numpy(), ref[t]), t
+    assert lib.tg_check_status(dec.status) == 0
+
+
 def test_page_topk_nan_sets_status(lib, cuda):
     """A NaN in one query head makes that head's sums NaN: the call reports NONFINITE."""
     batch, H, g, d, n_pages, K = 2, 2, 4, 128, 40, 8
@@ -196,6 +275,40 @@ def test_sparse_decode_small(lib, cuda, K):
             ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], K_h[b, h][tok], V_h[b, h][tok],
                                                          1.0 / math.sqrt(w.d))
     compare_out(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_sparse_layers_back_to_back(lib, cuda, overlap):
+    """Score + decode of several layers queued without a sync, sharing one page-list buffer:
+    each decode must read its own layer's lists (with overlap, the score call lets the decode
+    start early and the decode waits before reading them)."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=3, N=480, L=3)
+    P, n_pages, K = w.P, w.N // w.P, 6
+    dec = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=48, device=cuda, overlap=overlap)
+    layers = []
+    for l in range(w.L):
+        Kt, Vt = synth.keys_values(w, l, cuda)
+        layers.append((synth.queries(w, l, cuda), build_minmax(Kt, P), _dense_pool(Kt, Vt, P), Kt, Vt))
+    outs = [torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda) for _ in range(w.L)]
+    lses = [torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda) for _ in range(w.L)]
+    for rep in range(2):
+        for l, (q, mm, pool, _, _) in enumerate(layers):
+            dec.step(q, mm, pool, outs[l], lses[l])
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(dec.status) == 0
+    for l, (q, mm, pool, Kt, Vt) in enumerate(layers):
+        K_h, V_h, q_h = Kt.float().cpu().numpy(), Vt.float().cpu().numpy(), q.float().cpu().numpy()
+        mm_h = mm.float().cpu().numpy()
+        sel_ref = ofx.select_pages(q_h, mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
+        ref_out = np.zeros((w.batch, w.H_q, w.d))
+        ref_lse = np.zeros((w.batch, w.H_q))
+        for b in range(w.batch):
+            for j in range(w.H_q):
+                tok = ofx.page_tokens(sel_ref[b, j // w.g], P, w.N)
+                ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], K_h[b, j // w.g][tok],
+                                                             V_h[b, j // w.g][tok], 1.0 / math.sqrt(w.d))
+        compare_out(outs[l], lses[l], ref_out, ref_lse)
 
 
 def test_all_pages_equals_dense(lib, cuda):

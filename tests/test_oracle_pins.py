@@ -430,6 +430,69 @@ def test_all_pages_is_dense():
         np.testing.assert_allclose(o1, o2, rtol=1e-10, atol=1e-12)
 
 
+def pin_rerank_rows(fn=fx.rerank_rows):
+    """The rerank schedule: hand-derived cases, the closed-form row count, and every
+    stable row exactly once in any window of `period` consecutive steps."""
+    unst = [1, 0, 0, 1, 0]  # H = 5, heads 0 and 3 unstable
+    H = len(unst)
+    # stagger 0, step 0: every row; step 1: only the unstable heads of every request
+    assert fn(unst, 3, 0, 4, 0) == list(range(15))
+    assert fn(unst, 3, 1, 4, 0) == [0, 3, 5, 8, 10, 13]
+    # stagger 1, period 4, step 3: request 1 is due (3 + 1 = 4), requests 0 and 2 are not
+    assert fn(unst, 3, 3, 4, 1) == [0, 3, 5, 6, 7, 8, 9, 10, 13]
+    # an all-stable layer, stagger 0: nothing to rerank between the due steps
+    assert fn([0] * H, 4, 5, 16, 0) == [] and len(fn([0] * H, 4, 16, 16, 0)) == 4 * H
+    r = np.random.default_rng(12)
+    for _ in range(200):
+        H = int(r.integers(1, 9))
+        batch = int(r.integers(0, 7))
+        period = int(r.integers(1, 17))
+        stagger = int(r.integers(0, 2))
+        u = list(r.integers(0, 2, size=H))
+        t0 = int(r.integers(0, 50))
+        seen = {}
+        for step in range(t0, t0 + period):
+            rows = fn(u, batch, step, period, stagger)
+            assert rows == sorted(set(rows))
+            due = sum(1 for b in range(batch) if (step + b * stagger) % period == 0)
+            assert len(rows) == batch * sum(u) + due * (H - sum(u))
+            for row in rows:
+                seen[row] = seen.get(row, 0) + 1
+        for b in range(batch):
+            for h in range(H):
+                assert seen.get(b * H + h, 0) == (period if u[h] else 1), (b, h)
+
+
+def pin_stability_aware_selection(fn=fx.stability_aware_selection):
+    """period 1 re-ranks every row at every step (= select_pages per step); with every
+    head stable and a period past the last step, step 0's pages stay; and a mix keeps
+    the stable heads' pages between their due steps while the unstable heads follow q."""
+    r = np.random.default_rng(13)
+    batch, H, g, d, n_pages, K, T = 2, 3, 2, 32, 9, 3, 5
+    mn0 = r.standard_normal((batch, H, n_pages, d)).astype(np.float32)
+    mx0 = r.standard_normal((batch, H, n_pages, d)).astype(np.float32)
+    mn, mx = np.minimum(mn0, mx0), np.maximum(mn0, mx0)
+    qs = [r.standard_normal((batch, H * g, d)).astype(np.float32) for _ in range(T)]
+    every = [fx.select_pages(q, mn, mx, K) for q in qs]
+    assert len({tuple(e.ravel()) for e in every}) > 1  # the query changes the pages
+    got = fn(qs, mn, mx, K, [0] * H, 1, 0)
+    assert all(np.array_equal(a, b) for a, b in zip(got, every))
+    got = fn(qs, mn, mx, K, [0] * H, T + 1, 0)
+    assert all(np.array_equal(a, every[0]) for a in got)
+    got = fn(qs, mn, mx, K, [1, 0, 0], 2, 0)
+    for t in range(T):
+        assert np.array_equal(got[t][:, 0], every[t][:, 0])          # unstable: every step
+        assert np.array_equal(got[t][:, 1:], every[t - t % 2][:, 1:])  # stable: due at even steps
+
+
+def test_rerank_rows():
+    pin_rerank_rows()
+
+
+def test_stability_aware_selection():
+    pin_stability_aware_selection()
+
+
 # ------------------------------------------------- planted mistakes are caught
 
 def _wrong_ceil(B, N):
@@ -487,6 +550,19 @@ def _work_list_off_by_one(S_row, ntok_l, order_l, H_p):
     return ctas
 
 
+def _rerank_phase_shifted(u, batch, step, period, stagger):
+    return fx.rerank_rows(u, batch, step + 1, period, stagger)
+
+
+def _rerank_no_stagger(u, batch, step, period, stagger):
+    return fx.rerank_rows(u, batch, step, period, 0)
+
+
+def _selection_never_refreshed(q_steps, mn, mx, K, unstable, period, stagger):
+    first = fx.stability_aware_selection(q_steps[:1], mn, mx, K, unstable, period, stagger)[0]
+    return [first] * len(q_steps)
+
+
 @pytest.mark.parametrize("pin,mutant", [
     (pin_retained_count, _wrong_ceil),
     (pin_top_indices, _ties_high),
@@ -497,6 +573,9 @@ def _work_list_off_by_one(S_row, ntok_l, order_l, H_p):
     (pin_quest_bound, _quest_flat),
     (pin_top_pages, _ties_high),
     (pin_work_list, _work_list_off_by_one),
+    (pin_rerank_rows, _rerank_phase_shifted),
+    (pin_rerank_rows, _rerank_no_stagger),
+    (pin_stability_aware_selection, _selection_never_refreshed),
 ])
 def test_planted_mistake_is_caught(pin, mutant):
     with pytest.raises(AssertionError):

@@ -147,3 +147,39 @@ def test_plan_rejects(lib):
         lib.tg_plan_decode(S, order, ntok, 64, 2, 16, 128)
     with pytest.raises(lib.TGError):   # not a permutation
         lib.tg_plan_decode(S, np.zeros((1, 4), np.int32), ntok, 8, 2, 16, 128)
+
+
+def test_rerank_rows_matches_oracle(lib):
+    from oracle import flexicache as ofx
+    r = np.random.default_rng(21)
+    for _ in range(300):
+        L, H = int(r.integers(1, 5)), int(r.integers(1, 9))
+        batch = int(r.integers(0, 9))
+        period = int(r.integers(1, 20))
+        stagger = int(r.integers(0, 2))
+        u = r.integers(0, 2, size=(L, H)).astype(np.uint8)
+        layer, step = int(r.integers(0, L)), int(r.integers(0, 100))
+        got = lib.tg_rerank_rows(u, batch, layer, step, period, stagger)
+        assert got.tolist() == ofx.rerank_rows(u[layer], batch, step, period, stagger)
+
+
+def test_rerank_rows_rejects(lib):
+    u = np.zeros((2, 4), np.uint8)
+    with pytest.raises(lib.TGError):
+        lib.tg_rerank_rows(u, 3, 2, 0, 16, 0)   # layer out of range
+    with pytest.raises(lib.TGError):
+        lib.tg_rerank_rows(u, 3, 0, 0, 0, 0)    # period 0
+    with pytest.raises(lib.TGError):
+        lib.tg_rerank_rows(u, 3, 0, 0, 16, 2)   # stagger not 0/1
+
+
+def test_plan_flags(lib):
+    w = synth.small()
+    pg = lib.tg_build_pages(w.L, w.batch, w.H, w.H_p, w.P, w.alpha, synth.budgets_hat(w), synth.contexts(w), w.cluster)
+    S = lib.tg_split_map(pg["Phi"], 8)
+    plan, _ = lib.tg_plan_decode(S, pg["order"], pg["ntok"], w.H_q, w.H_p, w.P, w.d)
+    assert lib.plan_header(plan)["flags"] == 0
+    lib.tg_plan_set_flags(plan, lib.PLAN_WAIT_TABLES)
+    assert lib.plan_header(plan)["flags"] == lib.PLAN_WAIT_TABLES
+    with pytest.raises(lib.TGError):
+        lib.tg_plan_set_flags(plan, 0x80)
