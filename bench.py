@@ -603,6 +603,56 @@ def bench_rerank(args, w, q, mms, pools, out, stream, results, device):
     return out_rr
 
 
+def report_pages(args):
+    """Budget reservation memory report (host only): for 25/50/75% eviction and every page
+    layout (monolithic; ragged H_p = 1, 2, 4, 8 with and without budget-aware clustering),
+    the bytes each request reserves, the part trapped by page rounding, the memory reclaimed
+    against monolithic paging, the page-table size, and how many requests of an arrival stream
+    the allocator admits (first come, first served) into a fixed pool."""
+    import non_uniform_paged_gb300 as tg
+    cap_bytes = 200e9
+    n_req = 512
+    out = {"report": "page_footprint", "pool_bytes": cap_bytes, "requests": n_req,
+           "workload": "Llama-3.1-8B shape (32 layers, 8 KV heads, d 128, P 16), contexts log-uniform 4K-64K, "
+                       "budgets LogN(0, 0.8) scaled to the target mean and clipped at 1", "rows": []}
+    for rho in (0.75, 0.5, 0.25):
+        w = synth.workload(2, batch=n_req, N=65536, ctx_dist="loguniform", ctx_min=4096, budget_args=(0.8, rho))
+        Bhat, N = synth.budgets_hat(w), synth.contexts(w)
+        layouts = [("monolithic", w.H, False)] + [(f"H_p={hp}{' clustered' if cl else ''}", hp, cl)
+                                                  for hp in (1, 2, 4, 8) for cl in (False, True)]
+        mono_bytes = None
+        mono_admitted = None
+        for name, hp, cl in layouts:
+            t0 = time.perf_counter()
+            pg = tg.tg_build_pages(w.L, w.batch, w.H, hp, w.P, w.alpha, Bhat, N, cl)
+            plan_s = time.perf_counter() - t0
+            G = w.H // hp
+            page_bytes = hp * 2 * w.P * w.d * 2
+            off = pg["pt_off"]
+            counts = np.diff(off).reshape(w.L, w.batch, G)        # pages per (layer, request, group)
+            per_req_pages = counts.sum(axis=(0, 2))
+            exact = pg["ntok"].astype(np.int64).sum(axis=(0, 2)) * 2 * w.d * 2
+            alloc = tg.PageAllocator(int(cap_bytes // page_bytes))
+            admitted = 0
+            for b in range(w.batch):
+                if alloc.admit(counts[:, b, :].reshape(-1)) is None:
+                    break
+                admitted += 1
+            reserved = per_req_pages * page_bytes
+            row = {"retention": rho, "layout": name, "H_p": hp, "clustered": cl,
+                   "realised_retention": float(pg["ntok"].sum() / (w.L * w.H * N.astype(np.int64).sum())),
+                   "GB_per_request": float(reserved.mean() / 1e9),
+                   "trapped_pct": float(100 * (reserved.sum() - exact.sum()) / reserved.sum()),
+                   "page_table_entries_per_request": float(per_req_pages.mean()),
+                   "page_tables_per_request": w.L * G, "admitted": admitted, "plan_s": plan_s}
+            if mono_bytes is None:
+                mono_bytes, mono_admitted = reserved.sum(), admitted
+            row["reclaimed_vs_monolithic_pct"] = float(100 * (mono_bytes - reserved.sum()) / mono_bytes)
+            row["admitted_vs_monolithic"] = admitted / max(1, mono_admitted)
+            out["rows"].append(row)
+    print(json.dumps(out), flush=True)
+
+
 def bench_layerwise(args, w, rank, world, local, device):
     """Config 5 (d=256, ~220 GB of pages in total): one layer resident at a time.  For each
     H_p, every layer is compacted into a one-layer pool and its decode launch is timed; the
@@ -688,9 +738,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
+    ap.add_argument("--report-pages", action="store_true",
+                    help="host-only budget reservation memory report (H_p / clustering at 25/50/75%% eviction)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.report_pages:  # host only: no GPU, no process group
+        report_pages(args)
+        return
     rank, world, local = dist_setup()
     device = torch.device(f"cuda:{local}") if torch.cuda.is_available() else torch.device("cpu")
     if args.impl == "reference":

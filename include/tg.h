@@ -339,6 +339,28 @@ int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, con
                                   const int64_t *pt_off, const int32_t *pt_ids, float scale,
                                   uint16_t *out, float *lse, int32_t *dev_status, int64_t *cta_time);
 
+/* ------------------------------------------------------------------ f2 ---
+ * Page allocator for budget reservation.  [Tangram] 3.1 Budget Reservation: a
+ * request's compressed footprint is fixed when it is scheduled, so its pages
+ * are allocated once, with no runtime page reclamation; 3.2 Ragged Paging: one
+ * page table per (layer, request, head group).  Host only; the state lives in
+ * caller memory (tg_alloc_state_bytes), one allocator per pool.
+ *   tg_alloc_init: n_pages free pages, handed out lowest id first.
+ *   tg_alloc_admit: pages_per_list int32 [n_lists] (e.g. the per-list page counts
+ *     of tg_build_pages for one request); all-or-nothing: on success ids int32
+ *     [*n_ids] gets the pages list after list (ids_cap >= their sum), else
+ *     TG_ERR_CAPACITY and nothing is taken.  *n_ids is set either way.
+ *   tg_alloc_release: returns pages; released pages are reused last-in first-
+ *     out.  A page not allocated, or listed twice, is TG_ERR_INVALID_ARG and
+ *     nothing is released.
+ *   tg_alloc_query: free and allocated page counts. */
+int tg_alloc_state_bytes(int64_t n_pages, int64_t *bytes);
+int tg_alloc_init(void *state, int64_t state_cap, int64_t n_pages);
+int tg_alloc_admit(void *state, int n_lists, const int32_t *pages_per_list, int32_t *ids, int64_t ids_cap,
+                   int64_t *n_ids);
+int tg_alloc_release(void *state, int64_t n, const int32_t *ids);
+int tg_alloc_query(const void *state, int64_t *n_free, int64_t *n_live);
+
 /* tg_check_status -- synchronously read a device status word (waits for the
  *   device).  Returns TG_OK when it is 0, TG_ERR_TIMEOUT when TG_STATUS_TIMEOUT
  *   is set, TG_ERR_DEVICE for any other bit; *host_status (may be NULL) gets

@@ -21,7 +21,8 @@ from . import _build
 __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
-           "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START",
+           "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
+           "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
@@ -50,6 +51,11 @@ _SIGS = {
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, ctypes.c_uint32, _P]),
     "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
+    "tg_alloc_state_bytes": (_I, [_L, _P]),
+    "tg_alloc_init": (_I, [_P, _L, _L]),
+    "tg_alloc_admit": (_I, [_P, _I, _P, _P, _L, _P]),
+    "tg_alloc_release": (_I, [_P, _L, _P]),
+    "tg_alloc_query": (_I, [_P, _P, _P]),
     "tg_page_score_workspace": (_I, [_I, _I, _I, _P]),
     "tg_page_score_topk_rows": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _L, ctypes.c_uint32,
                                      _P]),
@@ -321,6 +327,64 @@ def tg_rerank_rows(unstable, batch, layer, step, period=16, stagger=0) -> np.nda
     _check(lib.tg_rerank_rows(L, batch, H, u.ctypes.data, layer, step, period, stagger, rows.ctypes.data,
                               ctypes.addressof(n)))
     return rows[:n.value].copy()
+
+
+def tg_alloc_state_bytes(n_pages: int) -> int:
+    """Host state bytes of an allocator over n_pages pages (tg.h: tg_alloc_state_bytes)."""
+    v = ctypes.c_int64(0)
+    _check(load().tg_alloc_state_bytes(int(n_pages), ctypes.addressof(v)))
+    return v.value
+
+
+def tg_alloc_init(state: np.ndarray, n_pages: int) -> None:
+    """Initialise an allocator in a uint8 host buffer (tg.h: tg_alloc_init)."""
+    _check(load().tg_alloc_init(state.ctypes.data, state.size, int(n_pages)))
+
+
+def tg_alloc_admit(state: np.ndarray, pages_per_list):
+    """Pages of one request, list after list, or None when the pool is short (tg.h: tg_alloc_admit)."""
+    lists = np.ascontiguousarray(np.asarray(pages_per_list, dtype=np.int32))
+    need = int(lists.astype(np.int64).sum())
+    ids = np.empty(max(1, need), dtype=np.int32)
+    n = ctypes.c_int64(0)
+    rc = load().tg_alloc_admit(state.ctypes.data, int(lists.size), lists.ctypes.data, ids.ctypes.data, need,
+                               ctypes.addressof(n))
+    if rc == -4:  # TG_ERR_CAPACITY: not enough free pages, nothing taken
+        return None
+    _check(rc)
+    return ids[:n.value].copy()
+
+
+def tg_alloc_release(state: np.ndarray, ids) -> None:
+    """Return pages to the pool (tg.h: tg_alloc_release)."""
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    _check(load().tg_alloc_release(state.ctypes.data, int(ids.size), ids.ctypes.data))
+
+
+def tg_alloc_query(state: np.ndarray):
+    """(free pages, allocated pages) (tg.h: tg_alloc_query)."""
+    f, l_ = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load().tg_alloc_query(state.ctypes.data, ctypes.addressof(f), ctypes.addressof(l_)))
+    return f.value, l_.value
+
+
+class PageAllocator:
+    """Budget-reservation page allocator over the tg_alloc_* calls; the state is a host buffer
+    owned by this object."""
+
+    def __init__(self, n_pages: int):
+        self._state = np.zeros(max(8, tg_alloc_state_bytes(n_pages)), dtype=np.uint8)
+        tg_alloc_init(self._state, n_pages)
+        self.n_pages = int(n_pages)
+
+    def admit(self, pages_per_list):
+        return tg_alloc_admit(self._state, pages_per_list)
+
+    def release(self, ids) -> None:
+        tg_alloc_release(self._state, ids)
+
+    def query(self):
+        return tg_alloc_query(self._state)
 
 
 def tg_check_status(dev_status) -> int:

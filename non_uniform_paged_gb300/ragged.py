@@ -31,7 +31,7 @@ BYTES_BF16 = 2
 
 class RaggedCache:
     def __init__(self, L, batch, H, H_q, d, P, H_p, alpha, Bhat, N, cluster=False, n_cta=None,
-                 uniform_split=False, device="cuda", alloc_pool=True):
+                 uniform_split=False, device="cuda", alloc_pool=True, allocator=None):
         self.L, self.batch, self.H, self.H_q, self.d, self.P, self.H_p = L, batch, H, H_q, d, P, H_p
         self.G = H // H_p
         self.g = H_q // H
@@ -39,6 +39,9 @@ class RaggedCache:
         self.N = np.asarray(N, np.int32)
         self.pages = tg_build_pages(L, batch, H, H_p, P, alpha, Bhat, self.N, cluster)
         self.n_pages = self.pages["n_pages"]
+        self.request_pages = None
+        if allocator is not None:
+            self._take_pages(allocator)
         self.n_cta = int(n_cta) if n_cta else tg_query_ncta(d, self.g)
         Phi = np.ones_like(self.pages["Phi"]) if uniform_split else self.pages["Phi"]
         self.S = tg_split_map(Phi, self.n_cta)
@@ -57,6 +60,27 @@ class RaggedCache:
         if alloc_pool:
             self.pool = torch.empty(max(self.n_pages, 1) * H_p * 2 * P * d, dtype=torch.bfloat16, device=dev)
         self.scale = 1.0 / math.sqrt(d)
+
+    def _take_pages(self, allocator):
+        """Budget reservation: each request's page lists, over all layers and groups, come from
+        the allocator at once (all or nothing); the pool is the allocator's."""
+        off, ids = self.pages["pt_off"], self.pages["pt_ids"].copy()
+        self.request_pages = []
+        for b in range(self.batch):
+            lists = [(l * self.batch + b) * self.G + g for l in range(self.L) for g in range(self.G)]
+            counts = [int(off[i + 1] - off[i]) for i in lists]
+            got = allocator.admit(counts)
+            if got is None:
+                for taken in self.request_pages:
+                    allocator.release(taken)
+                raise RuntimeError(f"page pool full: request {b} needs {sum(counts)} pages")
+            pos = 0
+            for i, c in zip(lists, counts):
+                ids[off[i]:off[i] + c] = got[pos:pos + c]
+                pos += c
+            self.request_pages.append(got)
+        self.pages = dict(self.pages, pt_ids=ids)
+        self.n_pages = allocator.n_pages
 
     # ---- sizes
     def list_offsets(self, layer: int) -> torch.Tensor:

@@ -71,6 +71,34 @@ def test_many_items_per_cta(lib, cuda, n_cta):
     assert np.diff(off).max() > 16
 
 
+def test_decode_over_allocator_pages(lib, cuda):
+    """Compaction and decode through page ids handed out by the budget-reservation allocator
+    after churn (scattered, not in request order): the results equal the oracle's."""
+    from non_uniform_paged_gb300.ragged import RaggedCache
+    w = synth.small(L=2, batch=3, H_p=2)
+    N = synth.contexts(w)
+    static = lib.tg_build_pages(w.L, w.batch, w.H, w.H_p, w.P, w.alpha, synth.budgets_hat(w), N, w.cluster)
+    a = lib.PageAllocator(2 * static["n_pages"] + 50)
+    r = np.random.default_rng(4)
+    held = [a.admit([int(x)]) for x in r.integers(1, 20, size=12)]
+    for i in r.permutation(len(held))[:8]:
+        a.release(held[i])
+    cache = RaggedCache(w.L, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, synth.budgets_hat(w), N,
+                        cluster=w.cluster, n_cta=24, device=cuda, allocator=a)
+    ids = cache.pages["pt_ids"]
+    assert not np.array_equal(ids, np.sort(ids))  # the pages are really scattered
+    for layer in range(w.L):
+        s, K, V, kept = run_layer(lib, w, layer, cache, cuda)
+        q = synth.queries(w, layer, cuda)
+        out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+        lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+        cache.decode_layer(layer, q, out, lse)
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(cache.status) == 0
+        ref_out, ref_lse, _ = oracle_layer(w, layer, s, K, V, q, cache.pages["ntok"][layer], N)
+        compare_out(out, lse, ref_out, ref_lse)
+
+
 def test_small_d256(lib, cuda):
     w = synth.small(d=256, H=8, H_q=16, H_p=4, batch=2, N=640)
     _decode_and_check(lib, w, cuda, n_cta=20)

@@ -13,6 +13,7 @@ import scipy.special
 import torch
 
 from oracle import flexicache as fx
+from oracle import pages as opg
 from oracle import tangram as tg
 
 
@@ -493,6 +494,58 @@ def test_stability_aware_selection():
     pin_stability_aware_selection()
 
 
+def pin_footprint(fn=opg.footprint):
+    """Page footprint: a hand-derived case, monolithic = one group of all H heads, the
+    order exact <= ragged <= monolithic, and sorted (budget-aware) groups are the cheapest
+    grouping of equal size (brute force over every assignment of heads to groups)."""
+    n = np.array([[[17, 1, 40, 16]]])
+    f = fn(n, [[0, 1, 2, 3]], 2, 16, 2)
+    assert (f["ragged"], f["monolithic"], f["exact"]) == (640, 768, 296)
+    assert f["ragged_pages"] == 5 and f["monolithic_pages"] == 3 and f["page_tables"] == 2
+    assert fn(n, [[2, 0, 3, 1]], 2, 16, 2)["ragged"] == 512   # sorted by n: groups {2,0}, {3,1}
+    r = np.random.default_rng(14)
+    for _ in range(60):
+        L, batch, H = int(r.integers(1, 3)), int(r.integers(1, 3)), int(r.choice([2, 4, 6]))
+        P, d = int(r.choice([1, 4, 16])), 2
+        ntok = r.integers(1, 80, size=(L, batch, H))
+        ident = [list(range(H))] * L
+        f_mono = fn(ntok, ident, H, P, d)
+        assert f_mono["ragged"] == f_mono["monolithic"]
+        for H_p in [x for x in (1, 2, 3) if H % x == 0]:
+            f = fn(ntok, ident, H_p, P, d)
+            assert f["exact"] <= f["ragged"] <= f["monolithic"]
+            if L == 1 and batch == 1:
+                best = min(fn(ntok, [list(pm)], H_p, P, d)["ragged"] for pm in itertools.permutations(range(H)))
+                srt = sorted(range(H), key=lambda h: (-int(ntok[0, 0, h]), h))
+                assert fn(ntok, [srt], H_p, P, d)["ragged"] == best
+
+
+def pin_page_pool(cls=opg.PagePool):
+    """Allocator policy: lowest ids first, all or nothing, last-in first-out reuse, and a bad
+    release raises and changes nothing."""
+    pool = cls(6)
+    assert pool.admit([2, 1]) == [0, 1, 2]
+    assert pool.admit([3]) == [3, 4, 5]
+    assert pool.admit([1]) is None
+    pool.release([0, 1, 2])
+    assert pool.admit([2]) == [0, 1]
+    with pytest.raises(ValueError):
+        pool.release([1, 1])
+    with pytest.raises(ValueError):
+        pool.release([2])          # free already
+    pool.release([3, 4, 5])
+    assert pool.admit([4]) == [3, 4, 5, 2]
+    assert pool.admit([1]) is None
+
+
+def test_footprint():
+    pin_footprint()
+
+
+def test_page_pool():
+    pin_page_pool()
+
+
 # ------------------------------------------------- planted mistakes are caught
 
 def _wrong_ceil(B, N):
@@ -550,6 +603,23 @@ def _work_list_off_by_one(S_row, ntok_l, order_l, H_p):
     return ctas
 
 
+def _footprint_min_head(ntok, order, H_p, P, d):
+    f = opg.footprint(ntok, order, H_p, P, d)
+    ntok = np.asarray(ntok)
+    L, batch, H = ntok.shape
+    pages = sum(-(-min(int(ntok[l, b, h]) for h in order[l][g * H_p:(g + 1) * H_p]) // P)
+                for l in range(L) for b in range(batch) for g in range(H // H_p))
+    f["ragged"], f["ragged_pages"] = pages * H_p * 2 * P * d, pages
+    return f
+
+
+class _PoolFifo(opg.PagePool):
+    def release(self, ids):
+        super().release(ids)
+        n = len(ids)
+        self.free[-n:] = self.free[-n:][::-1]
+
+
 def _rerank_phase_shifted(u, batch, step, period, stagger):
     return fx.rerank_rows(u, batch, step + 1, period, stagger)
 
@@ -576,6 +646,8 @@ def _selection_never_refreshed(q_steps, mn, mx, K, unstable, period, stagger):
     (pin_rerank_rows, _rerank_phase_shifted),
     (pin_rerank_rows, _rerank_no_stagger),
     (pin_stability_aware_selection, _selection_never_refreshed),
+    (pin_footprint, _footprint_min_head),
+    (pin_page_pool, _PoolFifo),
 ])
 def test_planted_mistake_is_caught(pin, mutant):
     with pytest.raises(AssertionError):
