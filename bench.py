@@ -528,6 +528,7 @@ def bench_sparse(args, w, rank, world, local, device):
             "bytes_per_step": step_bytes}
         del dec
     rerank = bench_rerank(args, w, q, mms, pools, out, stream, results, device)
+    tiered = bench_tiered(args, w, q, mms, pools, out, stream, device)
     if rank != 0:
         return
     best = results[f"K{w.topk_pages[0]}"]
@@ -540,7 +541,7 @@ def bench_sparse(args, w, rank, world, local, device):
             "pct_of_hbm_peak": best["pct_of_hbm_peak"],
             "sparse_vs_dense_speedup": {k: results["dense"]["ms_per_step"] / v["ms_per_step"]
                                         for k, v in results.items() if k != "dense"},
-            "variants": results, "rerank": rerank, "peak": peak, "peak_kind": peak_kind}
+            "variants": results, "rerank": rerank, "tiered": tiered, "peak": peak, "peak_kind": peak_kind}
     print(json.dumps(line), flush=True)
 
 
@@ -601,6 +602,91 @@ def bench_rerank(args, w, q, mms, pools, out, stream, results, device):
     tg_check(dec.status)
     del dec
     return out_rr
+
+
+def bench_tiered(args, w, q, mms, pools, out, stream, device, layers=4, steps=32, drift=0.05):
+    """Tiered KV placement on `layers` layers: stable heads keep K GPU blocks and their whole
+    KV in pinned host memory; unstable heads (25%, seeded) keep every page on the GPU.  The
+    query drifts by `drift` (times its spread) per step; stable heads re-rank every 16 steps.
+    Reports ms per step against the same schedule with every page on the GPU, the promoted
+    pages and their host-to-GPU bandwidth, and the GPU KV bytes against the dense cache."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, TieredSparseDecoder, RerankSchedule
+    K_sel, n_pages, period = w.topk_pages[0], w.N // w.P, 16
+    L = min(layers, w.L)
+    pairs = np.random.default_rng(w.seed + 77).permutation(w.L * w.H)[:(w.L * w.H) // 4]
+    unstable = np.zeros((w.L, w.H), np.uint8)
+    unstable.flat[pairs] = 1
+    sched = RerankSchedule(unstable[:L], w.batch, period=period, stagger=0, device=device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed + 5)
+    qs = [[q[l]] for l in range(L)]
+    for l in range(L):
+        cur = q[l].float()
+        for _ in range(steps - 1):
+            cur = cur + drift * torch.randn(cur.shape, generator=gen, device=device)
+            qs[l].append(cur.to(torch.bfloat16))
+    tiers = []
+    for l in range(L):
+        t = TieredSparseDecoder(w.batch, w.H, w.H_q, w.d, w.P, n_pages, K_sel, unstable[l], device=device)
+        t.load(pools[l])
+        tiers.append(t)
+    flat = SparseDecoder(w.batch, w.H, w.H_q, w.d, w.P, n_pages, K_sel, device=device, layers=L)
+
+    def run(tiered_mode, timed_steps):
+        ev = _events(2 * len(timed_steps))
+        for i, st in enumerate(timed_steps):
+            ev[2 * i].record(stream)
+            for l in range(L):
+                rows, n = sched.rows(l, st)
+                if st == 0:
+                    rows, n = None, None  # every row at the first step
+                if tiered_mode:
+                    tiers[l].rerank(qs[l][st], mms[l], rows, n, stream=stream)
+                    tiers[l].attend(qs[l][st], out, stream=stream)
+                else:
+                    if st == 0:
+                        flat.select(qs[l][st], mms[l], stream=stream, layer=l)
+                    else:
+                        flat.select_rows(qs[l][st], mms[l], rows, n, stream=stream, layer=l)
+                    flat.attend(qs[l][st], pools[l], out, stream=stream, layer=l)
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        return [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(timed_steps))]
+
+    res = {"layers": L, "steps": steps, "query_drift_per_step": drift, "period": period}
+    for mode in ("all_gpu", "tiered"):
+        for t in tiers:
+            t.load(pools[tiers.index(t)])
+            t.promoted.zero_()
+        run(mode == "tiered", [0])                       # first full rerank fills the blocks (untimed)
+        fill = int(sum(int(t.promoted.item()) for t in tiers))
+        ms = run(mode == "tiered", list(range(1, steps)))
+        res[mode] = {"ms_per_step": statistics.mean(ms) / L * w.L,  # scaled to the 32-layer model
+                     "ms_per_layer_step": statistics.mean(ms) / L,
+                     "rerank_step_ms_per_layer": statistics.mean(ms[period - 1::period]) / L,
+                     "other_step_ms_per_layer": statistics.mean([m for i, m in enumerate(ms, 1) if i % period]) / L}
+        if mode == "tiered":
+            moved = int(sum(int(t.promoted.item()) for t in tiers)) - fill
+            stable_rows = int(sum((unstable[l] == 0).sum() for l in range(L))) * w.batch
+            reranks = len(range(period, steps, period))
+            page_bytes = 2 * w.P * w.d * 2
+            extra_ms = (res["tiered"]["rerank_step_ms_per_layer"] - res["all_gpu"]["rerank_step_ms_per_layer"]) * L
+            res["tiered"].update({
+                "promoted_pages_per_stable_rerank": moved / max(1, reranks),
+                "promoted_fraction_of_topk": moved / max(1, reranks * stable_rows * K_sel),
+                "host_bytes_per_stable_rerank": moved / max(1, reranks) * page_bytes,
+                "promote_extra_ms_per_rerank_step": extra_ms,
+                "host_link_gbs": (moved / max(1, reranks) * page_bytes) / max(1e-9, extra_ms * 1e-3) / 1e9,
+                "gpu_kv_bytes_per_layer": statistics.mean([t.gpu_kv_bytes() for t in tiers]),
+                "dense_kv_bytes_per_layer": tiers[0].dense_kv_bytes()})
+            res["tiered"]["gpu_kv_saved_pct"] = 100 * (1 - res["tiered"]["gpu_kv_bytes_per_layer"]
+                                                       / res["tiered"]["dense_kv_bytes_per_layer"])
+    for t in tiers:
+        tg_status = t.status
+        __import__("non_uniform_paged_gb300").tg_check_status(tg_status)
+    del tiers, flat
+    torch.cuda.empty_cache()
+    return res
 
 
 def report_pages(args):

@@ -339,6 +339,39 @@ int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, con
                                   const int64_t *pt_off, const int32_t *pt_ids, float scale,
                                   uint16_t *out, float *lse, int32_t *dev_status, int64_t *cta_time);
 
+/* ------------------------------------------------------------------ f4 ---
+ * tg_tier_promote -- tiered KV placement: fetch newly promoted pages of stable
+ *   heads from host memory into GPU blocks freed in place, and build the decode
+ *   lists.  [FlexiCache] "Core method / Tiered KV placement" (a stable head keeps
+ *   only its top-K pages on the GPU, the rest in host memory; a rerank moves only
+ *   the newly promoted pages), "Block Allocator" (blocks reclaimed and reassigned
+ *   in place at rerank) and "KV transfer" (a kernel reads pinned host KV through
+ *   unified addressing).
+ * For each listed row r = b*H + h (device int32 rows[n_rows]):
+ *   unstable[h] != 0 (device uint8 [H] of this layer): every page is on the GPU;
+ *     pt_ids[r][k] = dense_base[r] + sel[r][k].
+ *   stable: the row owns the K blocks slot_block[r][0..K) (device int32) of pool;
+ *     slot_page[r][k] (device int32, in/out) is the page block k holds, -1 none.
+ *     Blocks whose page is not in sel[r] are freed; the pages of sel[r] not held
+ *     by any block are copied from host_kv into them, the lowest such page into
+ *     the lowest freed slot; pages already held are not touched.  Then
+ *     pt_ids[r][k] = the block holding sel[r][k].
+ *   sel int32 [batch*H][K], each row ascending, distinct pages in [0, n_pages)
+ *   (tg_page_score_topk's output).  host_kv: host memory [batch*H][n_pages][page_bytes],
+ *   pinned (read through its device mapping), or pageable on a device that reads
+ *   pageable memory (cudaDevAttrPageableMemoryAccess, e.g. Grace over NVLink-C2C);
+ *   anything else is TG_ERR_INVALID_ARG.  pool [pool_pages][page_bytes];
+ *   both 16-byte aligned, page_bytes a multiple of 16.  promoted (device int64,
+ *   may be NULL) is increased by the number of pages copied.  grid_limit > 0
+ *   caps the CTAs (one row at a time each), for a low-priority background copy.
+ *   A bad row or block sets TG_STATUS_BAD_INPUT / TG_STATUS_BAD_PAGE.
+ *   Sizes: 1 <= K <= n_pages, n_pages <= 16384, K <= 1024. */
+int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
+                    const uint8_t *unstable, int batch, int H, int n_pages, int K, const int32_t *sel,
+                    int32_t *slot_page, const int32_t *slot_block, const int64_t *dense_base,
+                    const void *host_kv, int page_bytes, void *pool, int64_t pool_pages,
+                    int32_t *pt_ids, int64_t *promoted, int32_t *dev_status);
+
 /* ------------------------------------------------------------------ f2 ---
  * Page allocator for budget reservation.  [Tangram] 3.1 Budget Reservation: a
  * request's compressed footprint is fixed when it is scheduled, so its pages

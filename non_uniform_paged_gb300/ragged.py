@@ -24,7 +24,7 @@ import torch
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
                tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
                tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
-               SCORE_LET_NEXT_START)
+               SCORE_LET_NEXT_START, tg_tier_promote)
 
 BYTES_BF16 = 2
 
@@ -181,6 +181,90 @@ class SparseDecoder:
         ids = self.batch * self.H * self.K * 4
         qo = 2 * self.batch * self.H_q * self.d * BYTES_BF16
         return mm + kv + ids + qo
+
+
+class TieredSparseDecoder:
+    """Sparse decode of one layer with tiered KV placement ([FlexiCache] "Tiered KV placement").
+
+    Unstable heads keep all their pages in GPU memory (a dense region each).  A stable head
+    keeps only K GPU blocks, holding its current top-K pages; its whole KV stays in pinned host
+    memory.  A rerank scores the rows due (MinMax stays on the GPU), then tg_tier_promote
+    copies only the newly promoted pages of stable heads from host into the blocks their
+    demoted pages free, and writes every re-ranked row's decode list."""
+
+    def __init__(self, batch, H, H_q, d, P, n_pages, K, unstable_heads, n_cta=None, device="cuda"):
+        self.batch, self.H, self.H_q, self.d, self.P, self.n_pages, self.K = batch, H, H_q, d, P, n_pages, K
+        self.g = H_q // H
+        dev = torch.device(device)
+        self.dev = dev
+        total = batch * H
+        self.unstable_h = np.asarray(unstable_heads, dtype=np.uint8).reshape(H)
+        self.unstable_dev = torch.from_numpy(self.unstable_h.copy()).to(dev)
+        rows = np.arange(total)
+        self.unstable_rows = rows[self.unstable_h[rows % H] != 0]
+        self.stable_rows = rows[self.unstable_h[rows % H] == 0]
+        nu, ns = self.unstable_rows.size, self.stable_rows.size
+        self.page_elems = 2 * P * d
+        self.page_bytes = self.page_elems * BYTES_BF16
+        self.pool_pages = nu * n_pages + ns * K
+        dense_base = np.zeros(total, np.int64)
+        dense_base[self.unstable_rows] = np.arange(nu, dtype=np.int64) * n_pages
+        slot_block = np.full((total, K), -1, np.int32)
+        slot_block[self.stable_rows] = (nu * n_pages + np.arange(ns)[:, None] * K + np.arange(K)[None]).astype(np.int32)
+        self.dense_base = torch.from_numpy(dense_base).to(dev)
+        self.slot_block = torch.from_numpy(slot_block).to(dev)
+        self.slot_page = torch.full((total, K), -1, dtype=torch.int32, device=dev)
+        self.pool = torch.zeros(max(1, self.pool_pages) * self.page_elems, dtype=torch.bfloat16, device=dev)
+        self.host_kv = torch.empty(total * n_pages * self.page_elems, dtype=torch.bfloat16, pin_memory=True)
+        self.sel = torch.empty((total, K), dtype=torch.int32, device=dev)
+        self.pt_ids = torch.empty((total, K), dtype=torch.int32, device=dev)
+        self.promoted = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.score_ws = torch.zeros(tg_page_score_workspace(batch, H, n_pages), dtype=torch.uint8, device=dev)
+        self.all_rows = torch.arange(total, dtype=torch.int32, device=dev)
+        self.n_cta = int(n_cta) if n_cta else tg_query_ncta(d, self.g)
+        ntok = np.full((1, batch, H), K * P, np.int32)
+        self.S = tg_split_map(ntok.sum(axis=1).astype(np.int64), self.n_cta)
+        self.plan, self.workspace_bytes = tg_plan_decode(self.S, np.arange(H, dtype=np.int32)[None], ntok, H_q, 1, P, d)
+        self.plan_dev = torch.from_numpy(self.plan).to(dev)
+        self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.pt_off = torch.arange(0, total * K + 1, K, dtype=torch.int64, device=dev)
+        self.scale = 1.0 / math.sqrt(d)
+
+    def load(self, dense):
+        """Place a layer's dense cache [batch][H][n_pages][2][P][d] (GPU): unstable heads' pages
+        into their GPU regions, everything into the pinned host copy; stable heads' GPU blocks
+        start empty (the first rerank fills them)."""
+        flat = dense.reshape(self.batch * self.H, self.n_pages * self.page_elems)
+        self.host_kv.copy_(flat.reshape(-1))
+        if self.unstable_rows.size:
+            idx = torch.from_numpy(self.unstable_rows).to(self.dev)
+            region = self.pool[:self.unstable_rows.size * self.n_pages * self.page_elems]
+            region.view(self.unstable_rows.size, -1).copy_(flat.index_select(0, idx))
+        self.slot_page.fill_(-1)
+
+    def rerank(self, q, minmax, rows=None, n_rows=None, stream=None, grid_limit=0):
+        """Score the rows due (all by default), then fetch promoted pages and rebuild their lists."""
+        if rows is None:
+            rows, n_rows = self.all_rows, self.batch * self.H
+        if n_rows == 0:
+            return
+        tg_page_score_topk_rows(self.batch, self.H, self.g, self.d, self.n_pages, self.K, rows, n_rows, q, minmax,
+                                self.sel, workspace=self.score_ws, dev_status=self.status, stream=stream)
+        tg_tier_promote(rows, n_rows, self.unstable_dev, self.batch, self.H, self.n_pages, self.K, self.sel,
+                        self.slot_page, self.slot_block, self.dense_base, self.host_kv, self.page_bytes, self.pool,
+                        self.pt_ids, promoted=self.promoted, dev_status=self.status, grid_limit=grid_limit,
+                        stream=stream)
+
+    def attend(self, q, out, lse=None, stream=None):
+        tg_decode_attn(self.plan, self.plan_dev, 0, q, self.pool, self.pool_pages, self.pt_off, self.pt_ids,
+                       self.scale, self.workspace, out, lse=lse, dev_status=self.status, stream=stream)
+
+    def gpu_kv_bytes(self) -> int:
+        return self.pool_pages * self.page_bytes
+
+    def dense_kv_bytes(self) -> int:
+        return self.batch * self.H * self.n_pages * self.page_bytes
 
 
 class RerankSchedule:

@@ -29,7 +29,12 @@ Readings (also listed in the design doc):
   heads are due at the steps with (step + b * stagger) % period == 0
   (stagger 0: all requests together, so an all-stable layer is skipped at the
   other steps; stagger 1: one phase per request).  A head that is not due
-  keeps the pages it selected at its last rerank.
+  keeps the pages it selected at its last rerank;
+* "Tiered KV placement": a stable head's K GPU blocks hold exactly its current
+  top-K pages.  At a rerank the blocks whose page left the selection are
+  reused for the pages that entered it, the lowest entering page in the lowest
+  freed block slot; pages that stay are not moved.  An unstable head keeps all
+  its pages on the GPU, page p of its dense region at dense_base + p.
 """
 from __future__ import annotations
 
@@ -148,3 +153,20 @@ def stability_aware_selection(q_steps, mn_l, mx_l, K: int, unstable_layer, perio
             cur[b, h] = top_pages(page_scores(q[b, h * g:(h + 1) * g], mn_l[b, h], mx_l[b, h]), K)
         out.append(cur)
     return out
+
+
+def tier_promote(sel_row, slot_page_row, slot_block_row):
+    """One stable head's rerank.  Returns (new slot pages, copies [(slot, page)], decode list):
+    the decode list gives, for each selected page in ascending order, the block holding it."""
+    sel_row = [int(p) for p in sel_row]
+    old = [int(p) for p in slot_page_row]
+    want = set(sel_row)
+    freed = [k for k, p in enumerate(old) if p not in want]          # ascending slots
+    held = {p for p in old if p in want}
+    incoming = sorted(p for p in want if p not in held)               # ascending pages
+    new = list(old)
+    copies = list(zip(freed, incoming))
+    for k, p in copies:
+        new[k] = p
+    block_of = {p: int(slot_block_row[k]) for k, p in enumerate(new)}
+    return new, copies, [block_of[p] for p in sorted(sel_row)]

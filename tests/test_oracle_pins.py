@@ -546,6 +546,32 @@ def test_page_pool():
     pin_page_pool()
 
 
+def pin_tier_promote(fn=fx.tier_promote):
+    """In-place block reuse: a hand-derived rerank, the first fill of empty blocks, and for
+    random reranks: the blocks end holding exactly the selection, pages that stay keep
+    their block, and only the entering pages are copied."""
+    new, copies, dec = fn([1, 4, 6, 9], [9, 2, 4, 7], [100, 101, 102, 103])
+    assert new == [9, 1, 4, 6] and copies == [(1, 1), (3, 6)] and dec == [101, 102, 103, 100]
+    new, copies, dec = fn([0, 5, 7], [-1, -1, -1], [10, 11, 12])
+    assert new == [0, 5, 7] and copies == [(0, 0), (1, 5), (2, 7)] and dec == [10, 11, 12]
+    r = np.random.default_rng(15)
+    for _ in range(200):
+        n_pages, K = int(r.integers(1, 40)), 0
+        K = int(r.integers(1, n_pages + 1))
+        old = list(r.permutation(n_pages)[:K])
+        sel = sorted(r.permutation(n_pages)[:K].tolist())
+        blocks = list(r.permutation(1000)[:K])
+        new, copies, dec = fn(sel, old, blocks)
+        assert sorted(new) == sel
+        assert all(new[k] == old[k] for k in range(K) if old[k] in sel)
+        assert len(copies) == len(set(sel) - set(old))
+        assert [blocks[new.index(p)] for p in sel] == dec
+
+
+def test_tier_promote():
+    pin_tier_promote()
+
+
 # ------------------------------------------------- planted mistakes are caught
 
 def _wrong_ceil(B, N):
@@ -620,6 +646,10 @@ class _PoolFifo(opg.PagePool):
         self.free[-n:] = self.free[-n:][::-1]
 
 
+def _promote_moves_everything(sel_row, slot_page_row, slot_block_row):
+    return fx.tier_promote(sel_row, [-1] * len(slot_page_row), slot_block_row)
+
+
 def _rerank_phase_shifted(u, batch, step, period, stagger):
     return fx.rerank_rows(u, batch, step + 1, period, stagger)
 
@@ -648,6 +678,7 @@ def _selection_never_refreshed(q_steps, mn, mx, K, unstable, period, stagger):
     (pin_stability_aware_selection, _selection_never_refreshed),
     (pin_footprint, _footprint_min_head),
     (pin_page_pool, _PoolFifo),
+    (pin_tier_promote, _promote_moves_everything),
 ])
 def test_planted_mistake_is_caught(pin, mutant):
     with pytest.raises(AssertionError):
