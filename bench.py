@@ -260,7 +260,48 @@ def build_cache(w, device, n_cta=None, uniform=False):
     rows = {"plan_host_s": plan_s, "compact_topk_ms_per_layer": statistics.mean(comp_ms),
             "compact_topk_gbs": sum(comp_bytes) / (sum(comp_ms) * 1e-3) / 1e9,
             "pages": cache.n_pages, "pages_monolithic": cache.pages["n_pages_monolithic"]}
+    rows["chunked_prefill_compaction"] = chunked_compaction(w, cache, device, comp_ms)
     return cache, rows, N
+
+
+def chunked_compaction(w, cache, device, oneshot_ms, C=2048, layers=2):
+    """Retention fused into chunked prefill (tg_compact_chunk) on the first layers: the chunks
+    (scores, K, V of C tokens) are cut before the timed region, as a chunked prefill produces
+    them; the layers are then compacted again in one shot so the decode pool is unchanged."""
+    import non_uniform_paged_gb300 as tg
+    Nmax = int(synth.contexts(w).max())
+    if Nmax < 2 * C:
+        return None
+    res = []
+    for layer in range(min(layers, w.L)):
+        s = synth.scores(w, layer, device)
+        K, V = synth.keys_values(w, layer, device)
+        chunks = []
+        for start in range(0, Nmax, C):
+            end = min(Nmax, start + C)
+            sc = torch.zeros((w.batch, w.H, C), dtype=s.dtype, device=device)
+            kc = torch.zeros((w.batch, w.H, C, w.d), dtype=K.dtype, device=device)
+            vc = torch.zeros_like(kc)
+            sc[:, :, :end - start] = s[:, :, start:end]
+            kc[:, :, :end - start] = K[:, :, start:end]
+            vc[:, :, :end - start] = V[:, :, start:end]
+            chunks.append((sc, kc, vc))
+        e0, e1 = _events(2)
+        torch.cuda.synchronize()
+        e0.record()
+        cache.compact_layer_chunked(layer, s, K, V, C, chunks=iter(chunks))
+        e1.record()
+        torch.cuda.synchronize()
+        res.append(e0.elapsed_time(e1))
+        cache.compact_layer(layer, s, K, V)
+        del s, K, V, chunks
+    torch.cuda.synchronize()
+    tg.tg_check_status(cache.status)
+    n_chunks = -(-Nmax // C)
+    return {"chunk_tokens": C, "chunks_per_layer": n_chunks, "ms_per_layer": statistics.mean(res),
+            "us_per_chunk": 1e3 * statistics.mean(res) / n_chunks,
+            "vs_one_shot": statistics.mean(res) / statistics.mean(oneshot_ms[:len(res)]),
+            "layers_timed": len(res)}
 
 
 def cta_skew(w, cache, q, out, lse, stream, Bhat, N, device):

@@ -245,6 +245,31 @@ int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d,
                     const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool,
                     int32_t *kept_idx, int32_t *dev_status);
 
+/* ------------------------------------------------------------------ f1 ---
+ * tg_compact_chunk -- retention fused into chunked prefill: after each chunk of
+ *   C tokens, every head's n = ntok[b][h] reserved slots hold the best n tokens
+ *   seen so far (score descending, token ascending), so after the last chunk
+ *   they hold exactly Top(n, s) (a token's score is fixed once its chunk is
+ *   computed).  [Tangram] 3.1: compression runs inside chunked prefill; section 4
+ *   "Compression Fusion into Prefill".
+ *   Call it once per chunk, chunk_start = 0, C, 2C, ... (N[b] is the request's
+ *   full prompt length; tokens past it are ignored).  While a head's slots are
+ *   not full the chunk's tokens are appended; afterwards a slot whose token drops
+ *   out is reused: the lowest freed slot takes the lowest entering token, and only
+ *   entering tokens' K/V rows are written.  Slot k is page k/P, row k%P of the
+ *   head's block (as tg_compact_topk), so tg_decode_attn reads the result
+ *   unchanged; the tokens are in slot order, not ascending.
+ * Arguments (device): scores float32 [batch][H][C], K, V bf16 [batch][H][C][d]
+ *   (this chunk); head_order, ntok, pt_off, pt_ids, pool as tg_compact_topk;
+ *   slot_tok int32 and slot_key uint32 [batch][H][nmax] (state, nmax >= every
+ *   n; slot_tok[..][k] = the token in slot k).  C <= 8192; the first chunk also
+ *   zeroes the rows of each head's last page past n. */
+int tg_compact_chunk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int chunk_start, int C,
+                     const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
+                     const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
+                     const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool, int32_t *slot_tok,
+                     uint32_t *slot_key, int nmax, int32_t *dev_status);
+
 /* ------------------------------------------------------------------ a9 ---
  * tg_build_minmax -- per-page elementwise min and max of the keys (the MinMax
  *   cache of [FlexiCache] "Assumption 2"), exact in bf16.

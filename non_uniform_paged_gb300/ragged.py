@@ -24,7 +24,7 @@ import torch
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
                tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
                tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
-               SCORE_LET_NEXT_START, tg_tier_promote)
+               SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk)
 
 BYTES_BF16 = 2
 
@@ -107,6 +107,34 @@ class RaggedCache:
         tg_compact_topk(self.batch, self.H, self.H_p, self.P, self.d, Nmax, self.N_dev, scores, K, V,
                         self.order_dev[layer], self.ntok_dev[layer], self.list_offsets(layer), self.pt_ids_dev,
                         self.n_pages, self.pool, kept_idx=kept_idx, dev_status=self.status, stream=stream)
+
+    def compact_layer_chunked(self, layer, scores, K, V, C, stream=None, chunks=None):
+        """Retention fused into chunked prefill (tg_compact_chunk): the prompt's scores and K/V
+        arrive C tokens at a time; after the last chunk each head's slots hold its Top(n, s).
+        Returns the slot tokens [batch][H][nmax] (slot k of head (b, h) holds token [b, h, k]).
+        `chunks` (optional) yields the (scores, K, V) tensors of each chunk [batch][H][C](...);
+        by default they are cut from the full tensors."""
+        ntok = self.pages["ntok"][layer]
+        nmax = max(1, int(ntok.max()))
+        slot_tok = torch.full((self.batch, self.H, nmax), -1, dtype=torch.int32, device=self.device)
+        slot_key = torch.zeros((self.batch, self.H, nmax), dtype=torch.int32, device=self.device)
+        Nmax = scores.shape[-1]
+        for start in range(0, Nmax, C):
+            if chunks is not None:
+                sc, kc, vc = next(chunks)
+            else:
+                end = min(Nmax, start + C)
+                sc = torch.zeros((self.batch, self.H, C), dtype=scores.dtype, device=self.device)
+                kc = torch.zeros((self.batch, self.H, C, self.d), dtype=K.dtype, device=self.device)
+                vc = torch.zeros_like(kc)
+                sc[:, :, :end - start] = scores[:, :, start:end]
+                kc[:, :, :end - start] = K[:, :, start:end]
+                vc[:, :, :end - start] = V[:, :, start:end]
+            tg_compact_chunk(self.batch, self.H, self.H_p, self.P, self.d, start, C, self.N_dev, sc, kc, vc,
+                             self.order_dev[layer], self.ntok_dev[layer], self.list_offsets(layer),
+                             self.pt_ids_dev, self.n_pages, self.pool, slot_tok, slot_key,
+                             dev_status=self.status, stream=stream)
+        return slot_tok
 
     # ---- decode: one layer's attention
     def decode_layer(self, layer, q, out, lse=None, cta_time=None, stream=None, pool=None):

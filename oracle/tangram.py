@@ -34,6 +34,13 @@ Readings of points the page leaves open (each also listed in the design doc):
 * Work list: inside group i the retained tokens are concatenated in
   (request, head-in-group, token) order into W = Phi_{l,i} units; CTA j of
   the group's S_i CTAs takes units [floor(j W / S_i), floor((j+1) W / S_i)).
+* Chunked prefill (3.1, "compression fused into chunked prefill"): a head's n
+  slots are reserved at admission; after each chunk they hold the best n tokens
+  seen so far by (score descending, token ascending) -- a token's score is fixed
+  once its chunk is computed, so after the last chunk they hold Top(n, s).
+  While the slots are not full a chunk's tokens are appended in order; then a
+  slot whose token drops out goes to an entering token, the lowest freed slot to
+  the lowest entering token.
 * Attention: scale = 1/sqrt(d) unless given; the softmax runs over the
   retained set only (no causal mask, window or softcap); query head j reads
   KV head j // g (contiguous GQA groups).
@@ -279,3 +286,27 @@ def decode_layer(q_l, K_l, V_l, idx_l, scale, pairs=None):
         Vb = np.asarray(V_l[b, h], dtype=np.float64)[I]
         out[b, j], lse[b, j] = attention(q_l[b, j], Kb, Vb, scale)
     return out, lse
+
+
+def compact_chunked(s_row, n: int, C: int) -> list:
+    """Tokens in the n slots of one head after chunked-prefill retention (chunks of C)."""
+    s_row = np.asarray(s_row, dtype=np.float32)
+    if np.isnan(s_row).any():
+        raise ValueError("NaN score")
+    N = s_row.size
+    slots, filled = [None] * n, 0
+    for start in range(0, N, C):
+        chunk = list(range(start, min(N, start + C)))
+        if filled + len(chunk) <= n:
+            slots[filled:filled + len(chunk)] = chunk
+            filled += len(chunk)
+            continue
+        cands = slots[:filled] + chunk
+        ranked = sorted(cands, key=lambda t: (-float(s_row[t]), t))   # -0.0 == +0.0 as floats
+        keep = set(ranked[:n])
+        freed = [k for k in range(filled) if slots[k] not in keep] + list(range(filled, n))
+        incoming = sorted(t for t in chunk if t in keep)
+        for k, t in zip(freed, incoming):
+            slots[k] = t
+        filled = n
+    return slots

@@ -572,6 +572,36 @@ def test_tier_promote():
     pin_tier_promote()
 
 
+def pin_compact_chunked(fn=tg.compact_chunked):
+    """Chunked retention: after the last chunk the slots hold exactly the one-shot Top(n, s)
+    for every chunk size (ties included); one chunk holding everything gives the one-shot
+    ascending layout; and a hand-derived case fixes the slot reuse order."""
+    s = np.array([5, 1, 4, 2, 8, 0, 3, 9], np.float32)
+    # n = 4, C = 3.  Chunk [0, 1, 2] is appended to slots 0-2.  Chunk [3, 4, 5]: the best 4 of
+    # tokens 0-5 are 4, 0, 2, 3; slot 1 (token 1) and the empty slot 3 are freed and take the
+    # entering tokens 3 and 4, lowest slot first.
+    assert fn(s[:6], 4, 3) == [0, 3, 2, 4]
+    # chunk [6, 7]: the best 4 are 7, 4, 0, 2; slot 1 (token 3) is freed and takes token 7
+    assert fn(s, 4, 3) == [0, 7, 2, 4]
+    r = np.random.default_rng(16)
+    for _ in range(300):
+        N = int(r.integers(1, 60))
+        n = int(r.integers(1, N + 1))
+        C = int(r.integers(1, N + 3))
+        sc = r.integers(-4, 5, size=N).astype(np.float32) if r.random() < 0.5 else \
+            r.standard_normal(N).astype(np.float32)
+        if r.random() < 0.2:
+            sc[r.integers(0, N)] = -0.0
+        got = fn(sc, n, C)
+        assert sorted(got) == list(tg.top_indices(sc, n)), (N, n, C)
+        if C >= N:
+            assert got == list(tg.top_indices(sc, n))
+
+
+def test_compact_chunked():
+    pin_compact_chunked()
+
+
 # ------------------------------------------------- planted mistakes are caught
 
 def _wrong_ceil(B, N):
@@ -646,6 +676,14 @@ class _PoolFifo(opg.PagePool):
         self.free[-n:] = self.free[-n:][::-1]
 
 
+def _chunked_ties_high(s_row, n, C):
+    return list(_ties_high(s_row, n))        # equal scores resolved toward the higher token
+
+
+def _chunked_sorted_slots(s_row, n, C):
+    return sorted(tg.compact_chunked(s_row, n, C))  # slots rewritten in token order each chunk
+
+
 def _promote_moves_everything(sel_row, slot_page_row, slot_block_row):
     return fx.tier_promote(sel_row, [-1] * len(slot_page_row), slot_block_row)
 
@@ -679,6 +717,8 @@ def _selection_never_refreshed(q_steps, mn, mx, K, unstable, period, stagger):
     (pin_footprint, _footprint_min_head),
     (pin_page_pool, _PoolFifo),
     (pin_tier_promote, _promote_moves_everything),
+    (pin_compact_chunked, _chunked_ties_high),
+    (pin_compact_chunked, _chunked_sorted_slots),
 ])
 def test_planted_mistake_is_caught(pin, mutant):
     with pytest.raises(AssertionError):
