@@ -32,7 +32,7 @@ using namespace tgk;
 
 constexpr int kThreads = 1024;
 constexpr int kMaxChunk = 8192;        // tokens per chunk (entering-token list in shared memory)
-constexpr int kSmemKeys = 16384;       // candidates whose score keys are cached in shared memory
+constexpr int kSmemKeys = 45056;       // candidates whose score keys are cached in shared memory (176 KB)
 
 struct ChunkArgs {
   const int32_t *N;
