@@ -22,7 +22,7 @@ __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
-           "tg_compact_chunk", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
+           "tg_sparse_layer", "tg_compact_chunk", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
@@ -51,6 +51,7 @@ _SIGS = {
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, ctypes.c_uint32, _P]),
     "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
+    "tg_sparse_layer": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _L, _I, _P, _L, _P, _F, _P, _L, _P, _P, _P]),
     "tg_compact_chunk": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P, _I,
                               _P]),
     "tg_tier_promote": (_I, [_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _L, _P, _P, _P]),
@@ -262,6 +263,21 @@ def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok
                                _dev(pt_ids, torch.int32, "pt_ids"), int(pool_pages),
                                _dev(pool, torch.bfloat16, "pool"), _dev(kept_idx, torch.int32, "kept_idx"),
                                _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_sparse_layer(plan_host, plan_dev, n_pages, K, q, minmax, sel, pt_ids, score_ws, epoch, pool, pool_pages,
+                    pt_off, scale, workspace, out, lse=None, dev_status=None, stream=None):
+    """Score + top-K + sparse decode of one layer in one kernel (tg.h: tg_sparse_layer)."""
+    import torch
+    _check(load().tg_sparse_layer(_stream(stream), plan_host.ctypes.data, _dev(plan_dev, torch.uint8, "plan_dev"),
+                                  int(n_pages), int(K), _dev(q, torch.bfloat16, "q"),
+                                  _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
+                                  _dev(pt_ids, torch.int32, "pt_ids"), _dev(score_ws, torch.uint8, "score_ws"),
+                                  score_ws.numel(), int(epoch), _dev(pool, torch.bfloat16, "pool"), int(pool_pages),
+                                  _dev(pt_off, torch.int64, "pt_off"), float(scale),
+                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                  _dev(out, torch.bfloat16, "out"), _dev(lse, torch.float32, "lse"),
+                                  _dev(dev_status, torch.int32, "dev_status")))
 
 
 def tg_compact_chunk(batch, H, H_p, P, d, chunk_start, C, N, scores, K, V, head_order, ntok, pt_off, pt_ids,

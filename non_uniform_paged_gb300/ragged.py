@@ -24,7 +24,7 @@ import torch
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
                tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
                tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
-               SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk)
+               SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk, tg_sparse_layer)
 
 BYTES_BF16 = 2
 
@@ -199,6 +199,13 @@ class SparseDecoder:
     def step(self, q, minmax, pool, out, lse=None, stream=None, layer=0):
         self.select(q, minmax, stream=stream, layer=layer)
         self.attend(q, pool, out, lse=lse, stream=stream, layer=layer)
+
+    def step_fused(self, q, minmax, pool, out, lse=None, stream=None, layer=0):
+        """select + attend of every row in one kernel (tg_sparse_layer; d = 128, n_pages <= 1024)."""
+        self._epoch = getattr(self, "_epoch", 0) % (2 ** 31 - 2) + 1
+        tg_sparse_layer(self.plan, self.plan_dev, self.n_pages, self.K, q, minmax, self.sel[layer],
+                        self.pt_ids[layer], self.score_ws, self._epoch, pool, self.batch * self.H * self.n_pages,
+                        self.pt_off, self.scale, self.workspace, out, lse=lse, dev_status=self.status, stream=stream)
 
     def algorithmic_bytes(self, scored_rows=None) -> int:
         """MinMax read (of the scored rows; all by default) + selected K/V pages + page ids +

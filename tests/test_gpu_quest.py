@@ -311,6 +311,34 @@ def test_sparse_layers_back_to_back(lib, cuda, overlap):
         compare_out(outs[l], lses[l], ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("g,K", [(4, 6), (1, 3), (8, 10)])
+def test_fused_layer_equals_separate_kernels(lib, cuda, g, K):
+    """tg_sparse_layer (score, top-K and decode in one kernel) gives the separate kernels'
+    selection and output bit for bit, over several layers queued back to back."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=3, N=480, L=3, H_q=8 * g)
+    P, n_pages = w.P, w.N // w.P
+    fused = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=40, device=cuda, layers=w.L)
+    sep = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=40, device=cuda, layers=w.L)
+    layers = []
+    for l in range(w.L):
+        Kt, Vt = synth.keys_values(w, l, cuda)
+        layers.append((synth.queries(w, l, cuda), build_minmax(Kt, P), _dense_pool(Kt, Vt, P)))
+    mk = lambda: (torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda),
+                  torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda))
+    res_f = [mk() for _ in range(w.L)]
+    res_s = [mk() for _ in range(w.L)]
+    for rep in range(2):
+        for l, (q, mm, pool) in enumerate(layers):
+            fused.step_fused(q, mm, pool, *res_f[l], layer=l)
+            sep.step(q, mm, pool, *res_s[l], layer=l)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(fused.status) == 0 and lib.tg_check_status(sep.status) == 0
+    assert torch.equal(fused.sel, sep.sel) and torch.equal(fused.pt_ids, sep.pt_ids)
+    for l in range(w.L):
+        assert torch.equal(res_f[l][0], res_s[l][0]) and torch.equal(res_f[l][1], res_s[l][1]), l
+
+
 def test_all_pages_equals_dense(lib, cuda):
     """K = n_pages: sparse decode is dense attention over the whole context."""
     from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
