@@ -704,7 +704,7 @@ def bench_tiered(args, w, q, mms, pools, out, stream, device, layers=4, steps=32
                 if st == 0:
                     rows, n = None, None  # every row at the first step
                 if tiered_mode:
-                    tiers[l].rerank(qs[l][st], mms[l], rows, n, stream=stream)
+                    tiers[l].rerank(qs[l][st], mms[l], rows, n, stream=stream, stable_due=st % period == 0)
                     tiers[l].attend(qs[l][st], out, stream=stream)
                 else:
                     if st == 0:

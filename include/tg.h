@@ -320,12 +320,15 @@ int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n
  *   rerank are scored; every other row keeps its previous sel / pt_ids.
  *   rows: device int32 [n_rows], distinct row numbers b*H + h in [0, batch*H)
  *   (an entry outside that range sets TG_STATUS_BAD_INPUT and is skipped).
- *   n_rows = 0 launches nothing.  Everything else as tg_page_score_topk, with
- *   sel / pt_ids still indexed by row (only the listed rows are written). */
+ *   n_rows = 0 launches nothing.  dense_base (device int64 [batch*H], may be NULL)
+ *   gives each row's page-id base: pt_ids[r][k] = dense_base[r] + sel[r][k]
+ *   (NULL: r*n_pages, as tg_page_score_topk).  Everything else as
+ *   tg_page_score_topk, with sel / pt_ids still indexed by row (only the listed
+ *   rows are written). */
 int tg_page_score_topk_rows(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                             int n_rows, const int32_t *rows, const uint16_t *q, const uint16_t *minmax,
-                            int32_t *sel, int32_t *pt_ids, void *workspace, int64_t workspace_bytes,
-                            uint32_t flags, int32_t *dev_status);
+                            int32_t *sel, int32_t *pt_ids, const int64_t *dense_base, void *workspace,
+                            int64_t workspace_bytes, uint32_t flags, int32_t *dev_status);
 
 /* tg_rerank_rows -- the rows of one layer due for a rerank at a decode step (host).
  *   [FlexiCache] "Core method" (stable heads re-ranked every 16 steps, unstable

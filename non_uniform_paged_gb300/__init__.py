@@ -61,8 +61,8 @@ _SIGS = {
     "tg_alloc_release": (_I, [_P, _L, _P]),
     "tg_alloc_query": (_I, [_P, _P, _P]),
     "tg_page_score_workspace": (_I, [_I, _I, _I, _P]),
-    "tg_page_score_topk_rows": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _L, ctypes.c_uint32,
-                                     _P]),
+    "tg_page_score_topk_rows": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _L,
+                                     ctypes.c_uint32, _P]),
     "tg_rerank_rows": (_I, [_I, _I, _I, _P, _I, _I, _I, _I, _P, _P]),
     "tg_check_status": (_I, [_P, _P]),
 }
@@ -336,7 +336,7 @@ def tg_page_score_topk(batch, H, g, d, n_pages, K, q, minmax, sel, pt_ids=None, 
 
 
 def tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows, n_rows, q, minmax, sel, pt_ids=None, workspace=None,
-                            dev_status=None, stream=None, flags=0):
+                            dev_status=None, stream=None, flags=0, dense_base=None):
     """tg_page_score_topk over the listed rows only (tg.h: tg_page_score_topk_rows).  rows is a
     device int32 tensor whose first n_rows entries are used."""
     import torch
@@ -346,7 +346,8 @@ def tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows, n_rows, q, minmax,
     _check(lib.tg_page_score_topk_rows(_stream(stream), batch, H, g, d, n_pages, K, int(n_rows),
                                        _dev(rows, torch.int32, "rows"), _dev(q, torch.bfloat16, "q"),
                                        _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
-                                       _dev(pt_ids, torch.int32, "pt_ids"), _dev(workspace, torch.uint8, "workspace"),
+                                       _dev(pt_ids, torch.int32, "pt_ids"), _dev(dense_base, torch.int64, "dense_base"),
+                                       _dev(workspace, torch.uint8, "workspace"),
                                        workspace.numel() * workspace.element_size(), int(flags),
                                        _dev(dev_status, torch.int32, "dev_status")))
 

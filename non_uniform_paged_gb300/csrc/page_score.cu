@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NW * 32, 1) page_score_kernel(con
 // One CTA per (request, KV head): top-K of the row's keys, ascending, ties to the lower page.
 __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t *keys, const int32_t *rows,
                                                                   int64_t total_rows, int n_pages, int K,
-                                                                  int32_t *sel, int32_t *pt_ids) {
+                                                                  int32_t *sel, int32_t *pt_ids,
+                                                                  const int64_t *dense_base) {
   extern __shared__ uint32_t skeys[];  // [n_pages]
   __shared__ int hist[256];
   __shared__ int scan[33];
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kSelThreads) page_select_kernel(const uint32_t
     const int k = taken + block_excl_count<kSelThreads>(take, scan, sel_total);
     if (take) {
       sel[(size_t)out_row * K + k] = p;
-      if (pt_ids) pt_ids[(size_t)out_row * K + k] = (int32_t)(out_row * n_pages + p);
+      if (pt_ids) pt_ids[(size_t)out_row * K + k] = (int32_t)((dense_base ? dense_base[out_row] : out_row * n_pages) + p);
     }
     taken += sel_total;
     eq_seen += eq_total;
@@ -127,7 +128,7 @@ cudaError_t launch_score_d(const ScoreArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_select(const uint32_t *keys, const int32_t *rows, int64_t total_rows, int n_rows, int n_pages,
-                          int K, int32_t *sel, int32_t *pt_ids, cudaStream_t s) {
+                          int K, int32_t *sel, int32_t *pt_ids, const int64_t *dense_base, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(page_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxPages * 4);
   if (e != cudaSuccess) return e;
@@ -142,7 +143,7 @@ cudaError_t launch_select(const uint32_t *keys, const int32_t *rows, int64_t tot
   cfg.gridDim = dim3(n_rows);
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = (size_t)n_pages * 4;
-  return cudaLaunchKernelEx(&cfg, page_select_kernel, keys, rows, total_rows, n_pages, K, sel, pt_ids);
+  return cudaLaunchKernelEx(&cfg, page_select_kernel, keys, rows, total_rows, n_pages, K, sel, pt_ids, dense_base);
 }
 
 // minmax[b][h][p][0][:] = min over the page's valid keys, [1][:] = max (exact in bf16)
@@ -184,7 +185,8 @@ extern "C" int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *w
 namespace {
 int score_topk(const char *fn, tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K, int n_rows,
                const int32_t *rows, const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
-               void *workspace, int64_t workspace_bytes, uint32_t flags, int32_t *dev_status) {
+               const int64_t *dense_base, void *workspace, int64_t workspace_bytes, uint32_t flags,
+               int32_t *dev_status) {
   if (flags & ~TG_SCORE_LET_NEXT_START) return tgi::fail(TG_ERR_INVALID_ARG, "%s: unknown flags 0x%x", fn, flags);
   if (batch < 0 || H <= 0 || g < 1 || g > 8) return tgi::fail(TG_ERR_INVALID_ARG, "%s: bad batch/H/g", fn);
   if (d != 128 && d != 256) return tgi::fail(TG_ERR_SHAPE, "%s: d=%d (128 or 256)", fn, d);
@@ -218,11 +220,13 @@ int score_topk(const char *fn, tg_stream_t stream, int batch, int H, int g, int 
   a.K = K;
   a.fused = n_pages <= 32 * kWarpKeysMax;
   a.let_next = (flags & TG_SCORE_LET_NEXT_START) != 0;
+  a.dense_base = dense_base;
   a.row_ready = nullptr;
   a.epoch = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = d == 128 ? launch_score_d<128>(a, s) : launch_score_d<256>(a, s);
-  if (e == cudaSuccess && !a.fused) e = launch_select(a.keys, rows, a.total_rows, n_rows, n_pages, K, sel, pt_ids, s);
+  if (e == cudaSuccess && !a.fused)
+    e = launch_select(a.keys, rows, a.total_rows, n_rows, n_pages, K, sel, pt_ids, dense_base, s);
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return tgi::ok();
 }
@@ -232,16 +236,16 @@ extern "C" int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, i
                                   const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
                                   void *workspace, int64_t workspace_bytes, uint32_t flags, int32_t *dev_status) {
   return score_topk("tg_page_score_topk", stream, batch, H, g, d, n_pages, K, batch * H, nullptr, q, minmax, sel,
-                    pt_ids, workspace, workspace_bytes, flags, dev_status);
+                    pt_ids, nullptr, workspace, workspace_bytes, flags, dev_status);
 }
 
 extern "C" int tg_page_score_topk_rows(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                                        int n_rows, const int32_t *rows, const uint16_t *q, const uint16_t *minmax,
-                                       int32_t *sel, int32_t *pt_ids, void *workspace, int64_t workspace_bytes,
-                                       uint32_t flags, int32_t *dev_status) {
+                                       int32_t *sel, int32_t *pt_ids, const int64_t *dense_base, void *workspace,
+                                       int64_t workspace_bytes, uint32_t flags, int32_t *dev_status) {
   if (n_rows > 0 && !rows) return tgi::fail(TG_ERR_INVALID_ARG, "tg_page_score_topk_rows: NULL rows");
   return score_topk("tg_page_score_topk_rows", stream, batch, H, g, d, n_pages, K, n_rows, rows, q, minmax, sel,
-                    pt_ids, workspace, workspace_bytes, flags, dev_status);
+                    pt_ids, dense_base, workspace, workspace_bytes, flags, dev_status);
 }
 
 extern "C" int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d, const uint16_t *K,

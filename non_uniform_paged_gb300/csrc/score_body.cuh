@@ -48,6 +48,7 @@ struct ScoreArgs {
   int g, n_pages, K;
   int fused;           // the warp that completes a row selects its top K (n_pages <= 1024)
   int let_next;        // let the next kernel start early (it waits before reading sel / pt_ids)
+  const int64_t *dense_base;  // [rows] page id of a row's page 0 in pt_ids (NULL: row * n_pages)
   int32_t *row_ready;  // [rows] set to `epoch` once a row's selection is written (NULL: not kept)
   int epoch;
 };
@@ -114,7 +115,7 @@ constexpr int kRowQueue = 64;  // completed rows a score CTA queues for its warp
 
 template <int KPL>
 __device__ __noinline__ void warp_select_row(const uint32_t *rk, int n_pages, int K, int64_t row, int32_t *sel,
-                                             int32_t *pt_ids) {
+                                             int32_t *pt_ids, int64_t id_base) {
   const int lane = threadIdx.x & 31;
   uint32_t key[KPL];
   uint32_t k_and = 0xffffffffu, k_or = 0u;
@@ -158,7 +159,7 @@ __device__ __noinline__ void warp_select_row(const uint32_t *rk, int n_pages, in
       const int pos = taken + __popc(btake & lt);
       const int p = 32 * i + lane;
       sel[(size_t)row * K + pos] = p;
-      if (pt_ids) pt_ids[(size_t)row * K + pos] = (int32_t)(row * n_pages + p);
+      if (pt_ids) pt_ids[(size_t)row * K + pos] = (int32_t)(id_base + p);
     }
     taken += __popc(btake);
     eq_seen += __popc(beq);
@@ -167,13 +168,13 @@ __device__ __noinline__ void warp_select_row(const uint32_t *rk, int n_pages, in
 
 // the KPL bucket for n_pages <= 32 * kWarpKeysMax
 __device__ __forceinline__ void warp_select(const uint32_t *rk, int n_pages, int K, int64_t row, int32_t *sel,
-                                            int32_t *pt_ids) {
+                                            int32_t *pt_ids, int64_t id_base) {
   const int kpl = (n_pages + 31) / 32;
-  if (kpl <= 4) warp_select_row<4>(rk, n_pages, K, row, sel, pt_ids);
-  else if (kpl <= 8) warp_select_row<8>(rk, n_pages, K, row, sel, pt_ids);
-  else if (kpl <= 16) warp_select_row<16>(rk, n_pages, K, row, sel, pt_ids);
-  else if (kpl <= 24) warp_select_row<24>(rk, n_pages, K, row, sel, pt_ids);
-  else warp_select_row<32>(rk, n_pages, K, row, sel, pt_ids);
+  if (kpl <= 4) warp_select_row<4>(rk, n_pages, K, row, sel, pt_ids, id_base);
+  else if (kpl <= 8) warp_select_row<8>(rk, n_pages, K, row, sel, pt_ids, id_base);
+  else if (kpl <= 16) warp_select_row<16>(rk, n_pages, K, row, sel, pt_ids, id_base);
+  else if (kpl <= 24) warp_select_row<24>(rk, n_pages, K, row, sel, pt_ids, id_base);
+  else warp_select_row<32>(rk, n_pages, K, row, sel, pt_ids, id_base);
 }
 
 // The scoring (and, with a.fused, the selection) done by one CTA; smem: ScoreCfg<D>::SMEM bytes
@@ -476,7 +477,8 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
       for (int i = warp; i < nq; i += NW) {
         const int64_t r = s_rows[i];
         const int64_t out = row_id(r);
-        if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids);
+        if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids,
+                                  a.dense_base ? a.dense_base[out] : out * a.n_pages);
         if (lane == 0) {
           a.row_cnt[r] = 0;
           if (a.row_ready && out >= 0) publish_ready(a.row_ready + out, a.epoch);
@@ -497,7 +499,8 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
           __threadfence();
           griddep_wait();
           const int64_t out = row_id(r);
-          if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids);
+          if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids,
+                                  a.dense_base ? a.dense_base[out] : out * a.n_pages);
           if (lane == 0) {
             a.row_cnt[r] = 0;
             if (a.row_ready && out >= 0) publish_ready(a.row_ready + out, a.epoch);

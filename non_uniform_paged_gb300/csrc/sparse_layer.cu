@@ -127,6 +127,7 @@ extern "C" int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const 
   sa.K = K;
   sa.fused = 1;
   sa.let_next = 0;
+  sa.dense_base = nullptr;
   sa.row_ready = ready;
   sa.epoch = epoch;
   DecodeArgs da = decode_args(hd, lt, plan_dev, static_cast<uint8_t *>(workspace), q, out, lse, pt_off, pt_ids,

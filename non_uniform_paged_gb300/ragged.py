@@ -278,14 +278,19 @@ class TieredSparseDecoder:
             region.view(self.unstable_rows.size, -1).copy_(flat.index_select(0, idx))
         self.slot_page.fill_(-1)
 
-    def rerank(self, q, minmax, rows=None, n_rows=None, stream=None, grid_limit=0):
-        """Score the rows due (all by default), then fetch promoted pages and rebuild their lists."""
+    def rerank(self, q, minmax, rows=None, n_rows=None, stream=None, grid_limit=0, stable_due=True):
+        """Score the rows due (all by default): the score kernel writes the decode lists of the
+        unstable rows (dense region + selection); when stable rows are among them
+        (stable_due), tg_tier_promote then fetches their promoted pages and rebuilds their lists."""
         if rows is None:
             rows, n_rows = self.all_rows, self.batch * self.H
         if n_rows == 0:
             return
         tg_page_score_topk_rows(self.batch, self.H, self.g, self.d, self.n_pages, self.K, rows, n_rows, q, minmax,
-                                self.sel, workspace=self.score_ws, dev_status=self.status, stream=stream)
+                                self.sel, pt_ids=self.pt_ids, dense_base=self.dense_base, workspace=self.score_ws,
+                                dev_status=self.status, stream=stream)
+        if not stable_due:
+            return
         tg_tier_promote(rows, n_rows, self.unstable_dev, self.batch, self.H, self.n_pages, self.K, self.sel,
                         self.slot_page, self.slot_block, self.dense_base, self.host_kv, self.page_bytes, self.pool,
                         self.pt_ids, promoted=self.promoted, dev_status=self.status, grid_limit=grid_limit,

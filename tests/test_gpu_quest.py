@@ -165,8 +165,9 @@ def test_select_rows_only_touches_listed_rows(lib, cuda, n_pages, K):
     sel = torch.full((batch, H, K), -7, dtype=torch.int32, device=cuda)
     ids = torch.full((batch, H, K), -7, dtype=torch.int32, device=cuda)
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    base = torch.from_numpy(np.arange(batch * H, dtype=np.int64) * 1000 + 7).to(cuda) if n_pages == 625 else None
     lib.tg_page_score_topk_rows(batch, H, g, d, n_pages, K, rows_dev, rows.size, q, mm, sel, pt_ids=ids,
-                                dev_status=status)
+                                dev_status=status, dense_base=base)
     torch.cuda.synchronize()
     assert lib.tg_check_status(status) == 0
     ref = ofx.select_pages(q.float().cpu().numpy(), mm.float().cpu().numpy()[:, :, :, 0],
@@ -176,7 +177,8 @@ def test_select_rows_only_touches_listed_rows(lib, cuda, n_pages, K):
         b, h = divmod(r, H)
         if r in rows:
             assert np.array_equal(got[b, h], ref[b, h]), r
-            assert np.array_equal(got_ids[b, h], r * n_pages + ref[b, h]), r
+            first = r * 1000 + 7 if base is not None else r * n_pages  # the row's page-id base
+            assert np.array_equal(got_ids[b, h], first + ref[b, h]), r
         else:
             assert (got[b, h] == -7).all() and (got_ids[b, h] == -7).all(), r
 

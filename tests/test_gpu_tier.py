@@ -121,11 +121,17 @@ def test_tiered_decode_equals_all_gpu_sparse(lib, cuda):
     gen.manual_seed(5)
     q = synth.queries(w, 0, cuda).float()
     copies_before = 0
-    for step in range(4):
+    unstable_rows = torch.tensor([r for r in range(w.batch * w.H) if unstable[r % w.H]], dtype=torch.int32,
+                                 device=cuda)
+    for step in range(6):
         q = q + 0.4 * torch.randn(q.shape, generator=gen, device=cuda)
         qb = q.to(torch.bfloat16)
-        tier.rerank(qb, mm)
-        ref.select(qb, mm)
+        if step % 2:  # only the unstable heads: the score kernel writes their lists, no promote
+            tier.rerank(qb, mm, unstable_rows, unstable_rows.numel(), stable_due=False)
+            ref.select_rows(qb, mm, unstable_rows, unstable_rows.numel())
+        else:
+            tier.rerank(qb, mm)
+            ref.select(qb, mm)
         out_t = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
         out_r = torch.empty_like(out_t)
         lse_t = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
@@ -140,6 +146,8 @@ def test_tiered_decode_equals_all_gpu_sparse(lib, cuda):
         stable_rows = w.batch * int((unstable == 0).sum())
         if step == 0:
             assert copies == stable_rows * K       # the first rerank fills every block
+        elif step % 2:
+            assert copies == copies_before         # unstable-only steps copy nothing
         else:
             assert copies - copies_before < stable_rows * K  # later ones move only what changed
         copies_before = copies
