@@ -13,8 +13,9 @@
 // Top(n, s).  One CTA per (request, KV head) row and chunk:
 //  * while the slots are not full, the chunk's tokens are appended in order;
 //  * otherwise the current slots and the chunk's tokens are ranked together by
-//    two radix selects (score key, then ~token among the keys equal to the
-//    n-th score) -- a total order, so exactly n survive.  The slots whose token
+//    a radix select on the score key and, only when the n-th score is tied
+//    across the cut, one on ~token among the keys equal to it -- a total
+//    order, so exactly n survive.  The slots whose token
 //    dropped out are reused, the lowest freed slot by the lowest entering token,
 //    and only the entering tokens' K/V rows are written into the pages.
 // Slot k lives at page k / P, row k % P of the head's block in its group page,
@@ -32,7 +33,96 @@ using namespace tgk;
 
 constexpr int kThreads = 1024;
 constexpr int kMaxChunk = 8192;        // tokens per chunk (entering-token list in shared memory)
-constexpr int kSmemKeys = 45056;       // candidates whose score keys are cached in shared memory (176 KB)
+constexpr int kSmemKeys = 40960;       // candidates whose score keys are cached in shared memory (160 KB)
+constexpr int kCopyUnroll = 4;         // 16-byte K/V vectors each thread has in flight while copying
+
+constexpr int kWarps = kThreads / 32;
+
+// Key T of the k-th largest of `count` keys (1 <= k <= count), the number of keys equal to T that
+// a top-k takes (need_eq = k - #{key > T}) and the number of keys equal to T (n_eq).  MSB-first
+// radix select over 8-bit digits.  After the first pass the keys that share the chosen top digit
+// are copied into `list` when at most `cap` of them do, and the remaining passes read only those
+// (the first digit of real scores already narrows the candidates to a few percent).  `hist` is
+// 256 ints and `scratch` 4 ints of shared memory.
+template <typename GetKey>
+__device__ void select_kth(int count, int k, GetKey get, uint32_t *list, int cap, int *hist, int *scratch,
+                           uint32_t &T, int &need_eq, int &n_eq) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, mask = 0;
+  int k_rem = k, n_list = -1, sel_count = count;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    const int cnt = n_list < 0 ? count : n_list;
+    for (int base = 0; base < cnt; base += kThreads) {
+      const int i = base + tid;
+      uint32_t dg = 256u;  // no digit
+      if (i < cnt) {
+        const uint32_t key = n_list < 0 ? get(i) : list[i];
+        if ((key & mask) == prefix) dg = (key >> shift) & 255u;
+      }
+      // lanes of a warp with the same digit add once
+      const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+      if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down
+      int local[8];
+      int sum = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        local[t] = hist[255 - 8 * lane - t];
+        sum += local[t];
+      }
+      int inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const int before = inc - sum;  // keys in digits above this lane's block
+      if (before < k_rem && k_rem <= inc) {
+        int above = before;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (above + local[t] >= k_rem) {
+            scratch[0] = 255 - 8 * lane - t;
+            scratch[1] = above;
+            scratch[2] = local[t];
+            break;
+          }
+          above += local[t];
+        }
+      }
+      if (lane == 0) scratch[3] = 0;
+    }
+    __syncthreads();
+    const uint32_t digit = (uint32_t)scratch[0];
+    k_rem -= scratch[1];
+    sel_count = scratch[2];
+    prefix |= digit << shift;
+    mask |= 255u << shift;
+    if (n_list < 0 && shift > 0 && sel_count <= cap) {
+      // copy the keys under the new prefix into the list (order does not matter for counts)
+      for (int base = 0; base < count; base += kThreads) {
+        const int i = base + tid;
+        uint32_t key = 0;
+        const bool keep = i < count && ((key = get(i)) & mask) == prefix;
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        int at = 0;
+        if (lane == 0 && bal) at = atomicAdd(&scratch[3], __popc(bal));
+        at = __shfl_sync(0xffffffffu, at, 0);
+        if (keep) list[at + __popc(bal & ((1u << lane) - 1u))] = key;
+      }
+      n_list = sel_count;
+    }
+    __syncthreads();
+  }
+  T = prefix;
+  need_eq = k_rem;
+  n_eq = sel_count;
+}
 
 struct ChunkArgs {
   const int32_t *N;
@@ -54,7 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   __shared__ int hist[256];
   __shared__ int scan[33];
   __shared__ int sel_scratch[4];
-  __shared__ int incoming[kMaxChunk];  // entering chunk positions, ascending
+  // the selects' key list, then: entering chunk positions (ascending) and the slot each takes
+  __shared__ int work[2 * kMaxChunk];
+  int *const incoming = work, *const slot_of = work + kMaxChunk;
   __shared__ int err_flag;
 
   const int row = blockIdx.x, b = row / a.H, h = row % a.H, tid = threadIdx.x;
@@ -101,20 +193,28 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
 
   // candidates: i < filled is slot i (its token and key), i >= filled is chunk position i - filled
   const int m = filled + len;
-  const bool cached = m <= kSmemKeys;
+  const bool append = m <= n;  // the slots are not full yet: every chunk token enters
+  const bool cached = !append && m <= kSmemKeys;
   bool nan_seen = false;
-  if (cached)
-    for (int i = tid; i < m; i += kThreads) {
-      if (i < filled) {
-        cache[i] = skey[i];
-      } else {
-        const float f = cs[i - filled];
-        nan_seen |= is_nan(f);
-        cache[i] = float_key(f);
+  if (cached) {
+    // the slot keys: several independent loads in flight per thread
+    for (int i0 = tid; i0 < filled; i0 += kCopyUnroll * kThreads) {
+      uint32_t v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int i = i0 + u * kThreads;
+        v[u] = i < filled ? __ldcg(skey + i) : 0u;
       }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (i0 + u * kThreads < filled) cache[i0 + u * kThreads] = v[u];
     }
-  else
-    for (int i = tid; i < len; i += kThreads) nan_seen |= is_nan(cs[i]);
+  }
+  for (int i = tid; i < len; i += kThreads) {
+    const float f = cs[i];
+    nan_seen |= is_nan(f);
+    if (cached) cache[filled + i] = float_key(f);
+  }
   if (nan_seen) err_flag = 1;
   __syncthreads();
   if (err_flag && tid == 0) report(a.status, TG_STATUS_NONFINITE);
@@ -126,14 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   // which chunk positions enter, and which slots they take
   int n_in = 0;
   uint32_t T_hi = 0u, T_lo = 0u;
-  const bool append = m <= n;  // the slots are not full yet: every chunk token enters
   if (!append) {
-    int need_hi;
-    block_radix_select<kThreads>(m, n, hi_of, hist, sel_scratch, T_hi, need_hi);
-    // among the keys equal to T_hi, the need_hi lowest tokens (largest ~token) survive
-    int unused;
-    block_radix_select<kThreads>(m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; },
-                                 hist, sel_scratch, T_lo, unused);
+    uint32_t *const list = reinterpret_cast<uint32_t *>(work);
+    int need_hi, n_eq;
+    select_kth(m, n, hi_of, list, 2 * kMaxChunk, hist, sel_scratch, T_hi, need_hi, n_eq);
+    // among the keys equal to T_hi, the need_hi lowest tokens (largest ~token) survive; with no
+    // tie across the cut every one of them does, and T_lo = 0 keeps them all
+    if (n_eq > need_hi) {
+      int unused0, unused1;
+      select_kth(m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; }, list,
+                 2 * kMaxChunk, hist, sel_scratch, T_lo, unused0, unused1);
+    }
   }
   auto survives = [&](int i) {
     if (append) return true;
@@ -150,39 +253,84 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   }
   __syncthreads();
   // freed slots in ascending order: dropped current slots, then the empty slots filled..n-1;
-  // the r-th freed slot takes incoming[r]
-  int freed = 0;
-  for (int s0 = 0; s0 < n && freed < n_in; s0 += kThreads) {
-    const int s = s0 + tid;
-    const bool fr = s < n && (s >= filled || !survives(s));
-    int total;
-    const int r = freed + block_excl_count<kThreads>(fr, scan, total);
-    int take = -1;
-    if (fr && r < n_in) take = incoming[r];
-    freed += total;
-    __syncthreads();  // every thread has read the old slot state of this block of slots
-    if (take >= 0) {
-      stok[s] = a.chunk_start + take;
-      skey[s] = float_key(cs[take]);
-      incoming[r] = -1 - s;  // remember the slot for the copy below
+  // the r-th freed slot takes incoming[r].  Warp w scans the slots [w*seg, (w+1)*seg): it counts
+  // its freed slots, a scan over the warps gives its first rank, and a second sweep assigns.  A
+  // lane writes only its own slot, whose old state it has just read.
+  if (append) {
+    // every chunk position enters, in order, into the empty slots filled, filled + 1, ...
+    for (int r = tid; r < n_in; r += kThreads) {
+      stok[filled + r] = a.chunk_start + r;
+      skey[filled + r] = float_key(cs[r]);
+      slot_of[r] = filled + r;
+    }
+  } else if (n_in > 0) {
+    const int lane = tid & 31, warp = tid >> 5;
+    const int seg = (((n + kWarps - 1) / kWarps) + 31) & ~31;
+    const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+    auto is_freed = [&](int s) { return s < hi && (s >= filled || !survives(s)); };
+    int cnt = 0;
+    for (int s0 = lo; s0 < hi; s0 += 32) cnt += __popc(__ballot_sync(0xffffffffu, is_freed(s0 + lane)));
+    if (lane == 0) scan[warp] = cnt;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = scan[lane];
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      scan[lane] = inc - v;
+    }
+    __syncthreads();
+    int r0 = scan[warp];
+    for (int s0 = lo; s0 < hi && r0 < n_in; s0 += 32) {
+      const int s = s0 + lane;
+      const bool fr = is_freed(s);
+      const uint32_t bal = __ballot_sync(0xffffffffu, fr);
+      const int r = r0 + __popc(bal & ((1u << lane) - 1u));
+      if (fr && r < n_in) {
+        const int take = incoming[r];
+        stok[s] = a.chunk_start + take;
+        skey[s] = cached ? cache[filled + take] : float_key(cs[take]);
+        slot_of[r] = s;
+      }
+      r0 += __popc(bal);
     }
   }
   __syncthreads();
-  // copy the entering tokens' K and V rows into their slots (16-byte vectors)
-  for (int e = tid; e < n_in * d16; e += kThreads) {
-    const int r = e / d16, c = e % d16;
-    const int s = -1 - incoming[r];
-    if (s < 0) continue;  // (cannot happen: every entering token found a slot)
-    const int i = stok[s] - a.chunk_start;
-    const int32_t page = a.pt_ids[base + s / a.P];
-    if (page < 0 || (int64_t)page >= a.pool_pages) {
-      report(a.status, TG_STATUS_BAD_PAGE);
-      continue;
+  // copy the entering tokens' K and V rows into their slots (16-byte vectors); the page id and
+  // the K/V vectors of kCopyUnroll elements are loaded before any is stored
+  const int n_vec = min(n_in, n) * d16;  // (every entering position found a slot: n_in <= freed)
+  for (int e0 = tid; e0 < n_vec; e0 += kCopyUnroll * kThreads) {
+    uint4 kv[kCopyUnroll][2];
+    int32_t page[kCopyUnroll];
+    int slot[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int e = e0 + u * kThreads;
+      slot[u] = -1;
+      if (e < n_vec) {
+        const int r = e / d16, c = e % d16;
+        slot[u] = slot_of[r];
+        page[u] = __ldcg(a.pt_ids + base + slot[u] / a.P);
+        const size_t src = ((size_t)row * a.C + incoming[r]) * a.d + (size_t)c * 8;
+        kv[u][0] = __ldcs(reinterpret_cast<const uint4 *>(a.K + src));
+        kv[u][1] = __ldcs(reinterpret_cast<const uint4 *>(a.V + src));
+      }
     }
-    const size_t dst = ((((size_t)page * a.H_p + hpos) * 2) * a.P + (s % a.P)) * a.d + (size_t)c * 8;
-    const size_t src = ((size_t)row * a.C + i) * a.d + (size_t)c * 8;
-    *reinterpret_cast<uint4 *>(a.pool + dst) = *reinterpret_cast<const uint4 *>(a.K + src);
-    *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = *reinterpret_cast<const uint4 *>(a.V + src);
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      if (slot[u] < 0) continue;
+      if (page[u] < 0 || (int64_t)page[u] >= a.pool_pages) {
+        report(a.status, TG_STATUS_BAD_PAGE);
+        continue;
+      }
+      const int c = (e0 + u * kThreads) % d16;
+      const size_t dst = ((((size_t)page[u] * a.H_p + hpos) * 2) * a.P + (slot[u] % a.P)) * a.d + (size_t)c * 8;
+      *reinterpret_cast<uint4 *>(a.pool + dst) = kv[u][0];
+      *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = kv[u][1];
+    }
   }
 }
 

@@ -70,6 +70,13 @@ def test_chunked_compaction_short_and_empty_requests(lib, cuda):
     _check(lib, w, cuda, 128, N=N)
 
 
+def test_chunked_compaction_beyond_key_cache(lib, cuda):
+    """Heads whose retained slots plus one chunk exceed the kernel's shared-memory key cache
+    (40960 keys): the selects read the keys from global memory instead."""
+    w = synth.small(batch=1, N=60000, L=1, H=2, H_q=4, H_p=1, budget_args=(0.7, 0.9))
+    _check(lib, w, cuda, 4096, N=np.array([60000]))
+
+
 def test_decode_after_chunked_compaction(lib, cuda):
     """Decode over chunk-compacted pages: the token order over the slots differs from the
     one-shot compaction, the attention does not (within the oracle tolerance)."""
