@@ -10,7 +10,7 @@
 // the prompt length).  After each chunk the slots hold the best n tokens seen
 // so far, by (score descending, token ascending); since a token's score is
 // fixed once its chunk is computed, after the last chunk they hold exactly
-// Top(n, s).  One CTA per (request, KV head) row and chunk:
+// Top(n, s).  Per (request, KV head) row and chunk, the row's first CTA:
 //  * while the slots are not full, the chunk's tokens are appended in order;
 //  * otherwise the current slots and the chunk's tokens are ranked together by
 //    a radix select on the score key and, only when the n-th score is tied
@@ -35,6 +35,7 @@ constexpr int kThreads = 1024;
 constexpr int kMaxChunk = 8192;        // tokens per chunk (entering-token list in shared memory)
 constexpr int kSmemKeys = 40960;       // candidates whose score keys are cached in shared memory (160 KB)
 constexpr int kCopyUnroll = 4;         // 16-byte K/V vectors each thread has in flight while copying
+constexpr int kRowCtas = 4;            // CTAs per row: the first ranks; the others help copy a filling row
 
 constexpr int kWarps = kThreads / 32;
 
@@ -149,12 +150,18 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   int *const incoming = work, *const slot_of = work + kMaxChunk;
   __shared__ int err_flag;
 
-  const int row = blockIdx.x, b = row / a.H, h = row % a.H, tid = threadIdx.x;
+  // CTA part 0 of a row ranks and copies; parts 1.. copy their share of a row whose slots are
+  // still filling (its chunk position i goes to slot filled + i, known without ranking), so
+  // such a row's copy is not carried by one SM.  For the other rows they return at once.
+  // (all rows' part 0 first, so every ranking CTA starts at once; the helpers fill the rest)
+  const int n_rows = gridDim.x / kRowCtas;
+  const int row = (int)(blockIdx.x % n_rows), part = (int)(blockIdx.x / n_rows);
+  const int b = row / a.H, h = row % a.H, tid = threadIdx.x;
   const int Nb = a.N[b], n = a.ntok[row];
   if (tid == 0) err_flag = 0;
   __syncthreads();
   if (Nb < 0 || n < 0 || n > Nb || n > a.nmax) {
-    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    if (tid == 0 && part == 0) report(a.status, TG_STATUS_BAD_INPUT);
     return;
   }
   const int len = max(0, min(a.C, Nb - a.chunk_start));
@@ -163,14 +170,14 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   for (int i = 0; i < a.H; ++i)
     if (a.head_order[i] == h) pos = i;
   if (pos < 0) {
-    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    if (tid == 0 && part == 0) report(a.status, TG_STATUS_BAD_INPUT);
     return;
   }
   const int grp = pos / a.H_p, hpos = pos % a.H_p;
   const int64_t base = a.pt_off[b * a.G + grp];
   const int64_t npages = a.pt_off[b * a.G + grp + 1] - base;
   if ((int64_t)(n + a.P - 1) / a.P > npages) {
-    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    if (tid == 0 && part == 0) report(a.status, TG_STATUS_BAD_INPUT);
     return;
   }
   const int filled = min(n, min(Nb, a.chunk_start));  // slots holding a token before this chunk
@@ -178,6 +185,45 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   uint32_t *skey = a.slot_key + (size_t)row * a.nmax;
   const float *cs = a.scores + (size_t)row * a.C;
   const int d16 = a.d / 8;
+
+  // candidates: i < filled is slot i (its token and key), i >= filled is chunk position i - filled
+  const int m = filled + len;
+  const bool append = m <= n;  // the slots are not full yet: every chunk token enters
+  // this CTA's share of the chunk positions of a filling row
+  const int share_lo = (int)((int64_t)part * len / kRowCtas), share_hi = (int)((int64_t)(part + 1) * len / kRowCtas);
+  if (part > 0) {
+    if (!append) return;
+    const int nv = (share_hi - share_lo) * d16;
+    for (int e0 = tid; e0 < nv; e0 += kCopyUnroll * kThreads) {
+      uint4 kv[kCopyUnroll][2];
+      int32_t page[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int e = e0 + u * kThreads;
+        page[u] = -2;
+        if (e < nv) {
+          const int i = share_lo + e / d16, c = e % d16;
+          page[u] = __ldcg(a.pt_ids + base + (filled + i) / a.P);
+          const size_t src = ((size_t)row * a.C + i) * a.d + (size_t)c * 8;
+          kv[u][0] = __ldcs(reinterpret_cast<const uint4 *>(a.K + src));
+          kv[u][1] = __ldcs(reinterpret_cast<const uint4 *>(a.V + src));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        if (page[u] == -2) continue;
+        if (page[u] < 0 || (int64_t)page[u] >= a.pool_pages) {
+          report(a.status, TG_STATUS_BAD_PAGE);
+          continue;
+        }
+        const int e = e0 + u * kThreads, s = filled + share_lo + e / d16, c = e % d16;
+        const size_t dst = ((((size_t)page[u] * a.H_p + hpos) * 2) * a.P + (s % a.P)) * a.d + (size_t)c * 8;
+        *reinterpret_cast<uint4 *>(a.pool + dst) = kv[u][0];
+        *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = kv[u][1];
+      }
+    }
+    return;
+  }
 
   // the first chunk zeroes the rows of the head's last page past n (decode reads whole tiles)
   if (a.chunk_start == 0 && n % a.P) {
@@ -191,9 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
       }
   }
 
-  // candidates: i < filled is slot i (its token and key), i >= filled is chunk position i - filled
-  const int m = filled + len;
-  const bool append = m <= n;  // the slots are not full yet: every chunk token enters
   const bool cached = !append && m <= kSmemKeys;
   bool nan_seen = false;
   if (cached) {
@@ -301,7 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   __syncthreads();
   // copy the entering tokens' K and V rows into their slots (16-byte vectors); the page id and
   // the K/V vectors of kCopyUnroll elements are loaded before any is stored
-  const int n_vec = min(n_in, n) * d16;  // (every entering position found a slot: n_in <= freed)
+  // (every entering position found a slot: n_in <= freed); of a filling row, only this CTA's share
+  const int n_vec = (append ? share_hi : min(n_in, n)) * d16;
   for (int e0 = tid; e0 < n_vec; e0 += kCopyUnroll * kThreads) {
     uint4 kv[kCopyUnroll][2];
     int32_t page[kCopyUnroll];
@@ -360,8 +404,8 @@ extern "C" int tg_compact_chunk(tg_stream_t stream, int batch, int H, int H_p, i
   cudaError_t e = cudaFuncSetAttribute(compact_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess) {
     const int64_t rows = (int64_t)batch * H;
-    if (rows > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_chunk: grid too large");
-    compact_chunk_kernel<<<(unsigned)rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    if (rows * kRowCtas > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_chunk: grid too large");
+    compact_chunk_kernel<<<(unsigned)(rows * kRowCtas), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_chunk: %s", cudaGetErrorString(e));
