@@ -15,9 +15,10 @@
 //  * otherwise the current slots and the chunk's tokens are ranked together by
 //    a radix select on the score key and, only when the n-th score is tied
 //    across the cut, one on ~token among the keys equal to it -- a total
-//    order, so exactly n survive.  The slots whose token
-//    dropped out are reused, the lowest freed slot by the lowest entering token,
-//    and only the entering tokens' K/V rows are written into the pages.
+//    order, so exactly n survive.  The slots whose token dropped out are
+//    reused, the lowest freed slot by the lowest entering token;
+//  * only the entering tokens' K/V rows are written into the pages.  A row
+//    whose slots are still filling shares that copy with three more CTAs.
 // Slot k lives at page k / P, row k % P of the head's block in its group page,
 // as in the one-shot compaction; only the order of tokens over the slots
 // differs (attention does not depend on it).
