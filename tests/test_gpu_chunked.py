@@ -70,6 +70,15 @@ def test_chunked_compaction_short_and_empty_requests(lib, cuda):
     _check(lib, w, cuda, 128, N=N)
 
 
+def test_chunked_compaction_head_dim_256(lib, cuda):
+    """d = 256 (two 16-byte vectors per lane for each K or V row), with chunks that are not
+    a multiple of 32 tokens and heads whose slots fill over several chunks."""
+    w = synth.small(batch=2, N=900, L=1, d=256, H_q=8, H=4, budget_args=(0.3, 1.0))
+    N = np.array([900, 641])
+    _check(lib, w, cuda, 96, N=N)
+    _check(lib, w, cuda, 250, N=N)
+
+
 def test_chunked_compaction_beyond_key_cache(lib, cuda):
     """Heads whose retained slots plus one chunk exceed the kernel's shared-memory key cache
     (40960 keys): the selects read the keys from global memory instead."""
