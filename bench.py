@@ -273,7 +273,7 @@ def chunked_compaction(w, cache, device, oneshot_ms, C=2048, layers=2):
     Nmax = int(synth.contexts(w).max())
     if Nmax < 2 * C:
         return None
-    res = []
+    res, res_eager = [], []
     for layer in range(min(layers, w.L)):
         s = synth.scores(w, layer, device)
         K, V = synth.keys_values(w, layer, device)
@@ -293,7 +293,23 @@ def chunked_compaction(w, cache, device, oneshot_ms, C=2048, layers=2):
         cache.compact_layer_chunked(layer, s, K, V, C, chunks=iter(chunks))
         e1.record()
         torch.cuda.synchronize()
+        res_eager.append(e0.elapsed_time(e1))
+        # the same calls captured in a CUDA graph and replayed: the device time without the
+        # host's per-call submission (a prefill issues them between its own kernels)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            cache.compact_layer_chunked(layer, s, K, V, C, chunks=iter(chunks), stream=side)
+        with torch.cuda.stream(side):
+            graph.replay()
+            torch.cuda.synchronize()
+            e0.record(side)
+            graph.replay()
+            e1.record(side)
+        torch.cuda.synchronize()
         res.append(e0.elapsed_time(e1))
+        del graph
         cache.compact_layer(layer, s, K, V)
         del s, K, V, chunks
     torch.cuda.synchronize()
@@ -301,7 +317,9 @@ def chunked_compaction(w, cache, device, oneshot_ms, C=2048, layers=2):
     n_chunks = -(-Nmax // C)
     return {"chunk_tokens": C, "chunks_per_layer": n_chunks, "ms_per_layer": statistics.mean(res),
             "us_per_chunk": 1e3 * statistics.mean(res) / n_chunks,
+            "us_per_chunk_eager": 1e3 * statistics.mean(res_eager) / n_chunks,
             "vs_one_shot": statistics.mean(res) / statistics.mean(oneshot_ms[:len(res)]),
+            "timing": "CUDA-graph replay of the layer's chunk calls (eager: Python launches)",
             "layers_timed": len(res)}
 
 

@@ -263,12 +263,24 @@ int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d,
  *   (this chunk); head_order, ntok, pt_off, pt_ids, pool as tg_compact_topk;
  *   slot_tok int32 and slot_key uint32 [batch][H][nmax] (state, nmax >= every
  *   n; slot_tok[..][k] = the token in slot k).  C <= 8192; the first chunk also
- *   zeroes the rows of each head's last page past n. */
+ *   zeroes the rows of each head's last page past n.
+ *   workspace: device scratch of at least tg_compact_chunk_workspace(batch, H, C)
+ *   bytes, 16-byte aligned, no initial contents; one per stream (a call overwrites it).
+ * Launch: a ranking kernel (one CTA per head) writes the slots and, for each head
+ *   whose slots are full, its list of (slot, chunk position) entries; a copy kernel
+ *   spread over the GPU (programmatic dependent launch) copies the entering K/V
+ *   rows.  It copies the heads whose slots are still filling (chunk position i to
+ *   slot filled + i) before it waits for the ranking kernel. */
 int tg_compact_chunk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int chunk_start, int C,
                      const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
                      const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
                      const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool, int32_t *slot_tok,
-                     uint32_t *slot_key, int nmax, int32_t *dev_status);
+                     uint32_t *slot_key, int nmax, void *workspace, int64_t workspace_bytes,
+                     int32_t *dev_status);
+
+/* tg_compact_chunk_workspace -- bytes of workspace tg_compact_chunk needs for
+ *   batch * H heads and chunks of C tokens (host; TG_ERR_INVALID_ARG on bad sizes). */
+int tg_compact_chunk_workspace(int batch, int H, int C, int64_t *workspace_bytes);
 
 /* ------------------------------------------------------------------ a9 ---
  * tg_build_minmax -- per-page elementwise min and max of the keys (the MinMax

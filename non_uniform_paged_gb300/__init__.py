@@ -22,7 +22,7 @@ __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
-           "tg_sparse_layer", "tg_compact_chunk", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
+           "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
 
@@ -53,7 +53,8 @@ _SIGS = {
     "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
     "tg_sparse_layer": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _L, _I, _P, _L, _P, _F, _P, _L, _P, _P, _P]),
     "tg_compact_chunk": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P, _I,
-                              _P]),
+                              _P, _L, _P]),
+    "tg_compact_chunk_workspace": (_I, [_I, _I, _I, _P]),
     "tg_tier_promote": (_I, [_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _L, _P, _P, _P]),
     "tg_alloc_state_bytes": (_I, [_L, _P]),
     "tg_alloc_init": (_I, [_P, _L, _L]),
@@ -280,10 +281,19 @@ def tg_sparse_layer(plan_host, plan_dev, n_pages, K, q, minmax, sel, pt_ids, sco
                                   _dev(dev_status, torch.int32, "dev_status")))
 
 
+def tg_compact_chunk_workspace(batch: int, H: int, C: int) -> int:
+    """Bytes of workspace tg_compact_chunk needs (tg.h: tg_compact_chunk_workspace)."""
+    lib = load()
+    n = ctypes.c_int64(0)
+    _check(lib.tg_compact_chunk_workspace(int(batch), int(H), int(C), ctypes.addressof(n)))
+    return n.value
+
+
 def tg_compact_chunk(batch, H, H_p, P, d, chunk_start, C, N, scores, K, V, head_order, ntok, pt_off, pt_ids,
-                     pool_pages, pool, slot_tok, slot_key, dev_status=None, stream=None):
+                     pool_pages, pool, slot_tok, slot_key, workspace, dev_status=None, stream=None):
     """One prefill chunk of retention + compaction (tg.h: tg_compact_chunk); slot_tok and
-    slot_key [batch][H][nmax] carry the state from chunk to chunk."""
+    slot_key [batch][H][nmax] carry the state from chunk to chunk; workspace is a device
+    uint8 tensor of tg_compact_chunk_workspace(batch, H, C) bytes."""
     import torch
     lib = load()
     _check(lib.tg_compact_chunk(_stream(stream), batch, H, H_p, P, d, int(chunk_start), int(C),
@@ -293,7 +303,8 @@ def tg_compact_chunk(batch, H, H_p, P, d, chunk_start, C, N, scores, K, V, head_
                                 _dev(pt_off, torch.int64, "pt_off"), _dev(pt_ids, torch.int32, "pt_ids"),
                                 int(pool_pages), _dev(pool, torch.bfloat16, "pool"),
                                 _dev(slot_tok, torch.int32, "slot_tok"), _dev(slot_key, None, "slot_key"),
-                                int(slot_tok.shape[-1]), _dev(dev_status, torch.int32, "dev_status")))
+                                int(slot_tok.shape[-1]), _dev(workspace, torch.uint8, "workspace"),
+                                int(workspace.numel()), _dev(dev_status, torch.int32, "dev_status")))
 
 
 def tg_build_minmax(batch, H, N, P, d, K, minmax, dev_status=None, stream=None):

@@ -24,7 +24,8 @@ import torch
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
                tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
                tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
-               SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk, tg_sparse_layer)
+               SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk, tg_compact_chunk_workspace,
+               tg_sparse_layer)
 
 BYTES_BF16 = 2
 
@@ -118,6 +119,7 @@ class RaggedCache:
         nmax = max(1, int(ntok.max()))
         slot_tok = torch.full((self.batch, self.H, nmax), -1, dtype=torch.int32, device=self.device)
         slot_key = torch.zeros((self.batch, self.H, nmax), dtype=torch.int32, device=self.device)
+        ws = torch.empty(tg_compact_chunk_workspace(self.batch, self.H, C), dtype=torch.uint8, device=self.device)
         Nmax = scores.shape[-1]
         for start in range(0, Nmax, C):
             if chunks is not None:
@@ -132,7 +134,7 @@ class RaggedCache:
                 vc[:, :, :end - start] = V[:, :, start:end]
             tg_compact_chunk(self.batch, self.H, self.H_p, self.P, self.d, start, C, self.N_dev, sc, kc, vc,
                              self.order_dev[layer], self.ntok_dev[layer], self.list_offsets(layer),
-                             self.pt_ids_dev, self.n_pages, self.pool, slot_tok, slot_key,
+                             self.pt_ids_dev, self.n_pages, self.pool, slot_tok, slot_key, ws,
                              dev_status=self.status, stream=stream)
         return slot_tok
 
