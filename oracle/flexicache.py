@@ -10,7 +10,7 @@ Efficient KV Cache Management (MLSys 2026)" (paper-review page):
   the GPU, decoupled from the KV pages;
 * "System engineering / Block Allocator": one block table per (head, layer).
 
-Readings (also listed in the design doc):
+Readings:
 
 * the min/max vectors are elementwise over the valid keys of a page, in the
   keys' own bf16 values (exact);

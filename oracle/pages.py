@@ -13,7 +13,7 @@ Multi-turn LLM Serving" (paper-review page):
 * 5.5 / 5.8 -- H_p trades fragmentation against management overhead at 25/50/
   75% eviction, and budget-aware clustering raises the memory reclaimed.
 
-Readings (also listed in the design doc):
+Readings:
 
 * allocated elements of (l, b, group g) = ceil(max_{h in g} n / P) * H_p * 2 * P * d;
   monolithic = ceil(max_h n / P) * H * 2 * P * d per (l, b);

@@ -13,7 +13,7 @@ architecture"):
   to its aggregate budget Phi_{l,i}; the result is the static Workload Split
   Map S in N^{L x (H/H_p)}.
 
-Readings of points the page leaves open (each also listed in the design doc):
+Readings of points the page leaves open:
 
 * B = min(1, fp32(alpha * B^)); n = ceil(B * N) of the stored float32 B,
   computed exactly (rational arithmetic), clamped to [1, N] (0 when N = 0).
