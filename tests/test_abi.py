@@ -43,3 +43,21 @@ def test_version_and_error_string(lib):
 def test_struct_sizes_match_header(lib):
     assert lib.WORK_ITEM_DTYPE.itemsize == 48
     assert lib._HEADER_DTYPE.itemsize == 80
+
+
+def test_compact_chunk_workspace_size_and_short_workspace_refused(lib):
+    """tg_compact_chunk_workspace: 8 bytes of (slot, chunk position) per head and chunk token,
+    then a count per head (256-byte aligned sections).  A workspace one byte short is refused
+    on the host, before anything is launched (the pointers below are never dereferenced)."""
+    batch, H, C = 3, 8, 100
+    need = lib.tg_compact_chunk_workspace(batch, H, C)
+    rows = batch * H
+    assert need == -(-(-(-rows * C * 8 // 256) * 256 + rows * 4) // 256) * 256
+    so = lib.load()
+    fake = ctypes.c_void_p(4096)  # 16-byte aligned, never read: the size check comes first
+    rc = so.tg_compact_chunk(None, batch, H, 2, 16, 128, 0, C, fake, fake, fake, fake, fake, fake, fake, fake,
+                             1, fake, fake, fake, 64, fake, need - 1, None)
+    assert rc == -4  # TG_ERR_CAPACITY
+    assert b"workspace" in so.tg_last_error_string()
+    with pytest.raises(lib.TGError):
+        lib.tg_compact_chunk_workspace(batch, 0, C)
