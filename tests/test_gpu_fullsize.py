@@ -139,3 +139,44 @@ def test_config4_fullsize_layer(lib, cuda, K_sel):
         ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], Kt[b, h][tok].float().cpu().numpy(),
                                                      Vt[b, h][tok].float().cpu().numpy(), 1.0 / math.sqrt(w.d))
     print(compare_out(out, lse, ref_out, ref_lse, rows=pairs))
+
+
+def test_config2_fullsize_chunked_compaction(lib, cuda):
+    """Chunked-prefill compaction at config 2's full size (32K-token prompts, chunks of 2048,
+    both launches in the configuration bench.py times): the slot tokens of sampled
+    (request, KV head) rows in the oracle's slot order, and their K/V rows in the pool,
+    bit-exact.  The sample includes the head with the largest budget (slots filling over
+    many chunks: copied before the ranking launch completes) and ranking heads."""
+    from non_uniform_paged_gb300.ragged import RaggedCache
+    w = synth.workload(2)
+    layer, C = 0, 2048
+    N = synth.contexts(w)
+    Bhat = synth.budgets_hat(w)[layer:layer + 1]
+    cache = RaggedCache(1, w.batch, w.H, w.H_q, w.d, w.P, w.H_p, w.alpha, Bhat, N, cluster=w.cluster,
+                        n_cta=w.n_cta, device=cuda)
+    s = synth.scores(w, layer, cuda)
+    K, V = synth.keys_values(w, layer, cuda)
+    slot_tok = cache.compact_layer_chunked(0, s, K, V, C)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(cache.status) == 0
+    ntok = cache.pages["ntok"][0]
+    order = list(cache.pages["order"][0])
+    pt_off, pt_ids = cache.pages["pt_off"], cache.pages["pt_ids"]
+    r = np.random.default_rng(7)
+    h_big = int(np.argmax(ntok[0]))
+    rows = [(0, h_big)] + [(int(b), int(h)) for b, h in zip(r.integers(0, w.batch, 5), r.integers(0, w.H, 5))]
+    pool = cache.pool.view(-1, w.d)
+    st = slot_tok.cpu().numpy()
+    for b, h in rows:
+        n = int(ntok[b, h])
+        ref = otg.compact_chunked(s[b, h, :N[b]].cpu().numpy(), n, C)
+        assert st[b, h, :n].tolist() == ref, (b, h)
+        pos = order.index(h)
+        g, j = pos // w.H_p, pos % w.H_p
+        base = pt_off[b * w.G + g]
+        k = np.arange(n)
+        page = pt_ids[base + k // w.P].astype(np.int64)
+        rk = torch.from_numpy((page * w.H_p + j) * 2 * w.P + k % w.P).to(cuda)
+        idx_t = torch.from_numpy(np.asarray(ref, dtype=np.int64)).to(cuda)
+        assert torch.equal(pool[rk].view(torch.int16).cpu(), K[b, h][idx_t].view(torch.int16).cpu()), (b, h)
+        assert torch.equal(pool[rk + w.P].view(torch.int16).cpu(), V[b, h][idx_t].view(torch.int16).cpu()), (b, h)
