@@ -69,9 +69,13 @@ __device__ void select_kth(int count, int k, GetKey get, uint32_t *list, int cap
         const uint32_t key = n_list < 0 ? get(i) : list[i];
         if ((key & mask) == prefix) dg = (key >> shift) & 255u;
       }
-      // lanes of a warp with the same digit add once
-      const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-      if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      if (shift == 24) {
+        // the leading digits of real scores coincide: lanes of a warp with the same digit add once
+        const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+        if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      } else if (dg < 256u) {
+        atomicAdd(&hist[dg], 1);  // later digits are spread out: grouping equal ones costs more
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -172,20 +176,6 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   }
   const int len = max(0, min(a.C, Nb - a.chunk_start));
   if (n == 0 || len == 0) return;
-  int pos = -1;
-  for (int i = 0; i < a.H; ++i)
-    if (a.head_order[i] == h) pos = i;
-  if (pos < 0) {
-    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
-    return;
-  }
-  const int grp = pos / a.H_p, hpos = pos % a.H_p;
-  const int64_t base = a.pt_off[b * a.G + grp];
-  const int64_t npages = a.pt_off[b * a.G + grp + 1] - base;
-  if ((int64_t)(n + a.P - 1) / a.P > npages) {
-    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
-    return;
-  }
   const int filled = min(n, min(Nb, a.chunk_start));  // slots holding a token before this chunk
   int32_t *stok = a.slot_tok + (size_t)row * a.nmax;
   uint32_t *skey = a.slot_key + (size_t)row * a.nmax;
@@ -195,18 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   // candidates: i < filled is slot i (its token and key), i >= filled is chunk position i - filled
   const int m = filled + len;
   const bool append = m <= n;  // the slots are not full yet: every chunk token enters
-
-  // the first chunk zeroes the rows of the head's last page past n (decode reads whole tiles)
-  if (a.chunk_start == 0 && n % a.P) {
-    const int rem = n % a.P, rows = a.P - rem;
-    const int32_t page = a.pt_ids[base + (n - 1) / a.P];
-    if (page >= 0 && (int64_t)page < a.pool_pages)
-      for (int e = tid; e < 2 * rows * d16; e += kThreads) {
-        const int kv = e / (rows * d16), r = (e / d16) % rows, c = e % d16;
-        const size_t dst = ((((size_t)page * a.H_p + hpos) * 2 + kv) * a.P + rem + r) * a.d + (size_t)c * 8;
-        *reinterpret_cast<uint4 *>(a.pool + dst) = make_uint4(0, 0, 0, 0);
-      }
-  }
 
   const bool cached = !append && m <= kSmemKeys;
   bool nan_seen = false;
@@ -229,6 +207,34 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
     nan_seen |= is_nan(f);
     if (cached) cache[filled + i] = float_key(f);
   }
+  // the head's group page list (checked while the loads above are in flight; nothing has
+  // been written yet)
+  int pos = -1;
+  for (int i = 0; i < a.H; ++i)
+    if (a.head_order[i] == h) pos = i;
+  if (pos < 0) {
+    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    return;
+  }
+  const int grp = pos / a.H_p, hpos = pos % a.H_p;
+  const int64_t base = a.pt_off[b * a.G + grp];
+  const int64_t npages = a.pt_off[b * a.G + grp + 1] - base;
+  if ((int64_t)(n + a.P - 1) / a.P > npages) {
+    if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    return;
+  }
+  // the first chunk zeroes the rows of the head's last page past n (decode reads whole tiles)
+  if (a.chunk_start == 0 && n % a.P) {
+    const int rem = n % a.P, rows = a.P - rem;
+    const int32_t page = a.pt_ids[base + (n - 1) / a.P];
+    if (page >= 0 && (int64_t)page < a.pool_pages)
+      for (int e = tid; e < 2 * rows * d16; e += kThreads) {
+        const int kv = e / (rows * d16), r = (e / d16) % rows, c = e % d16;
+        const size_t dst = ((((size_t)page * a.H_p + hpos) * 2 + kv) * a.P + rem + r) * a.d + (size_t)c * 8;
+        *reinterpret_cast<uint4 *>(a.pool + dst) = make_uint4(0, 0, 0, 0);
+      }
+  }
+
   if (nan_seen) err_flag = 1;
   __syncthreads();
   if (err_flag && tid == 0) report(a.status, TG_STATUS_NONFINITE);
