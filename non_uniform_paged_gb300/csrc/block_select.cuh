@@ -48,8 +48,10 @@ __device__ __forceinline__ void block_radix_select(int count, int k, GetKey get,
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
-    // histogram of the next digit among keys that match the prefix so far; lanes of a
-    // warp with the same digit add once (the leading digits of real scores coincide)
+    // histogram of the next digit among keys that match the prefix so far.  In the first
+    // pass the leading digits of real scores coincide, and lanes of a warp with the same
+    // digit add once; later digits are spread out, where that grouping costs more than
+    // the atomics it saves
     for (int base = 0; base < count; base += NT) {
       const int i = base + threadIdx.x;
       uint32_t dg = 256u;  // no digit
@@ -57,8 +59,12 @@ __device__ __forceinline__ void block_radix_select(int count, int k, GetKey get,
         const uint32_t key = get(i);
         if ((key & mask) == prefix) dg = (key >> shift) & 255u;
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-      if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      if (shift == 24) {
+        const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+        if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      } else if (dg < 256u) {
+        atomicAdd(&hist[dg], 1);
+      }
     }
     __syncthreads();
     if (warp == 0) {
