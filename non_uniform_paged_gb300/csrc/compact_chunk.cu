@@ -46,96 +46,6 @@ constexpr int kCopyTokens = 4;         // tokens a warp copies at once (their K/
 
 constexpr int kWarps = kThreads / 32;
 
-// Key T of the k-th largest of `count` keys (1 <= k <= count), the number of keys equal to T that
-// a top-k takes (need_eq = k - #{key > T}) and the number of keys equal to T (n_eq).  MSB-first
-// radix select over 8-bit digits.  After the first pass the keys that share the chosen top digit
-// are copied into `list` when at most `cap` of them do, and the remaining passes read only those
-// (the first digit of real scores already narrows the candidates to a few percent).  `hist` is
-// 256 ints and `scratch` 4 ints of shared memory.
-template <typename GetKey>
-__device__ void select_kth(int count, int k, GetKey get, uint32_t *list, int cap, int *hist, int *scratch,
-                           uint32_t &T, int &need_eq, int &n_eq) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int k_rem = k, n_list = -1, sel_count = count;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    const int cnt = n_list < 0 ? count : n_list;
-    for (int base = 0; base < cnt; base += kThreads) {
-      const int i = base + tid;
-      uint32_t dg = 256u;  // no digit
-      if (i < cnt) {
-        const uint32_t key = n_list < 0 ? get(i) : list[i];
-        if ((key & mask) == prefix) dg = (key >> shift) & 255u;
-      }
-      if (shift == 24) {
-        // the leading digits of real scores coincide: lanes of a warp with the same digit add once
-        const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-        if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
-      } else if (dg < 256u) {
-        atomicAdd(&hist[dg], 1);  // later digits are spread out: grouping equal ones costs more
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down
-      int local[8];
-      int sum = 0;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        local[t] = hist[255 - 8 * lane - t];
-        sum += local[t];
-      }
-      int inc = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-      }
-      const int before = inc - sum;  // keys in digits above this lane's block
-      if (before < k_rem && k_rem <= inc) {
-        int above = before;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (above + local[t] >= k_rem) {
-            scratch[0] = 255 - 8 * lane - t;
-            scratch[1] = above;
-            scratch[2] = local[t];
-            break;
-          }
-          above += local[t];
-        }
-      }
-      if (lane == 0) scratch[3] = 0;
-    }
-    __syncthreads();
-    const uint32_t digit = (uint32_t)scratch[0];
-    k_rem -= scratch[1];
-    sel_count = scratch[2];
-    prefix |= digit << shift;
-    mask |= 255u << shift;
-    if (n_list < 0 && shift > 0 && sel_count <= cap) {
-      // copy the keys under the new prefix into the list (order does not matter for counts)
-      for (int base = 0; base < count; base += kThreads) {
-        const int i = base + tid;
-        uint32_t key = 0;
-        const bool keep = i < count && ((key = get(i)) & mask) == prefix;
-        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-        int at = 0;
-        if (lane == 0 && bal) at = atomicAdd(&scratch[3], __popc(bal));
-        at = __shfl_sync(0xffffffffu, at, 0);
-        if (keep) list[at + __popc(bal & ((1u << lane) - 1u))] = key;
-      }
-      n_list = sel_count;
-    }
-    __syncthreads();
-  }
-  T = prefix;
-  need_eq = k_rem;
-  n_eq = sel_count;
-}
-
 struct ChunkArgs {
   const int32_t *N;
   const float *scores;                 // [batch][H][C]
@@ -249,13 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   if (!append) {
     uint32_t *const list = reinterpret_cast<uint32_t *>(work);
     int need_hi, n_eq;
-    select_kth(m, n, hi_of, list, 2 * kMaxChunk, hist, sel_scratch, T_hi, need_hi, n_eq);
+    block_select_kth<kThreads>(m, n, hi_of, list, 2 * kMaxChunk, hist, sel_scratch, T_hi, need_hi, n_eq);
     // among the keys equal to T_hi, the need_hi lowest tokens (largest ~token) survive; with no
     // tie across the cut every one of them does, and T_lo = 0 keeps them all
     if (n_eq > need_hi) {
       int unused0, unused1;
-      select_kth(m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; }, list,
-                 2 * kMaxChunk, hist, sel_scratch, T_lo, unused0, unused1);
+      block_select_kth<kThreads>(m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; },
+                                 list, 2 * kMaxChunk, hist, sel_scratch, T_lo, unused0, unused1);
     }
   }
   auto survives = [&](int i) {

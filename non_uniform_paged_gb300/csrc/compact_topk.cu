@@ -50,7 +50,7 @@ struct CompactArgs {
 };
 
 __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const CompactArgs a) {
-  extern __shared__ uint32_t cache[];  // kSmemKeys keys when the row fits, else unused
+  extern __shared__ uint32_t cache[];  // the row's keys when they fit, else the select's candidate list
   __shared__ int hist[256];
   __shared__ int scan[33];
   __shared__ int sel_scratch[4];
@@ -100,19 +100,50 @@ __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const Compact
   auto key_of = [&](int t) -> uint32_t { return cached ? cache[t] : float_key(srow[t]); };
 
   uint32_t T;
-  int need_eq;
-  block_radix_select<kThreads>(Nb, n, key_of, hist, sel_scratch, T, need_eq);
+  int need_eq, n_eq;
+  // keys read from global memory: once the first digit is chosen, the unused key cache holds
+  // the candidates left, and the remaining passes read only those
+  block_select_kth<kThreads>(Nb, n, key_of, cached ? nullptr : cache, cached ? 0 : kSmemKeys, hist, sel_scratch, T,
+                             need_eq, n_eq);
 
   const int d16 = a.d / 8;  // 16-byte chunks per row
   const size_t src_row0 = (size_t)row * a.Nmax;
   const int c_begin = (int)((int64_t)part * Nb / a.parts), c_end = (int)((int64_t)(part + 1) * Nb / a.parts);
   // keys kept before this chunk: all of them above T, and the first need_eq equal to T
+  // (per-thread counts, four keys in flight, then one block sum)
   int gt_before = 0, eq_before = 0;
-  for (int c0 = 0; c0 < c_begin; c0 += kThreads) {
-    const int t = c0 + threadIdx.x;
-    const uint32_t key = t < c_begin ? key_of(t) : 0u;
-    gt_before += __syncthreads_count(t < c_begin && key > T);
-    eq_before += __syncthreads_count(t < c_begin && key == T);
+  {
+    int gl = 0, el = 0;
+    for (int c0 = 0; c0 < c_begin; c0 += 4 * kThreads) {
+      uint32_t kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = c0 + u * kThreads + threadIdx.x;
+        kk[u] = t < c_begin ? key_of(t) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + u * kThreads + (int)threadIdx.x < c_begin) {
+          gl += kk[u] > T;
+          el += kk[u] == T;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gl += __shfl_xor_sync(0xffffffffu, gl, o);
+      el += __shfl_xor_sync(0xffffffffu, el, o);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+      scan[warp] = gl;
+      hist[warp] = el;
+    }
+    __syncthreads();
+    for (int w = 0; w < kThreads / 32; ++w) {
+      gt_before += scan[w];
+      eq_before += hist[w];
+    }
+    __syncthreads();
   }
   int taken = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
   for (int c0 = c_begin; c0 < c_end && taken < n; c0 += kThreads) {
@@ -181,7 +212,8 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   a.N = N; a.scores = scores; a.K = K; a.V = V; a.head_order = head_order; a.ntok = ntok;
   a.pt_off = pt_off; a.pt_ids = pt_ids; a.pool_pages = pool_pages; a.pool = pool; a.kept_idx = kept_idx;
   a.status = dev_status; a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
-  const int smem = (Nmax <= kSmemKeys ? Nmax : 0) * (int)sizeof(uint32_t);
+  // the keys of a row when they fit, else the select's candidate list (kSmemKeys entries)
+  const int smem = (Nmax <= kSmemKeys ? Nmax : kSmemKeys) * (int)sizeof(uint32_t);
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
