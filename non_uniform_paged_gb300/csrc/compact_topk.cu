@@ -46,8 +46,54 @@ struct CompactArgs {
   int32_t *kept_idx;
   int32_t *status;
   int H, H_p, G, P, d, Nmax;
-  int parts;  // CTAs per row
+  int parts;  // CTAs per row (the even split)
+  int prop;   // share the grid's CTAs among the rows in proportion to their retained tokens
 };
+
+constexpr int kPropRows = 1024;  // rows that the proportional split handles (one per thread)
+constexpr int kMinPart = 2048;   // tokens per CTA at least
+
+// Proportional shares: every row gets one CTA; the others go to the rows in proportion to
+// their retained tokens (a row's CTAs each keep at least kMinPart tokens of its range).  Every
+// CTA derives the same shares from ntok and writes its (row, part, parts) to out[0..2], or
+// out[0] = -1 past the last share.
+__device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int *scan, int *out) {
+  const int rows = (int)(gridDim.x / a.parts), tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int nr = 0, cap = 0;
+  if (tid < rows) {
+    nr = max(0, a.ntok[tid]);
+    cap = max(0, a.N[tid / a.H] / kMinPart - 1);
+  }
+  long long tot = nr;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  long long *wsum = reinterpret_cast<long long *>(hist);  // 32 warp sums (256 bytes)
+  if (lane == 0) wsum[warp] = tot;
+  __syncthreads();
+  tot = 0;
+  for (int w = 0; w < kThreads / 32; ++w) tot += wsum[w];
+  const long long extra_all = (long long)gridDim.x - rows;
+  const int pr = tid < rows ? 1 + (int)min((long long)cap, tot > 0 ? extra_all * nr / tot : 0ll) : 0;
+  // exclusive prefix of the shares: this CTA's row is the one whose range holds blockIdx.x
+  int inc = pr;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) scan[warp] = inc;
+  if (tid == 0) out[0] = -1;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += scan[w];
+  const int first = before + inc - pr;
+  if (tid < rows && (int)blockIdx.x >= first && (int)blockIdx.x < first + pr) {
+    out[0] = tid;
+    out[1] = (int)blockIdx.x - first;
+    out[2] = pr;
+  }
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const CompactArgs a) {
   extern __shared__ uint32_t cache[];  // the row's keys when they fit, else the select's candidate list
@@ -57,7 +103,16 @@ __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const Compact
   __shared__ int tok_list[kThreads];
   __shared__ int err_flag;
 
-  const int row = blockIdx.x / a.parts, part = blockIdx.x % a.parts, b = row / a.H, h = row % a.H;
+  int row = blockIdx.x / a.parts, part = blockIdx.x % a.parts, parts = a.parts;
+  if (a.prop) {
+    prop_share(a, hist, scan, sel_scratch);
+    if (sel_scratch[0] < 0) return;  // past the last share
+    row = sel_scratch[0];
+    part = sel_scratch[1];
+    parts = sel_scratch[2];
+    __syncthreads();  // (hist, scan and sel_scratch are reused below)
+  }
+  const int b = row / a.H, h = row % a.H;
   const int Nb = a.N[b], n = a.ntok[row];
   if (threadIdx.x == 0) err_flag = 0;
   __syncthreads();
@@ -108,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const Compact
 
   const int d16 = a.d / 8;  // 16-byte chunks per row
   const size_t src_row0 = (size_t)row * a.Nmax;
-  const int c_begin = (int)((int64_t)part * Nb / a.parts), c_end = (int)((int64_t)(part + 1) * Nb / a.parts);
+  const int c_begin = (int)((int64_t)part * Nb / parts), c_end = (int)((int64_t)(part + 1) * Nb / parts);
   // keys kept before this chunk: all of them above T, and the first need_eq equal to T
   // (per-thread counts, four keys in flight, then one block sum)
   int gt_before = 0, eq_before = 0;
@@ -179,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const Compact
 
   // zero the rows of the last page past n (K and V blocks)
   const int rem = n % a.P;
-  if (rem && part == a.parts - 1) {
+  if (rem && part == parts - 1) {
     const int32_t page = a.pt_ids[base + (n - 1) / a.P];
     if (page >= 0 && (int64_t)page < a.pool_pages) {
       const int rows = a.P - rem;
@@ -225,6 +280,7 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
     int parts = (2 * sms + rows - 1) / rows;
     parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
     a.parts = parts;
+    a.prop = parts > 1 && rows <= kPropRows;
     const int64_t grid = (int64_t)rows * parts;
     if (grid > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
     compact_topk_kernel<<<(unsigned)grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
