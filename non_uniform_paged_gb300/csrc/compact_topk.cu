@@ -6,11 +6,14 @@
 // ready) and 3.2 Ragged Paging (each H_p-head group writes into its own pages
 // of H_p x 2 x P x d elements).
 //
-// C CTAs per (request, KV head) row (C chosen so the grid fills the GPU); CTA j
-// owns tokens [j N / C, (j+1) N / C) and talks to no other CTA:
+// One 1024-thread CTA per SM; a row (request, KV head) gets C of them (C chosen so
+// the grid fills the GPU, or, for up to 1024 rows, shares in proportion to the
+// rows' retained tokens).  CTA j of a row owns tokens [j N / C, (j+1) N / C) and
+// talks to no other CTA:
 //  1. exact top-n by an MSB-first radix select over order-preserving keys of
 //     the float32 scores (every CTA of the row finds the same n-th largest key
-//     T and how many keys equal to T to keep; the scores stay in L2);
+//     T and how many keys equal to T to keep; the keys sit in shared memory when
+//     the row fits, else in L2);
 //  2. block-wide counts of the kept keys before its chunk give the chunk's
 //     first output position;
 //  3. one ascending sweep of its chunk keeps key > T, plus the lowest-indexed
@@ -32,7 +35,7 @@ namespace {
 using namespace tgk;
 
 constexpr int kThreads = 1024;
-constexpr int kSmemKeys = 24576;  // rows up to this length keep their keys in shared memory (2 CTAs/SM)
+constexpr int kSmemKeys = 49152;  // rows up to this length keep their keys in shared memory (192 KB)
 
 struct CompactArgs {
   const int32_t *N;
@@ -95,7 +98,7 @@ __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const CompactArgs a) {
   extern __shared__ uint32_t cache[];  // the row's keys when they fit, else the select's candidate list
   __shared__ int hist[256];
   __shared__ int scan[33];
@@ -214,18 +217,34 @@ __global__ void __launch_bounds__(kThreads, 2) compact_topk_kernel(const Compact
       if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in] = t;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < sel_total * d16; e += kThreads) {
-      const int r = e / d16, c = e % d16;
-      const int k = taken + r;
-      const int32_t page = a.pt_ids[base + k / a.P];
-      if (page < 0 || (int64_t)page >= a.pool_pages) {
-        report(a.status, TG_STATUS_BAD_PAGE);
-        continue;
+    // four rows' K and V vectors loaded before any is stored
+    for (int e0 = threadIdx.x; e0 < sel_total * d16; e0 += 4 * kThreads) {
+      uint4 kv[4][2];
+      int32_t page[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kThreads;
+        page[u] = -2;
+        if (e < sel_total * d16) {
+          const int r = e / d16, c = e % d16;
+          page[u] = a.pt_ids[base + (taken + r) / a.P];
+          const size_t src = (src_row0 + tok_list[r]) * a.d + (size_t)c * 8;
+          kv[u][0] = *reinterpret_cast<const uint4 *>(a.K + src);
+          kv[u][1] = *reinterpret_cast<const uint4 *>(a.V + src);
+        }
       }
-      const size_t dst = ((((size_t)page * a.H_p + hpos) * 2) * a.P + (k % a.P)) * a.d + (size_t)c * 8;
-      const size_t src = (src_row0 + tok_list[r]) * a.d + (size_t)c * 8;
-      *reinterpret_cast<uint4 *>(a.pool + dst) = *reinterpret_cast<const uint4 *>(a.K + src);
-      *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = *reinterpret_cast<const uint4 *>(a.V + src);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (page[u] == -2) continue;
+        if (page[u] < 0 || (int64_t)page[u] >= a.pool_pages) {
+          report(a.status, TG_STATUS_BAD_PAGE);
+          continue;
+        }
+        const int e = e0 + u * kThreads, k = taken + e / d16, c = e % d16;
+        const size_t dst = ((((size_t)page[u] * a.H_p + hpos) * 2) * a.P + (k % a.P)) * a.d + (size_t)c * 8;
+        *reinterpret_cast<uint4 *>(a.pool + dst) = kv[u][0];
+        *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = kv[u][1];
+      }
     }
     taken += sel_total;
     eq_seen += eq_total;
@@ -274,10 +293,10 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
   if (e == cudaSuccess) {
-    // enough CTAs per row for about two resident 1024-thread CTAs per SM, at most 16,
-    // and chunks of at least 2048 tokens
+    // enough CTAs per row for one resident 1024-thread CTA per SM, at most 16, and chunks
+    // of at least 2048 tokens
     const int rows = batch * H;
-    int parts = (2 * sms + rows - 1) / rows;
+    int parts = (sms + rows - 1) / rows;
     parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
     a.parts = parts;
     a.prop = parts > 1 && rows <= kPropRows;
