@@ -293,10 +293,13 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
   if (e == cudaSuccess) {
-    // enough CTAs per row for one resident 1024-thread CTA per SM, at most 16, and chunks
-    // of at least 2048 tokens
+    // CTAs per row: about two waves of one resident 1024-thread CTA per SM when a row's keys
+    // fit in shared memory (each CTA's select is then cheap), one wave when they are read
+    // from L2 (every CTA of a row repeats the select); at most 16, and chunks of at least
+    // 2048 tokens
     const int rows = batch * H;
-    int parts = (sms + rows - 1) / rows;
+    const int waves = Nmax <= kSmemKeys ? 2 : 1;
+    int parts = (waves * sms + rows - 1) / rows;
     parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
     a.parts = parts;
     a.prop = parts > 1 && rows <= kPropRows;
