@@ -51,6 +51,7 @@ struct CompactArgs {
   int H, H_p, G, P, d, Nmax;
   int parts;  // CTAs per row (the even split)
   int prop;   // share the grid's CTAs among the rows in proportion to their retained tokens
+  int rows;   // batch * H
 };
 
 constexpr int kPropRows = 1024;  // rows that the proportional split handles (one per thread)
@@ -61,7 +62,7 @@ constexpr int kMinPart = 2048;   // tokens per CTA at least
 // CTA derives the same shares from ntok and writes its (row, part, parts) to out[0..2], or
 // out[0] = -1 past the last share.
 __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int *scan, int *out) {
-  const int rows = (int)(gridDim.x / a.parts), tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows = a.rows, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int nr = 0, cap = 0;
   if (tid < rows) {
     nr = max(0, a.ntok[tid]);
@@ -302,8 +303,10 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
     int parts = (waves * sms + rows - 1) / rows;
     parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
     a.parts = parts;
+    a.rows = rows;
     a.prop = parts > 1 && rows <= kPropRows;
-    const int64_t grid = (int64_t)rows * parts;
+    // proportional shares take exactly the wanted waves (no partial wave at the end)
+    const int64_t grid = a.prop ? std::max<int64_t>(rows, (int64_t)waves * sms) : (int64_t)rows * parts;
     if (grid > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
     compact_topk_kernel<<<(unsigned)grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     e = cudaGetLastError();
