@@ -296,12 +296,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float c0 = ex2(m0 - mn0), c1 = ex2(m1 - mn1);
         const float p0 = ex2(z0 - mn0), p1 = ex2(z1 - mn1), p2 = ex2(z2 - mn0), p3 = ex2(z3 - mn1);
-        l0 = l0 * c0 + p0 + p2;
-        l1 = l1 * c1 + p1 + p3;
+        // the weights go to the P.V product rounded to bf16; the row sums add the same
+        // rounded weights, so the output is a weighted mean of V under one set of weights
+        const uint32_t pk01 = pack_bf16x2(p0, p1), pk23 = pack_bf16x2(p2, p3);
+        l0 = l0 * c0 + __uint_as_float(pk01 << 16) + __uint_as_float(pk23 << 16);
+        l1 = l1 * c1 + __uint_as_float(pk01 & 0xffff0000u) + __uint_as_float(pk23 & 0xffff0000u);
         m0 = mn0;
         m1 = mn1;
-        const uint32_t b0 = movmatrix_t(pack_bf16x2(p0, p1));
-        const uint32_t b1 = movmatrix_t(pack_bf16x2(p2, p3));
+        const uint32_t b0 = movmatrix_t(pk01);
+        const uint32_t b1 = movmatrix_t(pk23);
         // O^T += V^T . P^T
 #pragma unroll
         for (int mb = 0; mb < KS; ++mb) {

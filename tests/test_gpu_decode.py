@@ -71,6 +71,14 @@ def test_many_items_per_cta(lib, cuda, n_cta):
     assert np.diff(off).max() > 16
 
 
+def test_compaction_with_more_rows_than_the_proportional_split_takes(lib, cuda):
+    """1040 (request, KV head) rows: the one-shot compaction falls back to an even split of its
+    CTAs over the rows (the proportional shares cover up to 1024 rows); retained sets stay
+    bit-exact and the decode over them matches the oracle."""
+    w = synth.small(batch=130, H=8, H_q=16, H_p=4, N=300, L=1)
+    _decode_and_check(lib, w, cuda)
+
+
 def test_decode_over_allocator_pages(lib, cuda):
     """Compaction and decode through page ids handed out by the budget-reservation allocator
     after churn (scattered, not in request order): the results equal the oracle's."""
