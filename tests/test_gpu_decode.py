@@ -79,6 +79,14 @@ def test_compaction_with_more_rows_than_the_proportional_split_takes(lib, cuda):
     _decode_and_check(lib, w, cuda)
 
 
+@pytest.mark.parametrize("d,H,H_q", [(128, 4, 32), (256, 8, 16)])
+def test_many_outputs_within_tolerance(lib, cuda, d, H, H_q):
+    """Every output of 64 requests (2048 or 1024 query heads) against the float64 oracle:
+    the tolerance holds over a large sample, not only on a few sampled heads."""
+    w = synth.small(batch=64, H=H, H_q=H_q, H_p=2, d=d, N=400, L=1)
+    _decode_and_check(lib, w, cuda)
+
+
 def test_decode_over_allocator_pages(lib, cuda):
     """Compaction and decode through page ids handed out by the budget-reservation allocator
     after churn (scattered, not in request order): the results equal the oracle's."""
