@@ -56,17 +56,22 @@ struct CompactArgs {
 
 constexpr int kPropRows = 1024;  // rows that the proportional split handles (one per thread)
 constexpr int kMinPart = 2048;   // tokens per CTA at least
+constexpr int kSweepDiv = 16;    // one swept position costs about 1/16 of one kept token's copy
 
 // Proportional shares: every row gets one CTA; the others go to the rows in proportion to
-// their retained tokens (a row's CTAs each keep at least kMinPart tokens of its range).  Every
+// their work, retained tokens plus positions swept (a row's CTAs each keep at least kMinPart
+// tokens of its range).  Every
 // CTA derives the same shares from ntok and writes its (row, part, parts) to out[0..2], or
 // out[0] = -1 past the last share.
 __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int *scan, int *out) {
   const int rows = a.rows, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // a row's work: its kept tokens' copies, plus the sweep over all its N positions (about
+  // a sixteenth of a kept token's cost per position)
   int nr = 0, cap = 0;
   if (tid < rows) {
-    nr = max(0, a.ntok[tid]);
-    cap = max(0, a.N[tid / a.H] / kMinPart - 1);
+    const int Nr = max(0, a.N[tid / a.H]);
+    nr = max(0, a.ntok[tid]) + Nr / kSweepDiv;
+    cap = max(0, Nr / kMinPart - 1);
   }
   long long tot = nr;
 #pragma unroll
