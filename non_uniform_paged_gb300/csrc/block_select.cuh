@@ -1,7 +1,8 @@
 // Block-wide helpers for exact top-k selection with ties to the lower index:
-// an exclusive scan of per-thread flags and an MSB-first radix select over
-// order-preserving uint32 keys.  Used by the token top-k compaction and by the
-// page top-K.
+// an exclusive scan of per-thread flags and MSB-first radix selects over
+// order-preserving uint32 keys (a plain one, and one that narrows to a candidate
+// list in shared memory).  Used by the one-shot and the chunked token compaction
+// and by the page top-K of long rows.
 #pragma once
 
 #include <cstdint>
