@@ -158,6 +158,8 @@ __global__ void build_minmax_kernel(const uint16_t *K, uint16_t *mm, int N, int 
   const int t0 = p * P, t1 = min(N, t0 + P);
   const uint32_t *src = reinterpret_cast<const uint32_t *>(K + ((size_t)row * N + t0) * d) + c;
   float mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY;
+  // the page's rows are independent loads: unrolled so that they are all in flight
+#pragma unroll 16
   for (int t = t0; t < t1; ++t, src += d / 2) {
     const uint32_t v = *src;
     mn0 = fminf(mn0, bf16_lo(v));
