@@ -357,6 +357,30 @@ def cta_skew(w, cache, q, out, lse, stream, Bhat, N, device):
     return skew, uni
 
 
+def serialised_step(args, w, cache, q, out, lse, stream):
+    """The decode step with an event recorded after every launch.  The event keeps each launch
+    from overlapping the previous one's tail (programmatic dependent launch), as when a model
+    runs its other kernels between two layers' attention; the launches stay queued, so host
+    latency is not timed."""
+    steps = max(3, args.steps // 10)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps * w.L + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    k = 1
+    for _ in range(steps):
+        for l in range(w.L):
+            cache.decode_layer(l, q[l], out[l], lse[l], stream=stream)
+            evs[k].record(stream)
+            k += 1
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(k - 1)]
+    ms = sum(per) / steps
+    step_bytes = cache.algorithmic_bytes()
+    return {"ms_per_step": ms, "gbs": step_bytes / (ms * 1e-3) / 1e9,
+            "launch_us_median": 1e3 * statistics.median(per), "launch_us_max": 1e3 * max(per), "steps": steps,
+            "timing": "an event after every launch: no launch overlaps the previous one's tail"}
+
+
 def bench_ragged(args, w, rank, world, local, device):
     """Configs 1-3: one decode step = tg_decode_attn on every layer of a compacted ragged cache."""
     import non_uniform_paged_gb300 as tg
@@ -432,6 +456,7 @@ def bench_ragged(args, w, rank, world, local, device):
     barrier(world)
     tg.tg_check_status(cache.status)
     ms_step = max_over_ranks(total_ms / args.steps, world, device)
+    serial = serialised_step(args, w, cache, q, out, lse, stream) if not small else None
 
     # the same step under the uniform split (no flush; for the skew comparison)
     u_steps = max(3, args.steps // 4)
@@ -508,6 +533,8 @@ def bench_ragged(args, w, rank, world, local, device):
         "pct_of_hbm_peak": 100.0 * gbs / peak,
         "retained_kv_tokens_per_s": all_tokens / (ms_step * 1e-3),
         "us_per_step": 1e3 * ms_step,
+        "serialised": (dict(serial, pct_of_hbm_peak=100.0 * serial["gbs"] / peak) if serial else
+                       {"timing": "every launch already timed by its own event pair"}),
         "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
@@ -592,6 +619,8 @@ def bench_sparse(args, w, rank, world, local, device):
             "score_topk_gbs": (mm_bytes / (statistics.mean(sel_ms) * 1e-3) / 1e9) if not dense else None,
             "decode_us": 1e3 * statistics.mean(att_ms),
             "decode_gbs": kv_bytes / (statistics.mean(att_ms) * 1e-3) / 1e9,
+            # the per-launch events keep every launch from overlapping the one before it
+            "serialised_ms_per_step": w.L * (statistics.mean(sel_ms) + statistics.mean(att_ms)),
             "bytes_per_step": step_bytes}
         if not dense and w.d == 128 and n_pages <= 1024:
             # the same layer as one kernel (tg_sparse_layer): score, top-K and decode
@@ -840,7 +869,7 @@ def bench_layerwise(args, w, rank, world, local, device):
     sweep = {}
     for H_p in (1, 2, 4, 8):
         wl = w.replace(H_p=H_p)
-        total_ms, total_bytes, pages, mono, skews = 0.0, 0, 0, 0, []
+        total_ms, serial_ms, total_bytes, pages, mono, skews = 0.0, 0.0, 0, 0, 0, []
         pool = None
         for layer in layers:
             c = RaggedCache(1, wl.batch, wl.H, wl.H_q, wl.d, wl.P, H_p, wl.alpha, Bhat_all[layer:layer + 1], N,
@@ -867,7 +896,13 @@ def bench_layerwise(args, w, rank, world, local, device):
             for _ in range(reps):
                 c.decode_layer(0, q, out)
             b.record()
+            sev = _events(reps + 1)  # an event after every launch: no overlap with the one before
+            sev[0].record()
+            for i in range(reps):
+                c.decode_layer(0, q, out)
+                sev[i + 1].record()
             torch.cuda.synchronize()
+            serial_ms += sum(sev[i].elapsed_time(sev[i + 1]) for i in range(reps)) / reps
             c.decode_layer(0, q, out, cta_time=ct)
             torch.cuda.synchronize()
             tg.tg_check_status(c.status)
@@ -881,6 +916,8 @@ def bench_layerwise(args, w, rank, world, local, device):
         scale = w.L / len(layers)
         sweep[f"H_p={H_p}"] = {"ms_per_step": total_ms * scale, "gbs": total_bytes / (total_ms * 1e-3) / 1e9,
                                "pct_of_hbm_peak": 100 * total_bytes / (total_ms * 1e-3) / 1e9 / peak,
+                               "serialised_ms_per_step": serial_ms * scale,
+                               "serialised_gbs": total_bytes / (serial_ms * 1e-3) / 1e9,
                                "pool_gb": pages * H_p * 2 * w.P * w.d * 2 * scale / 1e9,
                                "monolithic_pool_gb": mono * w.H * 2 * w.P * w.d * 2 * scale / 1e9,
                                "cta_skew_max": float(max(skews)), "cta_skew_mean": float(np.mean(skews)),
