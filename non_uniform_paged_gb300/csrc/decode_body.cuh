@@ -58,11 +58,11 @@ template <int D>
 struct KCfg;
 template <>
 struct KCfg<128> {
-  static constexpr int NW = 8, R = 3;
+  static constexpr int NW = 8, R = 2;
 };
 template <>
 struct KCfg<256> {
-  static constexpr int NW = 4, R = 3;
+  static constexpr int NW = 4, R = 2;
 };
 
 constexpr int kMaxItems = 16;  // work items per CTA kept in shared memory (more are read from global)
