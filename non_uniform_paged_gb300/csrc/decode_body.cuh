@@ -426,22 +426,36 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
               }
             }
             __syncthreads();
-            // O = sum_p o_p 2^(m_p - M), parts in order, eight loads in flight per thread
-            for (int e = tid; e < g * D; e += NT) {
+            // O = sum_p o_p 2^(m_p - M), parts in order.  A thread takes outputs e and e + NT
+            // together, eight parts of each per batch: sixteen loads in flight
+            auto put = [&](int e, float O) {
               const int hd = e / D, dd = e % D;
-              float O = 0.f;
-              int p = 0;
-              for (; p + 8 <= np; p += 8) {
-                float v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(p + u) * g * D + e);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) O += v[u] * fac[(p + u) * g + hd];
-              }
-              for (; p < np; ++p) O += __ldcg(po + (size_t)p * g * D + e) * fac[p * g + hd];
               __nv_bfloat16 v = __float2bfloat16_rn(O / comb_l[hd]);
               a.out[(out_row0 + hd) * D + dd] = *reinterpret_cast<uint16_t *>(&v);
               if (dd == 0 && a.lse) a.lse[out_row0 + hd] = (comb_m[hd] + log2f(comb_l[hd])) * kLn2;
+            };
+            for (int e0 = tid; e0 < g * D; e0 += 2 * NT) {
+              const int e1 = e0 + NT;
+              const bool has1 = e1 < g * D;
+              const int hd0 = e0 / D, hd1 = has1 ? e1 / D : 0;
+              float O0 = 0.f, O1 = 0.f;
+              for (int p = 0; p < np; p += 8) {
+                float v0[8], v1[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const bool ok = p + u < np;
+                  v0[u] = ok ? __ldcg(po + (size_t)(p + u) * g * D + e0) : 0.f;
+                  v1[u] = ok && has1 ? __ldcg(po + (size_t)(p + u) * g * D + e1) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (p + u < np) {
+                    O0 += v0[u] * fac[(p + u) * g + hd0];
+                    if (has1) O1 += v1[u] * fac[(p + u) * g + hd1];
+                  }
+              }
+              put(e0, O0);
+              if (has1) put(e1, O1);
             }
           } else {  // more parts than the buffer holds factors for: straight loops
             for (int e = tid; e < g * D; e += NT) {
