@@ -36,6 +36,53 @@ __device__ __forceinline__ int block_excl_count(bool flag, int *scratch, int &to
   return scratch[warp] + in_warp;
 }
 
+// Exclusive prefix counts of U flags per thread over the block, in the order (u, thread):
+// every thread's flag u comes after all flags u' < u and after flag u of lower threads.
+// rank[u] is flag u's count of earlier set flags; `total` the block's set flags.  `scratch`
+// holds at least U * NT / 32 + 1 ints of shared memory.  Contains two __syncthreads.
+template <int NT, int U>
+__device__ __forceinline__ void block_excl_count_multi(const bool (&flag)[U], int *scratch, int (&rank)[U],
+                                                       int &total) {
+  constexpr int NWARP = NT / 32, NV = U * NWARP, PER = NV / 32;
+  static_assert(NT % 32 == 0 && NT <= 1024 && NV % 32 == 0, "block size");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  int in_warp[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, flag[u]);
+    in_warp[u] = __popc(bal & lt);
+    if (lane == 0) scratch[u * NWARP + warp] = __popc(bal);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lane l scans values l*PER .. l*PER + PER - 1 of the (u, warp) sequence
+    int v[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      v[j] = scratch[lane * PER + j];
+      sum += v[j];
+    }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    int run = inc - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      scratch[lane * PER + j] = run;
+      run += v[j];
+    }
+    if (lane == 31) scratch[NV] = inc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < U; ++u) rank[u] = scratch[u * NWARP + warp] + in_warp[u];
+  total = scratch[NV];
+}
+
 // Find the key T of the k-th largest of `count` keys (1 <= k <= count) and the
 // number of keys equal to T that a top-k must take (the lowest-indexed ones):
 // need_eq = k - #{key > T}.  get(i) returns key i.  `hist` is 256 ints and

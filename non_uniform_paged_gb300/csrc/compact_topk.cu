@@ -35,6 +35,7 @@ namespace {
 using namespace tgk;
 
 constexpr int kThreads = 1024;
+constexpr int kRound = 4;  // positions per thread in one round of the kept-token sweep
 constexpr int kSmemKeys = 49152;  // rows up to this length keep their keys in shared memory (192 KB)
 
 struct CompactArgs {
@@ -109,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
   __shared__ int hist[256];
   __shared__ int scan[33];
   __shared__ int sel_scratch[4];
-  __shared__ int tok_list[kThreads];
+  __shared__ int tok_list[kRound * kThreads];
+  __shared__ int rank_scratch[kRound * kThreads / 32 + 1];
   __shared__ int err_flag;
 
   int row = blockIdx.x / a.parts, part = blockIdx.x % a.parts, parts = a.parts;
@@ -210,18 +212,28 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
     __syncthreads();
   }
   int taken = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
-  for (int c0 = c_begin; c0 < c_end && taken < n; c0 += kThreads) {
-    const int t = c0 + threadIdx.x;
-    const uint32_t key = t < c_end ? key_of(t) : 0u;
-    const bool gt = t < c_end && key > T, eq = t < c_end && key == T;
-    int eq_total, sel_total;
-    const int eq_rank = eq_seen + block_excl_count<kThreads>(eq, scan, eq_total);
-    const bool sel = gt || (eq && eq_rank < need_eq);
-    const int k_in = block_excl_count<kThreads>(sel, scan, sel_total);
-    if (sel) {
-      tok_list[k_in] = t;
-      if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in] = t;
+  // rounds of kRound * kThreads positions, position c0 + u * kThreads + thread
+  for (int c0 = c_begin; c0 < c_end && taken < n; c0 += kRound * kThreads) {
+    bool gt[kRound], eq[kRound], sel[kRound];
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+      const int t = c0 + u * kThreads + threadIdx.x;
+      const uint32_t key = t < c_end ? key_of(t) : 0u;
+      gt[u] = t < c_end && key > T;
+      eq[u] = t < c_end && key == T;
     }
+    int eq_rank[kRound], k_in[kRound], eq_total, sel_total;
+    block_excl_count_multi<kThreads, kRound>(eq, rank_scratch, eq_rank, eq_total);
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) sel[u] = gt[u] || (eq[u] && eq_seen + eq_rank[u] < need_eq);
+    block_excl_count_multi<kThreads, kRound>(sel, rank_scratch, k_in, sel_total);
+#pragma unroll
+    for (int u = 0; u < kRound; ++u)
+      if (sel[u]) {
+        const int t = c0 + u * kThreads + threadIdx.x;
+        tok_list[k_in[u]] = t;
+        if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in[u]] = t;
+      }
     __syncthreads();
     // four rows' K and V vectors loaded before any is stored
     for (int e0 = threadIdx.x; e0 < sel_total * d16; e0 += 4 * kThreads) {
