@@ -235,15 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
         if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in[u]] = t;
       }
     __syncthreads();
-    // four rows' K and V vectors loaded before any is stored
-    for (int e0 = threadIdx.x; e0 < sel_total * d16; e0 += 4 * kThreads) {
-      uint4 kv[4][2];
-      int32_t page[4];
+    // the round's kept rows: element e = (row e / d16, 16-byte chunk e % d16) of K and of V;
+    // a thread takes e = thread + j * kThreads.  Two groups of two elements alternate, so one
+    // group's loads are in flight while the other group is stored
+    const int total = sel_total * d16;
+    auto load2 = [&](int j0, uint4 (&kv)[2][2], int32_t (&page)[2]) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kThreads;
+      for (int u = 0; u < 2; ++u) {
+        const int e = (int)threadIdx.x + (j0 + u) * kThreads;
         page[u] = -2;
-        if (e < sel_total * d16) {
+        if (e < total) {
           const int r = e / d16, c = e % d16;
           page[u] = a.pt_ids[base + (taken + r) / a.P];
           const size_t src = (src_row0 + tok_list[r]) * a.d + (size_t)c * 8;
@@ -251,17 +252,35 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
           kv[u][1] = *reinterpret_cast<const uint4 *>(a.V + src);
         }
       }
+    };
+    auto store2 = [&](int j0, const uint4 (&kv)[2][2], const int32_t (&page)[2]) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         if (page[u] == -2) continue;
         if (page[u] < 0 || (int64_t)page[u] >= a.pool_pages) {
           report(a.status, TG_STATUS_BAD_PAGE);
           continue;
         }
-        const int e = e0 + u * kThreads, k = taken + e / d16, c = e % d16;
+        const int e = (int)threadIdx.x + (j0 + u) * kThreads, k = taken + e / d16, c = e % d16;
         const size_t dst = ((((size_t)page[u] * a.H_p + hpos) * 2) * a.P + (k % a.P)) * a.d + (size_t)c * 8;
         *reinterpret_cast<uint4 *>(a.pool + dst) = kv[u][0];
         *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = kv[u][1];
+      }
+    };
+    const int J = (total - (int)threadIdx.x + kThreads - 1) / kThreads;  // this thread's elements
+    if (J > 0) {
+      uint4 ka[2][2], kb[2][2];
+      int32_t pa[2], pb[2];
+      load2(0, ka, pa);
+      for (int j = 0;; j += 4) {
+        load2(j + 2, kb, pb);
+        store2(j, ka, pa);
+        if (j + 4 >= J) {
+          store2(j + 2, kb, pb);
+          break;
+        }
+        load2(j + 4, ka, pa);
+        store2(j + 2, kb, pb);
       }
     }
     taken += sel_total;
