@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
                              need_eq, n_eq);
 
   const int d16 = a.d / 8;  // 16-byte chunks per row
+  // copy layout: rpp rows per pass, chunk c8 / 8 of row r0 + j * rpp for this thread
+  const int rpp = kThreads / d16, r0 = (int)threadIdx.x / d16;
+  const int c8 = ((int)threadIdx.x % d16) * 8;
+  const int pshift = (a.P & (a.P - 1)) == 0 ? __ffs(a.P) - 1 : -1;  // page of a slot by a shift when P is 2^k
   const size_t src_row0 = (size_t)row * a.Nmax;
   const int c_begin = (int)((int64_t)part * Nb / parts), c_end = (int)((int64_t)(part + 1) * Nb / parts);
   // keys kept before this chunk: all of them above T, and the first need_eq equal to T
@@ -235,19 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
         if (a.kept_idx) a.kept_idx[src_row0 + taken + k_in[u]] = t;
       }
     __syncthreads();
-    // the round's kept rows: element e = (row e / d16, 16-byte chunk e % d16) of K and of V;
-    // a thread takes e = thread + j * kThreads.  Two groups of two elements alternate, so one
-    // group's loads are in flight while the other group is stored
-    const int total = sel_total * d16;
+    // the round's kept rows: thread (r0, c) copies 16-byte chunk c of rows r0, r0 + rpp,
+    // r0 + 2 rpp, ... of K and of V.  Two groups of two rows alternate, so one group's loads
+    // are in flight while the other group is stored
     auto load2 = [&](int j0, uint4 (&kv)[2][2], int32_t (&page)[2]) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int e = (int)threadIdx.x + (j0 + u) * kThreads;
+        const int r = r0 + (j0 + u) * rpp;
         page[u] = -2;
-        if (e < total) {
-          const int r = e / d16, c = e % d16;
-          page[u] = a.pt_ids[base + (taken + r) / a.P];
-          const size_t src = (src_row0 + tok_list[r]) * a.d + (size_t)c * 8;
+        if (r < sel_total) {
+          const int k = taken + r;
+          page[u] = a.pt_ids[base + (pshift >= 0 ? k >> pshift : k / a.P)];
+          const size_t src = (src_row0 + tok_list[r]) * a.d + c8;
           kv[u][0] = *reinterpret_cast<const uint4 *>(a.K + src);
           kv[u][1] = *reinterpret_cast<const uint4 *>(a.V + src);
         }
@@ -261,14 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
           report(a.status, TG_STATUS_BAD_PAGE);
           continue;
         }
-        const int e = (int)threadIdx.x + (j0 + u) * kThreads, k = taken + e / d16, c = e % d16;
-        const size_t dst = ((((size_t)page[u] * a.H_p + hpos) * 2) * a.P + (k % a.P)) * a.d + (size_t)c * 8;
+        const int k = taken + r0 + (j0 + u) * rpp;
+        const int slot = pshift >= 0 ? k & (a.P - 1) : k % a.P;
+        const size_t dst = (((size_t)page[u] * a.H_p + hpos) * 2 * a.P + slot) * a.d + c8;
         *reinterpret_cast<uint4 *>(a.pool + dst) = kv[u][0];
         *reinterpret_cast<uint4 *>(a.pool + dst + (size_t)a.P * a.d) = kv[u][1];
       }
     };
-    const int J = (total - (int)threadIdx.x + kThreads - 1) / kThreads;  // this thread's elements
-    if (J > 0) {
+    if (r0 < rpp && r0 < sel_total) {
+      const int J = (sel_total - r0 + rpp - 1) / rpp;  // this thread's rows
       uint4 ka[2][2], kb[2][2];
       int32_t pa[2], pb[2];
       load2(0, ka, pa);
