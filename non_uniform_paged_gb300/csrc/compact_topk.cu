@@ -151,14 +151,23 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
   const float *srow = a.scores + (size_t)row * a.Nmax;
   const bool cached = a.Nmax <= kSmemKeys;  // the launch sized the cache for Nmax keys
   bool nan_seen = false;
-  if (cached) {
-    for (int t = threadIdx.x; t < Nb; t += kThreads) {
-      const float f = srow[t];
-      nan_seen |= is_nan(f);
-      cache[t] = float_key(f);
+  // the row's scores, eight loads in flight per thread: into the key cache when they fit,
+  // else only checked for NaN
+  for (int t0 = threadIdx.x; t0 < Nb; t0 += 8 * kThreads) {
+    float f[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * kThreads;
+      f[u] = t < Nb ? srow[t] : 0.f;
     }
-  } else {
-    for (int t = threadIdx.x; t < Nb; t += kThreads) nan_seen |= is_nan(srow[t]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * kThreads;
+      if (t < Nb) {
+        nan_seen |= is_nan(f[u]);
+        if (cached) cache[t] = float_key(f[u]);
+      }
+    }
   }
   if (nan_seen) err_flag = 1;
   __syncthreads();
