@@ -60,8 +60,8 @@ constexpr int kMinPart = 2048;   // tokens per CTA at least
 constexpr int kSweepDiv = 16;    // one swept position costs about 1/16 of one kept token's copy
 
 // Proportional shares: every row gets one CTA; the others go to the rows in proportion to
-// their work, retained tokens plus positions swept (a row's CTAs each keep at least kMinPart
-// tokens of its range).  Every
+// their work, retained tokens plus positions swept, rounded on the running sum (a row's CTAs
+// each keep at least kMinPart tokens of its range).  Every
 // CTA derives the same shares from ntok and writes its (row, part, parts) to out[0..2], or
 // out[0] = -1 past the last share.
 __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int *scan, int *out) {
@@ -74,16 +74,26 @@ __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int 
     nr = max(0, a.ntok[tid]) + Nr / kSweepDiv;
     cap = max(0, Nr / kMinPart - 1);
   }
-  long long tot = nr;
+  // inclusive prefix of the work over the rows (row order), and the total
+  long long cum = nr;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, cum, o);
+    if (lane >= o) cum += v;
+  }
   long long *wsum = reinterpret_cast<long long *>(hist);  // 32 warp sums (256 bytes)
-  if (lane == 0) wsum[warp] = tot;
+  if (lane == 31) wsum[warp] = cum;
   __syncthreads();
-  tot = 0;
-  for (int w = 0; w < kThreads / 32; ++w) tot += wsum[w];
+  long long tot = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) cum += wsum[w];
+    tot += wsum[w];
+  }
+  // the extra CTAs in proportion to the work, rounded on the running sum: row r gets
+  // floor(E C_{r+1} / tot) - floor(E C_r / tot), so every CTA of the grid has a share
   const long long extra_all = (long long)gridDim.x - rows;
-  const int pr = tid < rows ? 1 + (int)min((long long)cap, tot > 0 ? extra_all * nr / tot : 0ll) : 0;
+  const long long hi = tot > 0 ? extra_all * cum / tot : 0ll, lo = tot > 0 ? extra_all * (cum - nr) / tot : 0ll;
+  const int pr = tid < rows ? 1 + (int)min((long long)cap, hi - lo) : 0;
   // exclusive prefix of the shares: this CTA's row is the one whose range holds blockIdx.x
   int inc = pr;
 #pragma unroll
