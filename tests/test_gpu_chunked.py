@@ -58,6 +58,13 @@ def test_chunked_compaction_matches_oracle(lib, cuda, C):
     _check(lib, w, cuda, C)
 
 
+@pytest.mark.parametrize("P", [32, 48])
+def test_chunked_compaction_page_sizes(lib, cuda, P):
+    """Pages of 32 and 48 slots (48 is not a power of two)."""
+    w = synth.small(batch=3, N=1300, L=1, P=P, H=8, H_q=16, H_p=4)
+    _check(lib, w, cuda, 300)
+
+
 def test_chunked_compaction_ties(lib, cuda):
     w = synth.small(batch=2, N=700, L=1)
     _check(lib, w, cuda, 96, ties=True)

@@ -226,3 +226,34 @@ def test_runs_split_into_very_many_parts(lib, cuda, n_cta):
     cache, _ = _decode_and_check(lib, w, cuda, n_cta=n_cta)
     _, items = lib.plan_items(cache.plan, 0)
     assert items["nparts"].max() > (1056 if n_cta == 8000 else 50)
+
+
+@pytest.mark.parametrize("P,H_p", [(32, 2), (48, 4)])
+def test_page_sizes_other_than_16(lib, cuda, P, H_p):
+    """Pages of 32 (a shift other than 4) and 48 (not a power of two) slots: the compacted
+    pool rows are bit-exact copies of the retained K/V (the unused rows of each head's last
+    page are zero) and the decode over them matches the oracle."""
+    w = synth.small(P=P, H=8, H_q=16, H_p=H_p, N=1300, batch=3, L=1)
+    cache, _ = _decode_and_check(lib, w, cuda, n_cta=40)
+    s = synth.scores(w, 0, cuda)
+    K, V = synth.keys_values(w, 0, cuda)
+    N = synth.contexts(w)
+    ntok = cache.pages["ntok"][0]
+    order = list(cache.pages["order"][0])
+    pt_off, pt_ids = cache.pages["pt_off"], cache.pages["pt_ids"]
+    pool = cache.pool.view(-1, w.d)
+    for b in range(w.batch):
+        for h in range(w.H):
+            n = int(ntok[b, h])
+            if n == 0:
+                continue
+            idx = torch.from_numpy(otg.top_indices(s[b, h, :N[b]].cpu().numpy(), n)).to(cuda)
+            pos = order.index(h)
+            g, j = pos // H_p, pos % H_p
+            k = np.arange(-(-n // P) * P)
+            page = pt_ids[pt_off[b * w.G + g] + k // P].astype(np.int64)
+            rk = torch.from_numpy((page * H_p + j) * 2 * P + k % P).to(cuda)
+            got_k, got_v = pool[rk].view(torch.int16), pool[rk + P].view(torch.int16)
+            assert torch.equal(got_k[:n], K[b, h][idx].view(torch.int16)), (b, h)
+            assert torch.equal(got_v[:n], V[b, h][idx].view(torch.int16)), (b, h)
+            assert not got_k[n:].any() and not got_v[n:].any(), (b, h)
