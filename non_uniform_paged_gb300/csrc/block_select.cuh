@@ -1,5 +1,5 @@
 // Block-wide helpers for exact top-k selection with ties to the lower index:
-// an exclusive scan of per-thread flags and MSB-first radix selects over
+// exclusive scans of per-thread flags (one, or U per thread) and MSB-first radix selects over
 // order-preserving uint32 keys (a plain one, and one that narrows to a candidate
 // list in shared memory).  Used by the one-shot and the chunked token compaction
 // and by the page top-K of long rows.

@@ -8,18 +8,19 @@
 //
 // One 1024-thread CTA per SM; a row (request, KV head) gets C of them (C chosen so
 // the grid fills the GPU, or, for up to 1024 rows, shares in proportion to the
-// rows' retained tokens).  CTA j of a row owns tokens [j N / C, (j+1) N / C) and
-// talks to no other CTA:
+// rows' work, rounded on the running sum).  CTA j of a row owns tokens
+// [j N / C, (j+1) N / C) and talks to no other CTA:
 //  1. exact top-n by an MSB-first radix select over order-preserving keys of
 //     the float32 scores (every CTA of the row finds the same n-th largest key
 //     T and how many keys equal to T to keep; the keys sit in shared memory when
 //     the row fits, else in L2);
 //  2. block-wide counts of the kept keys before its chunk give the chunk's
 //     first output position;
-//  3. one ascending sweep of its chunk keeps key > T, plus the lowest-indexed
-//     keys equal to T, numbers them with a block scan and copies their K and V
-//     rows (16-byte vectors) to page k/P, row k%P of the head's block inside
-//     its group page;
+//  3. one ascending sweep of its chunk, four positions per thread per round,
+//     keeps key > T, plus the lowest-indexed keys equal to T, numbers them with
+//     a block scan and copies their K and V rows (a fixed 16-byte column per
+//     thread, two groups of rows alternating between load and store) to page
+//     k/P, row k%P of the head's block inside its group page;
 //  4. the row's last CTA zero-fills the rows of the head's last page past n,
 //     so a decode kernel may read whole tiles.
 #include "block_select.cuh"
