@@ -40,7 +40,7 @@ using namespace tgk;
 constexpr int kThreads = 1024;
 constexpr int kMaxChunk = 8192;        // tokens per chunk (entering-token list in shared memory)
 constexpr int kSmemKeys = 40960;       // candidates whose score keys are cached in shared memory (160 KB)
-constexpr int kLoadUnroll = 4;         // slot keys each thread has in flight while loading
+constexpr int kLoadUnroll = 12;        // slot keys each thread has in flight while loading
 constexpr int kCopyThreads = 256;      // copy kernel: 8 warps per CTA
 constexpr int kCopyTokens = 4;         // tokens a warp copies at once (their K/V vectors in flight)
 
@@ -112,10 +112,17 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
         if (i0 + u * kThreads < filled) cache[i0 + u * kThreads] = v[u];
     }
   }
-  for (int i = tid; i < len; i += kThreads) {
-    const float f = cs[i];
-    nan_seen |= is_nan(f);
-    if (cached) cache[filled + i] = float_key(f);
+  // the chunk's scores, two per thread in flight
+  for (int i0 = tid; i0 < len; i0 += 2 * kThreads) {
+    float f[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) f[u] = i0 + u * kThreads < len ? cs[i0 + u * kThreads] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (i0 + u * kThreads < len) {
+        nan_seen |= is_nan(f[u]);
+        if (cached) cache[filled + i0 + u * kThreads] = float_key(f[u]);
+      }
   }
   // the head's group page list (checked while the loads above are in flight; nothing has
   // been written yet)
