@@ -35,12 +35,17 @@ METRIC = "decode-attn achieved HBM GB/s (% of GB300 peak) and retained KV tokens
 FALLBACK_HBM_GBS = 6800.0
 
 
-def decode_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, while the kernel
-    sources are unchanged since the capture (else None)."""
+TRAFFIC_PROFILES = {2: "ragged_decode_cfg2_dram.md", 3: "ragged_decode_cfg3_dram.md"}
+
+
+def decode_traffic(cfg=2):
+    """DRAM bytes per decode launch of a workload from its committed ncu summary, while the
+    kernel sources are unchanged since the capture (else None)."""
     import hashlib
+    if cfg not in TRAFFIC_PROFILES:  # (None: no capture applies)
+        return None
     try:
-        text = open(os.path.join(ROOT, "profiles", "ragged_decode_cfg2_dram.md")).read()
+        text = open(os.path.join(ROOT, "profiles", TRAFFIC_PROFILES[cfg])).read()
         vals = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("traffic_", "kernel_")))
         h = hashlib.sha256()
         for f in ("non_uniform_paged_gb300/csrc/decode_attn.cu", "non_uniform_paged_gb300/csrc/decode_body.cuh",
@@ -476,6 +481,8 @@ def bench_ragged(args, w, rank, world, local, device):
     gbs = all_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
     bytes_per_launch = step_bytes / w.L
+    # the workload whose full-size capture applies (none for reduced runs)
+    cap_cfg = next((c for c in TRAFFIC_PROFILES if w.name == synth.workload(c).name), None)
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
 
@@ -538,8 +545,9 @@ def bench_ragged(args, w, rank, world, local, device):
         "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": decode_traffic() if w.name == synth.workload(2).name else None,
-                     "traffic_source": "profiles/ragged_decode_cfg2_dram.md (ncu, full size)",
+                     "traffic": decode_traffic(cap_cfg),
+                     "traffic_source": (f"profiles/{TRAFFIC_PROFILES[cap_cfg]} (ncu, full size)" if cap_cfg
+                                        else None),
                      "peak_kind": peak_kind,
                      "kernel": f"ragged_decode_kernel<{w.d}>",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": 1e3 * avg_launch_ms},
