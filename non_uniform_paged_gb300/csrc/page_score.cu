@@ -22,8 +22,10 @@
 //    form one flat sequence (the MinMax rows are contiguous), split evenly over
 //    one persistent CTA per SM and, inside it, over its warps.  Each warp
 //    streams its contiguous range through its own ring of 1-D bulk copies; each
-//    half warp scores two pages at once, lane j owning slice j, with the two
-//    pages' chains packed into f32x2 FMAs.  The 16 slice sums are combined by an
+//    half warp scores its pages with lane j owning slice j; f32x2 FMAs pair two
+//    query heads of one page (2 <= g <= 4 at d = 128, g = 2 at d = 256) or two
+//    pages (g = 1), and wider groups use scalar FMAs, each chain in the fixed
+//    order below.  The 16 slice sums are combined by an
 //    xor butterfly that also spreads the g heads over the lanes (every add is
 //    one of the fixed pairs; a + b == b + a in float32).  Scores go to the
 //    workspace as order-preserving keys.

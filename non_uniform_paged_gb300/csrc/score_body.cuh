@@ -186,7 +186,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
   constexpr int NW = CF::NW, SP = CF::SP, PPL = CF::PPL, R = CF::R, PAGE = CF::PAGE, STAGE = CF::STAGE;
   constexpr int W = D / 16;   // elements per slice
   constexpr int WV = W / 8;   // 16-byte vectors per slice
-  constexpr bool kPack = GQ * W <= 32;  // q+ and q- as duplicated f32x2 pairs fit in registers
+  constexpr bool kPack = GQ * W <= 32;  // q+ and q- of the slice fit in registers as f32x2 pairs
   // values per lane after the slice sums: NV = PPL pages x GQ heads, value number slot * GQ + head
   constexpr int NV = PPL * GQ;
   constexpr int LS = log2c(NV) < 4 ? log2c(NV) : 4;  // split levels of transpose_sum
@@ -262,8 +262,11 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
     for (int st = 0; st < R && st < nst; ++st) issue(st);
   int issued = min(R, nst);
 
-  // query slice of the current row: packed (q, q) pairs of q+ and q-, or raw bf16 words
-  uint64_t qp2[kPack ? GQ : 1][kPack ? W : 1], qm2[kPack ? GQ : 1][kPack ? W : 1];
+  // query slice of the current row: q+ and q- as f32x2 pairs of heads (2i, 2i+1) when g >= 2,
+  // as (q, q) pairs for g = 1, or raw bf16 words
+  constexpr bool kPair = kPack && GQ >= 2;  // q+ and q- of head pairs (2i, 2i+1) per f32x2
+  constexpr int QA = kPair ? GQ / 2 : (kPack ? GQ : 1);
+  uint64_t qp2[QA][kPack ? W : 1], qm2[QA][kPack ? W : 1];
   uint32_t qv[kPack ? 1 : GQ][kPack ? 1 : W / 2];
   int64_t row = u0 / a.n_pages;
   int64_t row_lo = row * a.n_pages, row_hi = row_lo + a.n_pages;
@@ -281,7 +284,23 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           q_nan |= i < a.g && (is_nan(bf16_lo(w4[e])) || is_nan(bf16_hi(w4[e])));
-          if constexpr (kPack) {
+          if constexpr (kPair) {
+            const float lo = bf16_lo(w4[e]), hi = bf16_hi(w4[e]);
+            const int el = 8 * v + 2 * e;
+            auto put = [&](uint64_t &p, float f) {
+              if ((i & 1) == 0) {
+                p = pack2(f, 0.f);
+              } else {
+                float x, y;
+                unpack2(p, x, y);
+                p = pack2(x, f);
+              }
+            };
+            put(qp2[i / 2][el], fmaxf(lo, 0.f));
+            put(qm2[i / 2][el], fminf(lo, 0.f));
+            put(qp2[i / 2][el + 1], fmaxf(hi, 0.f));
+            put(qm2[i / 2][el + 1], fminf(hi, 0.f));
+          } else if constexpr (kPack) {
             const float lo = bf16_lo(w4[e]), hi = bf16_hi(w4[e]);
             qp2[i][8 * v + 2 * e] = pack2(fmaxf(lo, 0.f), fmaxf(lo, 0.f));
             qm2[i][8 * v + 2 * e] = pack2(fminf(lo, 0.f), fminf(lo, 0.f));
@@ -332,7 +351,49 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
     // score the stage pages in `mine` against the current row's query (all of them lie in it)
     auto score_pages = [&](const uint32_t mine) {
       float val[NV];  // slot * GQ + head
-      if constexpr (kPack) {
+      if constexpr (kPair) {
+        uint64_t acc[PPL][QA];  // (head 2i, head 2i+1) of slot k
+#pragma unroll
+        for (int k = 0; k < PPL; ++k)
+#pragma unroll
+          for (int i = 0; i < QA; ++i) acc[k][i] = 0ull;
+#pragma unroll
+        for (int v = 0; v < WV; ++v) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int el = 8 * v + 2 * e;
+            uint64_t x0[PPL], n0[PPL], x1[PPL], n1[PPL];
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+              const uint32_t wx = (&mx[k][v].x)[e], wn = (&mn[k][v].x)[e];
+              x0[k] = pack2(bf16_lo(wx), bf16_lo(wx));
+              n0[k] = pack2(bf16_lo(wn), bf16_lo(wn));
+              x1[k] = pack2(bf16_hi(wx), bf16_hi(wx));
+              n1[k] = pack2(bf16_hi(wn), bf16_hi(wn));
+            }
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+#pragma unroll
+              for (int i = 0; i < QA; ++i) ffma2(acc[k][i], qp2[i][el], x0[k]);
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+#pragma unroll
+              for (int i = 0; i < QA; ++i) ffma2(acc[k][i], qm2[i][el], n0[k]);
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+#pragma unroll
+              for (int i = 0; i < QA; ++i) ffma2(acc[k][i], qp2[i][el + 1], x1[k]);
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+#pragma unroll
+              for (int i = 0; i < QA; ++i) ffma2(acc[k][i], qm2[i][el + 1], n1[k]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < PPL; ++k)
+#pragma unroll
+          for (int i = 0; i < QA; ++i) unpack2(acc[k][i], val[k * GQ + 2 * i], val[k * GQ + 2 * i + 1]);
+      } else if constexpr (kPack) {
         uint64_t acc[PPL / 2][GQ];  // (slot 2k, slot 2k+1) of head i
 #pragma unroll
         for (int k = 0; k < PPL / 2; ++k)
