@@ -402,6 +402,78 @@ def pin_top_pages(fn=fx.top_pages):
             assert got == (brute_top(list(sc), K) if K else [])
 
 
+def _recursive_sum_bound(e):
+    """Worst-case float32 error of adding the terms e (rows) in any order: d * eps * sum |e|."""
+    e = np.asarray(e, np.float64)
+    return e.shape[-1] * np.finfo(np.float32).eps * np.abs(e).sum(axis=-1)
+
+
+def pin_page_scores(fn=fx.page_scores):
+    """A KV head's page score stands for all of its g query heads.  It must bound max q_j.k_t
+    over every head j of the group and every key t of the page (the reason the page keeps the
+    best key of any head), and on pages of one key (min = max = k) the min-max bound of head j
+    is q_j.k itself, so the score is max_j q_j.k: the dot products alone, in float64, fix it."""
+    r = np.random.default_rng(14)
+    d, P, n_pages = 64, 8, 6
+    for trial in range(30):
+        g = int(r.integers(2, 9))
+        # heads of very different sizes, the largest at a random position: a score that
+        # looked at one head, or at the smallest or mean bound, misses the largest q.k
+        scale = np.float32(2.0) ** r.permutation(np.arange(g)).astype(np.float32) * 3
+        qh = (r.standard_normal((g, d)).astype(np.float32) * scale[:, None]).astype(np.float32)
+        qh = torch.from_numpy(qh).to(torch.bfloat16).float().numpy()   # bf16 values, as stored
+        K = torch.from_numpy(r.standard_normal((n_pages * P, d)).astype(np.float32)).to(
+            torch.bfloat16).float().numpy()
+        mn, mx = fx.page_minmax(K, P)
+        sc = np.asarray(fn(qh, mn, mx), np.float64)
+        assert sc.shape == (n_pages,)
+        for p in range(n_pages):
+            page = K[p * P:(p + 1) * P].astype(np.float64)
+            dots = page @ qh.astype(np.float64).T                      # [P][g]
+            e = np.maximum(qh * mn[p], qh * mx[p])                     # per head: the bound's terms
+            slack = _recursive_sum_bound(e).max()
+            assert sc[p] >= dots.max() - slack, (trial, p)
+        # single-key pages: the score is the largest dot product over the heads
+        k1 = K[:n_pages]
+        sc1 = np.asarray(fn(qh, k1, k1), np.float64)
+        dots1 = k1.astype(np.float64) @ qh.astype(np.float64).T        # [n_pages][g]
+        slack1 = np.array([_recursive_sum_bound(qh * k1[p]).max() for p in range(n_pages)])
+        assert (np.abs(sc1 - dots1.max(axis=1)) <= slack1).all(), trial
+        # a head's order inside the group and a repeated head change nothing
+        perm = r.permutation(g)
+        assert np.array_equal(fn(qh[perm], mn, mx), fn(qh, mn, mx))
+        assert np.array_equal(fn(np.concatenate([qh, qh[:1]]), mn, mx), fn(qh, mn, mx))
+
+
+def pin_select_pages(fn=fx.select_pages):
+    """Query head j belongs to KV head j // g (contiguous groups of g), and each (request, KV
+    head) keeps its K best pages.  On single-key pages whose best dot products are far apart,
+    the selection is the brute-force top K of max over the group's heads of q_j.k (float64)."""
+    r = np.random.default_rng(15)
+    batch, H, g, d, n_pages, K = 2, 3, 4, 32, 7, 3
+    for _ in range(10):
+        q = torch.from_numpy(r.standard_normal((batch, H * g, d)).astype(np.float32)).to(
+            torch.bfloat16).float().numpy()
+        keys = torch.from_numpy(r.standard_normal((batch, H, n_pages, d)).astype(np.float32)).to(
+            torch.bfloat16).float().numpy()
+        got = fn(q, keys, keys, K)
+        for b in range(batch):
+            for h in range(H):
+                best = (keys[b, h].astype(np.float64) @ q[b, h * g:(h + 1) * g].astype(np.float64).T).max(axis=1)
+                srt = np.sort(best)[::-1]
+                if srt[K - 1] - srt[K] < 1e-3:
+                    continue          # too close to call from float64 alone
+                assert list(got[b, h]) == sorted(np.argsort(-best, kind="stable")[:K].tolist()), (b, h)
+
+
+def test_page_scores():
+    pin_page_scores()
+
+
+def test_select_pages():
+    pin_select_pages()
+
+
 def test_page_minmax():
     pin_page_minmax()
 
@@ -650,6 +722,33 @@ def _quest_flat(q, mn, mx):
     return acc
 
 
+def _scores_first_head(q_heads, mn, mx):
+    return fx.quest_bound_f32(np.asarray(q_heads)[0], mn, mx)
+
+
+def _scores_min_heads(q_heads, mn, mx):
+    return np.min(np.stack([fx.quest_bound_f32(q, mn, mx) for q in np.asarray(q_heads)]), axis=0)
+
+
+def _scores_mean_heads(q_heads, mn, mx):
+    return np.mean(np.stack([fx.quest_bound_f32(q, mn, mx) for q in np.asarray(q_heads)]), axis=0)
+
+
+def _scores_sum_heads(q_heads, mn, mx):
+    return np.sum(np.stack([fx.quest_bound_f32(q, mn, mx) for q in np.asarray(q_heads)]), axis=0)
+
+
+def _select_strided_heads(q_l, mn_l, mx_l, K):
+    q_l = np.asarray(q_l, np.float32)
+    batch, H_q, _ = q_l.shape
+    H = np.asarray(mn_l).shape[1]
+    sel = np.empty((batch, H, K), dtype=np.int64)
+    for b in range(batch):
+        for h in range(H):
+            sel[b, h] = fx.top_pages(fx.page_scores(q_l[b, h::H], mn_l[b, h], mx_l[b, h]), K)
+    return sel
+
+
 def _work_list_off_by_one(S_row, ntok_l, order_l, H_p):
     ctas = tg.work_list(S_row, ntok_l, order_l, H_p)
     for items in ctas:
@@ -710,6 +809,11 @@ def _selection_never_refreshed(q_steps, mn, mx, K, unstable, period, stagger):
     (pin_quest_bound, _quest_min),
     (pin_quest_bound, _quest_flat),
     (pin_top_pages, _ties_high),
+    (pin_page_scores, _scores_first_head),
+    (pin_page_scores, _scores_min_heads),
+    (pin_page_scores, _scores_mean_heads),
+    (pin_page_scores, _scores_sum_heads),
+    (pin_select_pages, _select_strided_heads),
     (pin_work_list, _work_list_off_by_one),
     (pin_rerank_rows, _rerank_phase_shifted),
     (pin_rerank_rows, _rerank_no_stagger),
