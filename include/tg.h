@@ -387,16 +387,25 @@ int tg_page_score_workspace(int batch, int H, int n_pages, int64_t *workspace_by
  *   host framework that owns all device memory).  It computes exactly what
  *   tg_decode_attn computes and takes the same arguments except the workspace:
  *   its scratch is a fixed 4 MiB array inside this library, present on every
- *   GPU that loads the library until the process exits.  Nothing is allocated
- *   (no cudaMalloc, no cudaFree, no allocating library call).
+ *   GPU that loads the library until the process exits.  Nothing is
+ *   allocated at call time (no cudaMalloc, no cudaFree, no allocating library
+ *   call).
  *   - Plans whose workspace_bytes exceed 4 MiB are rejected with
  *     TG_ERR_CAPACITY (use tg_decode_attn with a workspace then).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
- *   - Each call clears the array's counters and status word on `stream`
- *     before the kernel.  All calls share the one array, so calls whose
- *     kernels may overlap on the GPU (different streams or host threads) race
- *     on it and must be serialised by the caller. */
+ *   - dev_status is required (NULL is TG_ERR_INVALID_ARG): device faults are
+ *     reported only there.
+ *   - Under CUDA's lazy module loading (the default) the array is loaded with
+ *     this library's module on the first call on a device.  A caller that
+ *     reserves the GPU heap for its own allocator should make one call first
+ *     (or run with CUDA_MODULE_LOADING=EAGER).
+ *   - The array's address is looked up (cudaGetSymbolAddress) on the first
+ *     call in each CUDA context and cached under the context's id, so a call
+ *     after a device reset or from another context looks it up again; make
+ *     the first call in a context before any stream capture.
+ *   - Each call clears the array's merge counters on `stream` before the
+ *     kernel.  All calls share the one array, so calls whose kernels may
+ *     overlap on the GPU (different streams or host threads) race on it and
+ *     must be serialised by the caller. */
 int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
                                   const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
                                   const int64_t *pt_off, const int32_t *pt_ids, float scale,

@@ -239,6 +239,8 @@ def tg_decode_attn_static_scratch(plan_host: np.ndarray, plan_dev, layer: int, q
     Same arguments and result as tg_decode_attn minus the workspace: the scratch
     is a fixed 4 MiB array inside libtg (tg.h: tg_decode_attn_static_scratch).
     Calls that may overlap on the GPU share that array and must be serialised.
+    dev_status (int32, 1 element on the device) is required: device faults are
+    reported only there.
     """
     import torch
     lib = load()

@@ -134,38 +134,81 @@ extern "C" int tg_decode_attn(tg_stream_t stream, const void *plan_host, const v
 // process whose allocator reserved all GPU memory up front, or a plug-in that
 // runs inside a host framework that owns the device heap, gets an error (or
 // breaks the host's memory accounting) from cudaMalloc at request time.  This
-// entry point takes its scratch (merge counters, status word, split-KV
-// partials) from the fixed array below instead of a caller workspace.
+// entry point takes its scratch (merge counters and split-KV partials) from
+// the fixed array below instead of a caller workspace.
 //
 // The array lives in this library's module on every GPU that loads it, until
-// the process exits.  Its device address is looked up once per device with
-// cudaGetSymbolAddress, on that device's first call; make that first call
-// before any stream capture.  Every call shares the array: the counters and
-// the status word are cleared (cudaMemsetAsync) at the start of each call, and
-// calls that overlap on the GPU (two streams, two host threads) race on it.
+// the process exits.  Under CUDA's lazy module loading (the default) the
+// module, and with it the array, is loaded on this entry point's first call on
+// a device; a caller that reserves the GPU heap for its own allocator should
+// make one call (or run with CUDA_MODULE_LOADING=EAGER) before reserving it.
+// The array's device address belongs to a CUDA context, not to a device: it is
+// looked up with cudaGetSymbolAddress on the first call in each context and
+// cached under the context's unique id (cuCtxGetId), so a call after a device
+// reset, or from another context on the same device, looks it up again.  Make
+// the first call in a context before any stream capture.  Every call shares
+// the array: the counters are cleared (cudaMemsetAsync) at the start of each
+// call, and calls that overlap on the GPU (two streams, two host threads) race
+// on it.
 constexpr int64_t kStaticScratchBytes = 4 << 20;  // 4 MiB
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  unsigned long long ctx_id;  // cuCtxGetId of the context the address belongs to
+  void *addr;
+};
+ScratchSlot g_scratch_slot[kMaxDevices] = {};
 
+// cuCtxGetCurrent and cuCtxGetId through the runtime's driver entry points (no link to libcuda)
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns &ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return f;
+}
+
+// the array's address in the current context (the runtime has made it current by now)
 int static_scratch_address(void **out) {
+  const char *fn_name = "tg_decode_attn_static_scratch";
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "%s: %s", fn_name, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: device %d >= %d", dev, kMaxDevices);
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: device %d >= %d", fn_name, dev, kMaxDevices);
+  const CtxFns &cf = ctx_fns();
+  if (!cf.get_current || !cf.get_id) return tgi::fail(TG_ERR_CUDA, "%s: cuCtxGetCurrent/cuCtxGetId unavailable", fn_name);
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (cf.get_current(&ctx) != CUDA_SUCCESS || !ctx || cf.get_id(ctx, &id) != CUDA_SUCCESS)
+    return tgi::fail(TG_ERR_CUDA, "%s: no current CUDA context", fn_name);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchSlot &slot = g_scratch_slot[dev];
+  if (!slot.addr || slot.ctx_id != id) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess || !p)
-      return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+      return tgi::fail(TG_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", fn_name, cudaGetErrorString(e));
+    slot.ctx_id = id;
+    slot.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return TG_OK;
 }
 }  // namespace
@@ -178,6 +221,11 @@ extern "C" int tg_decode_attn_static_scratch(tg_stream_t stream, const void *pla
   const char *fn_name = "tg_decode_attn_static_scratch";
   if (!plan_host || !plan_dev || !q || !pool || !pt_off || !pt_ids || !out)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: NULL pointer argument");
+  // device faults (a copy wait that timed out, a bad page id) are reported only through the
+  // caller's status word: the array's own word is cleared by the next call and read by nobody
+  if (!dev_status)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_decode_attn_static_scratch: dev_status is required (device faults "
+                                         "are reported only there)");
   const tg_plan_header *hd;
   const tg_plan_layer *lt;
   int rc = check_decode_call(fn_name, plan_host, plan_dev, layer, q, pool, scale, &hd, &lt);
@@ -200,7 +248,7 @@ extern "C" int tg_decode_attn_static_scratch(tg_stream_t stream, const void *pla
   uint8_t *ws = static_cast<uint8_t *>(scratch);
   const tgi::WorkspaceLayout wl = tgi::workspace_layout(hd->batch, hd->H, hd->H_q / hd->H, hd->d, hd->max_slots);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the merge counters and the fallback status word must start at zero
+  // the merge counters must start at zero
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)wl.ml, st);
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_decode_attn_static_scratch: memset: %s", cudaGetErrorString(e));
   DecodeArgs args = decode_args(hd, lt, plan_dev, ws, q, out, lse, pt_off, pt_ids, pool_pages, scale, dev_status,
