@@ -2,10 +2,18 @@
 
 One step = one decode step of the whole model: tg_decode_attn (split-KV
 decode + fused log-sum-exp merge) on every layer, over a cache whose retained
-tokens were compacted into ragged group pages at prefill.  Default workload:
-Llama-3.1-8B shape, 32 layers, batch 16, 32K context, P=16, H_p=4, lognormal
-per-head budgets at global retention 0.3 (20.6 GB of retained K/V per step,
-far larger than the 129 MB L2, so no flush is needed between steps).
+tokens were compacted into ragged group pages at prefill.
+
+Default workload: the largest one, Gemma-3-12B-like mixed lengths (48 layers,
+16 q / 8 KV heads, d=256, batch 32, contexts log-uniform in 4K-64K, lognormal
+budgets with safety alpha=2, H_p=4 with budget-aware clustering).  All 48
+layers stay resident (a ~221 GB page pool) and a step is the 48 decode
+launches back to back; each launch reads ~4 GB, far above the 129 MB L2, so no
+flush is needed.  The JSON line's ``rows`` adds the H_p sweep of that workload
+and compact results of the four other workloads (single layer after an L2
+flush; Llama-3.1-8B 32K at rho 0.3; the skew stress with static vs uniform
+split; FlexiCache score + top-K + sparse decode at K = 64 and 128), so one run
+records every target.  ``--config N`` runs one workload alone, in full.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
 reference arm).  Multi-GPU (torchrun): every rank runs an independent replica
@@ -200,7 +208,7 @@ def run_reference(args, rank, world, device):
     """The reference arm: the CPU oracle, timed on this host, on the same workload."""
     if rank != 0:
         return
-    w = synth.workload(args.config)
+    w = synth.workload(args.config or 5)   # the default run's headline is config 5
     gen_dev = device if torch.cuda.is_available() else "cpu"
     for _ in range(args.warmup):
         oracle_sample(w, 0.0, 1, gen_dev, seed=1000)
@@ -240,7 +248,7 @@ def compact_bytes(cache, layer) -> int:
     return scores + kept + tail
 
 
-def build_cache(w, device, n_cta=None, uniform=False):
+def build_cache(w, device, n_cta=None, uniform=False, chunked=True):
     from non_uniform_paged_gb300.ragged import RaggedCache
     import non_uniform_paged_gb300 as tg
     Bhat = synth.budgets_hat(w)
@@ -273,7 +281,8 @@ def build_cache(w, device, n_cta=None, uniform=False):
     rows = {"plan_host_s": plan_s, "compact_topk_ms_per_layer": statistics.mean(comp_ms),
             "compact_topk_gbs": sum(comp_bytes) / (sum(comp_ms) * 1e-3) / 1e9,
             "pages": cache.n_pages, "pages_monolithic": cache.pages["n_pages_monolithic"]}
-    rows["chunked_prefill_compaction"] = chunked_compaction(w, cache, device, comp_ms)
+    if chunked:
+        rows["chunked_prefill_compaction"] = chunked_compaction(w, cache, device, comp_ms)
     return cache, rows, N
 
 
@@ -386,10 +395,11 @@ def serialised_step(args, w, cache, q, out, lse, stream):
             "timing": "an event after every launch: no launch overlaps the previous one's tail"}
 
 
-def bench_ragged(args, w, rank, world, local, device):
-    """Configs 1-3: one decode step = tg_decode_attn on every layer of a compacted ragged cache."""
+def bench_ragged(args, w, rank, world, local, device, emit=True, chunked=True, cpu_baseline=True, e2e_on=True):
+    """Configs 1, 2, 3 and 5: one decode step = tg_decode_attn on every layer of a compacted
+    ragged cache, all layers resident.  Returns the JSON line (printed on rank 0 if emit)."""
     import non_uniform_paged_gb300 as tg
-    cache, rows, N = build_cache(w, device)
+    cache, rows, N = build_cache(w, device, chunked=chunked)
     Bhat = synth.budgets_hat(w)
     q = torch.stack([synth.queries(w, l, device) for l in range(w.L)])        # [L][batch][H_q][d]
     out = torch.empty((w.L, w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=device)
@@ -487,7 +497,7 @@ def bench_ragged(args, w, rank, world, local, device):
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
 
     e2e = None
-    if not args.no_e2e:
+    if e2e_on and not args.no_e2e:
         q_h = q.cpu().pin_memory()
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -517,14 +527,17 @@ def bench_ragged(args, w, rank, world, local, device):
                "l2": "no flush (host copies inside the step)"}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and cpu_baseline and not args.no_cpu_baseline:
         nb, nt, secs, heads = oracle_sample(w, args.cpu_budget, 512, device)
         cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "tokens_per_s": nt / secs,
                "sample": f"{heads} random (layer, request, KV head) runs of this workload, "
                          f"{nt} retained tokens, {secs:.1f} s of float64 numpy attention on one core"}
+    n_cta = cache.n_cta
+    del cache, q, out, lse
+    torch.cuda.empty_cache()
     if rank != 0:
-        return
+        return None
     realised_rho = step_tokens / (w.L * w.batch * w.H * float(np.mean(N)))
     l2 = (f"L2 flushed before every timed iteration (512 MB write); each step reads {step_bytes / 1e6:.1f} MB; "
           f"iterations replayed from one CUDA graph, each decode launch timed by its own event pair"
@@ -536,7 +549,7 @@ def bench_ragged(args, w, rank, world, local, device):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "layers": w.L, "batch": w.batch, "context": int(w.N), "H_q": w.H_q,
                    "H_kv": w.H, "head_dim": w.d, "page": w.P, "H_p": w.H_p, "alpha": w.alpha,
-                   "clustering": w.cluster, "realised_retention": realised_rho, "n_cta": cache.n_cta, "l2": l2},
+                   "clustering": w.cluster, "realised_retention": realised_rho, "n_cta": n_cta, "l2": l2},
         "pct_of_hbm_peak": 100.0 * gbs / peak,
         "retained_kv_tokens_per_s": all_tokens / (ms_step * 1e-3),
         "us_per_step": 1e3 * ms_step,
@@ -557,12 +570,15 @@ def bench_ragged(args, w, rank, world, local, device):
         "clocks": clk,
         "rows": rows,
     }
-    print(json.dumps(line), flush=True)
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
 
 
-def bench_sparse(args, w, rank, world, local, device):
+def bench_sparse(args, w, rank, world, local, device, emit=True, extras=True):
     """Config 4: per layer, Quest page score + top-K (tg_page_score_topk) then decode over the
-    selected pages (tg_decode_attn), for each K; and dense decode over all pages."""
+    selected pages (tg_decode_attn), for each K; and dense decode over all pages.  With extras,
+    also the fused layer, stability-aware rerank and tiered placement.  Returns the JSON line."""
     import non_uniform_paged_gb300 as tg
     from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
     P, n_pages = w.P, w.N // w.P
@@ -630,7 +646,7 @@ def bench_sparse(args, w, rank, world, local, device):
             # the per-launch events keep every launch from overlapping the one before it
             "serialised_ms_per_step": w.L * (statistics.mean(sel_ms) + statistics.mean(att_ms)),
             "bytes_per_step": step_bytes}
-        if not dense and w.d == 128 and n_pages <= 1024:
+        if extras and not dense and w.d == 128 and n_pages <= 1024:
             # the same layer as one kernel (tg_sparse_layer): score, top-K and decode
             def step_fused():
                 for l in range(w.L):
@@ -650,10 +666,12 @@ def bench_sparse(args, w, rank, world, local, device):
                                           "pct_of_hbm_peak": 100 * step_bytes / (ms_f * 1e-3) / 1e9 / peak,
                                           "bytes_per_step": step_bytes}
         del dec
-    rerank = bench_rerank(args, w, q, mms, pools, out, stream, results, device)
-    tiered = bench_tiered(args, w, q, mms, pools, out, stream, device)
+    rerank = bench_rerank(args, w, q, mms, pools, out, stream, results, device) if extras else None
+    tiered = bench_tiered(args, w, q, mms, pools, out, stream, device) if extras else None
+    del pools, mms
+    torch.cuda.empty_cache()
     if rank != 0:
-        return
+        return None
     k0 = f"K{w.topk_pages[0]}"
     best = min((results[k] for k in (k0, k0 + "_fused") if k in results), key=lambda v: v["ms_per_step"])
     line = {"metric": METRIC, "value": best["gbs"], "unit": "GB/s", "n_gpus": world, "steps": args.steps // 10,
@@ -667,7 +685,9 @@ def bench_sparse(args, w, rank, world, local, device):
                                         for k, v in results.items() if k != "dense"},
             "headline_variant": "fused" if best is results.get(k0 + "_fused") else "separate",
             "variants": results, "rerank": rerank, "tiered": tiered, "peak": peak, "peak_kind": peak_kind}
-    print(json.dumps(line), flush=True)
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
 
 
 def bench_rerank(args, w, q, mms, pools, out, stream, results, device):
@@ -864,16 +884,17 @@ def report_pages(args):
     print(json.dumps(out), flush=True)
 
 
-def bench_layerwise(args, w, rank, world, local, device):
-    """Config 5 (d=256, ~220 GB of pages in total): one layer resident at a time.  For each
-    H_p, every layer is compacted into a one-layer pool and its decode launch is timed; the
-    step time is the sum over layers."""
+def hp_sweep(args, w, device, layers):
+    """The page-group size trade-off on the first `layers` layers of a workload, one layer
+    resident at a time: for each H_p, every layer is compacted into a one-layer pool and its
+    decode launch is timed (back to back and with an event after every launch); per-step
+    figures are scaled to all layers."""
     import non_uniform_paged_gb300 as tg
     from non_uniform_paged_gb300.ragged import RaggedCache
     Bhat_all = synth.budgets_hat(w)
     N = synth.contexts(w)
-    layers = range(w.L if not args.layers else args.layers)
-    peak, peak_kind = peaks()
+    layers = range(min(layers, w.L))
+    peak, _ = peaks()
     sweep = {}
     for H_p in (1, 2, 4, 8):
         wl = w.replace(H_p=H_p)
@@ -932,26 +953,72 @@ def bench_layerwise(args, w, rank, world, local, device):
                                "layers_timed": len(layers)}
         del pool
         torch.cuda.empty_cache()
+    return {"timing": f"first {len(layers)} layers, one resident at a time, scaled to {w.L}", **sweep}
+
+
+def _ragged_summary(line, peak):
+    """The figures of a ragged-decode line that its targets are judged on."""
+    if line is None:
+        return None
+    out = {"workload": line["config"]["workload"], "ms_per_step": line["ms_per_step"], "gbs": line["value"],
+           "pct_of_hbm_peak": line["pct_of_hbm_peak"], "retained_kv_tokens_per_s": line["retained_kv_tokens_per_s"],
+           "avg_launch_us": line["roofline"]["avg_launch_us"], "roofline_frac": line["roofline"]["frac"],
+           "l2": line["config"]["l2"]}
+    ser = line.get("serialised") or {}
+    if "ms_per_step" in ser:
+        out["serialised"] = {k: ser[k] for k in ("ms_per_step", "gbs", "pct_of_hbm_peak", "launch_us_median")}
+    sk = line.get("cta_skew") or {}
+    out["cta_skew"] = {k: {kk: v[kk] for kk in ("max_over_mean_busy", "mean_over_layers",
+                                               "isolated_launch_us_mean", "ms_per_step_back_to_back") if kk in v}
+                       for k, v in sk.items()}
+    return out
+
+
+def _sparse_summary(line):
+    if line is None:
+        return None
+    keep = ("ms_per_step", "gbs", "pct_of_hbm_peak", "score_topk_us", "score_topk_gbs", "decode_us", "decode_gbs",
+            "serialised_ms_per_step")
+    return {"workload": line["config"]["workload"],
+            "variants": {k: {kk: v[kk] for kk in keep if kk in v} for k, v in line["variants"].items()},
+            "sparse_vs_dense_speedup": line["sparse_vs_dense_speedup"]}
+
+
+def bench_default(args, rank, world, local, device):
+    """The default run: the largest workload (config 5) fully resident as the headline, then
+    the H_p sweep and compact results of configs 1-4 in `rows`."""
+    w5 = synth.workload(5)
+    line = bench_ragged(args, w5, rank, world, local, device, emit=False, chunked=False)
+    peak, _ = peaks()
+    other = {}
+    if not args.no_rows:
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = 300
+        other["H_p_sweep"] = hp_sweep(args, w5, device, layers=4)
+        for cfg in (1, 2, 3):
+            r = bench_ragged(sub, synth.workload(cfg), rank, world, local, device, emit=False, chunked=cfg != 1,
+                             cpu_baseline=False, e2e_on=False)
+            other[f"config{cfg}"] = _ragged_summary(r, peak)
+            if r is not None:
+                other[f"config{cfg}"]["rows"] = {k: v for k, v in r["rows"].items() if k != "pages_monolithic"}
+        other["config4"] = _sparse_summary(bench_sparse(sub, synth.workload(4), rank, world, local, device,
+                                                        emit=False, extras=False))
     if rank != 0:
         return
-    main_v = sweep["H_p=4"]
-    line = {"metric": METRIC, "value": main_v["gbs"], "unit": "GB/s", "n_gpus": world, "steps": 5,
-            "warmup": args.warmup, "ms_per_step": main_v["ms_per_step"], "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "layers": w.L, "batch": w.batch, "head_dim": w.d, "alpha": w.alpha,
-                       "clustering": True, "timing": "one layer resident at a time; per-layer launches summed",
-                       "l2": "no flush: each launch reads several GB"},
-            "pct_of_hbm_peak": main_v["pct_of_hbm_peak"], "H_p_sweep": sweep, "peak": peak, "peak_kind": peak_kind}
+    line["rows"].update(other)
+    line["config"]["H_p_sweep_layers"] = 4
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default 100 for config 5, else 300)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload 1-5; default 2 (the headline)")
+    ap.add_argument("--config", type=int, default=0,
+                    help="workload 1-5 alone; default 0: config 5 as the headline, with the other configs in rows")
+    ap.add_argument("--no-rows", action="store_true", help="default run: the config-5 headline only")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -962,6 +1029,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is None:
+        args.steps = 100 if args.config in (0, 5) else 300
     if args.report_pages:  # host only: no GPU, no process group
         report_pages(args)
         return
@@ -973,9 +1042,14 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: the GPU arm needs CUDA")
     torch.cuda.set_device(device)
+    if args.config == 0:
+        bench_default(args, rank, world, local, device)
+        return
     w = synth.workload(args.config)
-    if args.config == 5:
-        bench_layerwise(args, w, rank, world, local, device)
+    if args.config == 5 and not (args.layers or args.batch):
+        line = bench_ragged(args, w, rank, world, local, device, emit=True, chunked=False)
+        if rank == 0 and not args.no_rows:
+            print(json.dumps({"H_p_sweep": hp_sweep(args, w, device, layers=w.L)}), flush=True)
         return
     if args.layers or args.batch:
         w = w.replace(L=args.layers or w.L, batch=args.batch or w.batch,
