@@ -10,9 +10,9 @@
 // lists).
 //
 // Design (GB300):
-//  * One persistent CTA per SM slot, NW warps.  The CTA walks its work items
-//    (pieces of one (request, KV head) run); inside an item, 16-token tiles go
-//    round-robin to the warps.
+//  * One persistent CTA per SM slot: NW streaming warps and NE epilogue warps.
+//    The CTA walks its work items (pieces of one (request, KV head) run); inside
+//    an item, 16-token tiles go round-robin to the streaming warps.
 //  * Each warp owns an R-stage ring in shared memory.  Its lane 0 streams the
 //    K and V rows of a tile with 2-D TMA loads (128-byte swizzle) that complete
 //    on the stage's mbarrier; the warp waits with a time limit.
@@ -21,11 +21,13 @@
 //    query heads of the KV head are the N columns), then O^T[d x 8] +=
 //    V^T[d x 16] . P^T[16 x 8].  movmatrix turns the S^T accumulator into the
 //    P^T operand without shared memory.  Online softmax in base 2.
-//  * At the end of an item the warps' (m, l, O) are merged in shared memory.
-//    A run finished by one CTA is normalised and written directly; a run
-//    shared by several CTAs leaves a float32 partial in the workspace, and the
-//    last CTA to finish (atomic counter, no waiting) merges all partials and
-//    resets the counter.
+//  * At the end of an item each streaming warp hands its (m, l, O) to the
+//    epilogue warps through a double-buffered shared-memory slot and streams
+//    on.  The epilogue merges the warps' states: a run finished by one CTA is
+//    normalised and written directly; a run shared by several CTAs leaves a
+//    float32 partial in the workspace, and the last CTA to finish (atomic
+//    counter, no waiting) merges all partials and resets the counter.  Pieces
+//    of shared runs are processed first, so their merges overlap streaming.
 #include "decode_body.cuh"
 
 #include <cuda_runtime.h>
@@ -39,7 +41,7 @@ namespace {
 using namespace tgk;
 
 template <int D>
-__global__ void __launch_bounds__(KCfg<D>::NW * 32, 1)
+__global__ void __launch_bounds__(Layout<D>::THREADS, 1)
     ragged_decode_kernel(const __grid_constant__ CUtensorMap pool_map, const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   decode_body<D>(&pool_map, a, smem_raw);
@@ -53,11 +55,11 @@ void *kernel_ptr() {
 int kernel_config(int d, int g, void **fn, int *threads, int *smem) {
   if (d == 128) {
     *fn = kernel_ptr<128>();
-    *threads = KCfg<128>::NW * 32;
+    *threads = Layout<128>::THREADS;
     *smem = Layout<128>::smem_bytes(g);
   } else if (d == 256) {
     *fn = kernel_ptr<256>();
-    *threads = KCfg<256>::NW * 32;
+    *threads = Layout<256>::THREADS;
     *smem = Layout<256>::smem_bytes(g);
   } else {
     return tgi::fail(TG_ERR_SHAPE, "tg_decode_attn: d=%d (128 or 256)", d);

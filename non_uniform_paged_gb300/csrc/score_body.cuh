@@ -213,8 +213,12 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
     s_more = 0;
   }
   __syncthreads();
-  uint8_t *wring = smem + warp * R * STAGE;                                     // [R][STAGE]
-  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + CF::RING) + warp * R;   // [R]
+  // warps past NW (a kernel launched with more threads, the fused sparse layer) stream nothing:
+  // they take part in the barriers and in the row selections
+  const bool streams = warp < NW;
+  const int nwarps = (int)(blockDim.x >> 5);
+  uint8_t *wring = smem + (streams ? warp : 0) * R * STAGE;                                 // [R][STAGE]
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + CF::RING) + (streams ? warp : 0) * R;  // [R]
 
   // with a separate select kernel next, it may be scheduled now (it waits for this grid
   // before reading keys); with the select fused in, the next kernel (a decode reading the
@@ -224,9 +228,10 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
   // this warp's units [u0, u1)
   const int64_t c0 = (int64_t)blockIdx.x * a.units / gridDim.x;
   const int64_t c1 = (int64_t)(blockIdx.x + 1) * a.units / gridDim.x;
-  const int64_t u0 = c0 + warp * (c1 - c0) / NW, u1 = c0 + (warp + 1) * (c1 - c0) / NW;
+  const int64_t u0 = streams ? c0 + warp * (c1 - c0) / NW : c1;
+  const int64_t u1 = streams ? c0 + (warp + 1) * (c1 - c0) / NW : c1;
   const int nst = (int)((u1 - u0 + SP - 1) / SP);
-  if (lane < R) mbar_init(&wbar[lane], 1);
+  if (streams && lane < R) mbar_init(&wbar[lane], 1);
   fence_barrier_init();
   __syncwarp();
   const uint8_t *src = reinterpret_cast<const uint8_t *>(a.minmax);
@@ -535,7 +540,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs &a, uint8_t *smem) {
     if (nq > 0) {
       __threadfence();   // the other CTAs' key stores, ordered by their counts
       griddep_wait();    // the previous kernel (a decode) may still read sel / pt_ids
-      for (int i = warp; i < nq; i += NW) {
+      for (int i = warp; i < nq; i += nwarps) {
         const int64_t r = s_rows[i];
         const int64_t out = row_id(r);
         if (out >= 0) warp_select(a.keys + r * a.n_pages, a.n_pages, a.K, out, a.sel, a.pt_ids,

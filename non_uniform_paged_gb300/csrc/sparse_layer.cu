@@ -26,10 +26,12 @@ namespace {
 
 constexpr int kD = 128;
 
+// Launched with the decode body's threads; the score phase streams on its first ScoreCfg::NW
+// warps, and the rest join its barriers and row selections.
 template <int GQ>
-__global__ void __launch_bounds__(ScoreCfg<kD>::NW * 32, 1)
+__global__ void __launch_bounds__(Layout<kD>::THREADS, 1)
     sparse_layer_kernel(const __grid_constant__ CUtensorMap pool_map, const ScoreArgs sa, const DecodeArgs da) {
-  static_assert(ScoreCfg<kD>::NW == KCfg<kD>::NW, "both phases run on the same warps");
+  static_assert(ScoreCfg<kD>::NW <= Layout<kD>::THREADS / 32, "the score phase runs on the decode's warps");
   extern __shared__ __align__(1024) uint8_t smem[];
   score_body<kD, GQ>(sa, smem);
   __syncthreads();
@@ -45,7 +47,7 @@ int launch_fused(const char *fn_name, const CUtensorMap &map, const ScoreArgs &s
                  cudaStream_t s) {
   auto fn = sparse_layer_kernel<GQ>;
   const int smem = std::max(ScoreCfg<kD>::SMEM, Layout<kD>::smem_bytes(da.g));
-  const int threads = ScoreCfg<kD>::NW * 32;
+  const int threads = Layout<kD>::THREADS;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   int dev = 0, sms = 0, per_sm = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
