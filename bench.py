@@ -43,27 +43,34 @@ METRIC = "decode-attn achieved HBM GB/s (% of GB300 peak) and retained KV tokens
 FALLBACK_HBM_GBS = 6800.0
 
 
-TRAFFIC_PROFILES = {2: "ragged_decode_cfg2_dram.md", 3: "ragged_decode_cfg3_dram.md"}
+# DRAM traffic of the decode kernel, measured by ncu on small cases that still spill L2 (one
+# kernel, two launches): read+write bytes per algorithmic byte, per head dim
+TRAFFIC_PROFILES = {256: "ragged_decode_cfg5small_dram.md", 128: "ragged_decode_cfg2small_dram.md"}
 
 
-def decode_traffic(cfg=2):
-    """DRAM bytes per decode launch of a workload from its committed ncu summary, while the
-    kernel sources are unchanged since the capture (else None)."""
+def decode_traffic(d, bytes_per_launch):
+    """DRAM bytes of one full decode launch: the ratio of the committed small-case ncu capture of
+    the same kernel times the launch's algorithmic bytes (traffic grows with the tokens read),
+    while the kernel sources are unchanged since the capture (else None).  Returns
+    (bytes or None, source)."""
     import hashlib
-    if cfg not in TRAFFIC_PROFILES:  # (None: no capture applies)
-        return None
+    name = TRAFFIC_PROFILES.get(d)
+    if name is None:
+        return None, None
     try:
-        text = open(os.path.join(ROOT, "profiles", TRAFFIC_PROFILES[cfg])).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
         vals = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("traffic_", "kernel_")))
         h = hashlib.sha256()
         for f in ("non_uniform_paged_gb300/csrc/decode_attn.cu", "non_uniform_paged_gb300/csrc/decode_body.cuh",
                   "non_uniform_paged_gb300/csrc/ptx.cuh"):
             h.update(open(os.path.join(ROOT, f), "rb").read())
         if h.hexdigest() != vals["kernel_sources_sha256"].strip():
-            return None
-        return float(vals["traffic_bytes_per_launch"])
+            return None, f"profiles/{name} (kernel changed since the capture)"
+        ratio = float(vals["traffic_ratio"])
+        return ratio * bytes_per_launch, (f"profiles/{name}: ncu on a small case of the same kernel, "
+                                          f"{ratio:.4f} DRAM bytes per algorithmic byte, scaled to this launch")
     except Exception:
-        return None
+        return None, None
 
 
 def peaks():
@@ -277,6 +284,7 @@ def build_cache(w, device, n_cta=None, uniform=False, chunked=True):
         comp_bytes.append(compact_bytes(cache, layer))
         del s, K, V
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # the per-layer inputs are gone: hold only the cache from here on
     tg.tg_check_status(cache.status)
     rows = {"plan_host_s": plan_s, "compact_topk_ms_per_layer": statistics.mean(comp_ms),
             "compact_topk_gbs": sum(comp_bytes) / (sum(comp_ms) * 1e-3) / 1e9,
@@ -291,8 +299,8 @@ def chunked_compaction(w, cache, device, oneshot_ms, C=2048, layers=2):
     (scores, K, V of C tokens) are cut before the timed region, as a chunked prefill produces
     them; the layers are then compacted again in one shot so the decode pool is unchanged."""
     import non_uniform_paged_gb300 as tg
-    Nmax = int(synth.contexts(w).max())
-    if Nmax < 2 * C:
+    Nmax = int(w.N)  # the width of the score and K/V tensors (every request's context fits in it)
+    if int(synth.contexts(w).max()) < 2 * C:
         return None
     res, res_eager = [], []
     for layer in range(min(layers, w.L)):
@@ -491,9 +499,8 @@ def bench_ragged(args, w, rank, world, local, device, emit=True, chunked=True, c
     gbs = all_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
     bytes_per_launch = step_bytes / w.L
-    # the workload whose full-size capture applies (none for reduced runs)
-    cap_cfg = next((c for c in TRAFFIC_PROFILES if w.name == synth.workload(c).name), None)
     avg_launch_ms = statistics.mean(launch_ms)
+    traffic, traffic_src = decode_traffic(w.d, bytes_per_launch)
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
 
     e2e = None
@@ -558,9 +565,8 @@ def bench_ragged(args, w, rank, world, local, device, emit=True, chunked=True, c
         "cta_skew": skew,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": decode_traffic(cap_cfg),
-                     "traffic_source": (f"profiles/{TRAFFIC_PROFILES[cap_cfg]} (ncu, full size)" if cap_cfg
-                                        else None),
+                     "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "peak_kind": peak_kind,
                      "kernel": f"ragged_decode_kernel<{w.d}>",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_us": 1e3 * avg_launch_ms},
@@ -1057,7 +1063,7 @@ def main():
     if args.config == 4:
         bench_sparse(args, w, rank, world, local, device)
     else:
-        bench_ragged(args, w, rank, world, local, device)
+        bench_ragged(args, w, rank, world, local, device, chunked=args.config != 5)
 
 
 if __name__ == "__main__":

@@ -109,6 +109,48 @@ def test_page_topk_many_rows(lib, cuda):
     _select_case(lib, cuda, 37, 9, 2, 128, 101, 17, seed=5)
 
 
+def _near_tie_case(lib, cuda, batch, H, g, d, n_pages, K, seed, identical=False):
+    """Rows whose pages are one base page with a few bf16 ulps added to one max element:
+    their scores differ by far less than the tensor-core bound band, so the selection rests
+    on the exact float32 scores of the ambiguous pages (and ties go to the lower page)."""
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(seed)
+    q = torch.randn((batch, H * g, d), generator=gen, device=cuda).to(torch.bfloat16)
+    base = torch.randn((batch, H, 1, 2, d), generator=gen, device=cuda).to(torch.bfloat16)
+    base = torch.stack([torch.minimum(base[:, :, :, 0], base[:, :, :, 1]),
+                        torch.maximum(base[:, :, :, 0], base[:, :, :, 1])], 3)
+    mm = base.expand(batch, H, n_pages, 2, d).contiguous()
+    if not identical:
+        bits = mm.view(torch.int16)
+        bump = torch.randint(0, 6, (batch, H, n_pages), generator=gen, device=cuda).to(torch.int16)
+        col = int(torch.argmax(q[0, 0].float().abs()))
+        # one ulp step at a time on the magnitude of a max element (stays >= the min element
+        # when positive; a negative max moves toward zero)
+        mx = bits[:, :, :, 1, col]
+        bits[:, :, :, 1, col] = torch.where(mx >= 0, mx + bump, mx - bump)
+    sel = torch.empty((batch, H, K), dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    lib.tg_page_score_topk(batch, H, g, d, n_pages, K, q, mm, sel, dev_status=status)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(status) == 0
+    mm_h = mm.float().cpu().numpy()
+    ref = ofx.select_pages(q.float().cpu().numpy(), mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
+    assert np.array_equal(sel.cpu().numpy(), ref)
+    if identical:
+        assert (ref == np.arange(K)).all()
+
+
+@pytest.mark.parametrize("g,d,n_pages,K", [(4, 128, 625, 64), (1, 128, 300, 17), (8, 256, 500, 100),
+                                           (4, 128, 1500, 64), (2, 256, 2049, 300)])
+def test_page_topk_near_ties_decided_by_exact_scores(lib, cuda, g, d, n_pages, K):
+    _near_tie_case(lib, cuda, 2, 3, g, d, n_pages, K, seed=n_pages + g)
+
+
+@pytest.mark.parametrize("n_pages,K", [(625, 64), (3000, 700)])
+def test_page_topk_identical_pages_take_the_lowest(lib, cuda, n_pages, K):
+    _near_tie_case(lib, cuda, 1, 2, 4, 128, n_pages, K, seed=9, identical=True)
+
+
 def test_page_topk_workspace_checks(lib, cuda):
     batch, H, n_pages, K = 2, 3, 50, 5
     need = lib.tg_page_score_workspace(batch, H, n_pages)
