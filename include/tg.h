@@ -354,23 +354,33 @@ int tg_rerank_rows(int L, int batch, int H, const uint8_t *unstable, int layer, 
                    int stagger, int32_t *rows, int32_t *n_rows);
 
 /* tg_sparse_layer -- one sparse decode layer (a7 + a8) in one persistent kernel:
- *   Quest scores and top-K pages of every (request, KV head), then flash decoding
- *   over the selected pages.  [FlexiCache] "Core method / Sparse decode".
+ *   Quest scores and top-K pages of the re-ranked (request, KV head) rows, then
+ *   flash decoding over every row's selected pages.  [FlexiCache] "Core method /
+ *   Sparse decode" and "Stability-aware rerank frequency".
  *   A cooperative launch of the plan's N_CTA CTAs (all resident): each scores its
- *   share of pages, the warp completing a row selects it and raises the row's
- *   ready flag to `epoch`; then each CTA waits (about 2 s at most; then
- *   TG_STATUS_TIMEOUT) for the rows of its work items and decodes them.  Results
- *   are those of tg_page_score_topk followed by tg_decode_attn, bit for bit.
+ *   share of the re-ranked rows' pages, the warp completing a row selects it and
+ *   raises the row's ready flag (in score_ws) to `epoch`; then each CTA waits for
+ *   the re-ranked rows of its work items (at most wait_limit_ns each, 0 = about
+ *   2 s; then TG_STATUS_TIMEOUT, and the rows it gave up on decode whatever page
+ *   lists they hold) and decodes them.  Results are those of
+ *   tg_page_score_topk_rows followed by tg_decode_attn, bit for bit.
  * Arguments: plan as tg_decode_attn, built for d = 128 and H_p = 1 page lists of
  *   K pages per (request, KV head) (pt_off = 0, K, 2K, ...); the plan's N_CTA must
  *   not exceed the CTAs that can be resident together (tg_query_ncta gives it).
+ *   rows (device int32 [n_rows], b*H + h) and due (device uint8 [batch*H]): the
+ *   rows re-ranked by this call and, for the decode phase, which rows to wait
+ *   for (1) -- every listed row, and no other.  NULL rows: every row is
+ *   re-ranked (due unused).  A row not re-ranked keeps the page list an earlier
+ *   call wrote.  A row marked due that the list omits is never raised: its wait
+ *   runs out (TG_STATUS_TIMEOUT) and its output is unspecified.
  *   q, minmax, sel, pt_ids, score_ws (tg_page_score_workspace bytes, zero-filled
  *   before the first call) as tg_page_score_topk, n_pages <= 1024; pt_ids doubles
  *   as the decode's page lists over pool (the dense cache [batch][H][n_pages] of
- *   H_p = 1 pages).  epoch >= 1 and different from the previous call's on the
- *   same score workspace (e.g. a call counter).  workspace, out, lse, dev_status
- *   as tg_decode_attn.  Launched without programmatic dependent launch. */
+ *   H_p = 1 pages).  epoch >= 1 and above every earlier call's on the same score
+ *   workspace (e.g. a call counter).  workspace, out, lse, dev_status as
+ *   tg_decode_attn.  Launched without programmatic dependent launch. */
 int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const void *plan_dev, int n_pages, int K,
+                    int n_rows, const int32_t *rows, const uint8_t *due, int64_t wait_limit_ns,
                     const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
                     void *score_ws, int64_t score_ws_bytes, int epoch, const uint16_t *pool,
                     int64_t pool_pages, const int64_t *pt_off, float scale, void *workspace,

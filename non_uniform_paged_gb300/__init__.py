@@ -24,9 +24,12 @@ __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
            "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
-           "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT"]
+           "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT", "ERR_INVALID_ARG",
+           "ERR_SHAPE", "ERR_NONFINITE", "ERR_CAPACITY", "ERR_CUDA", "ERR_TIMEOUT", "ERR_DEVICE"]
 
 STATUS_NONFINITE, STATUS_BAD_PAGE, STATUS_TIMEOUT, STATUS_BAD_INPUT = 0x1, 0x2, 0x4, 0x8
+# tg.h return codes (TGError.code)
+ERR_INVALID_ARG, ERR_SHAPE, ERR_NONFINITE, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = -1, -2, -3, -4, -5, -6, -7
 PLAN_WAIT_TABLES = 0x1       # tg.h TG_PLAN_WAIT_TABLES
 SCORE_LET_NEXT_START = 0x1   # tg.h TG_SCORE_LET_NEXT_START
 PLAN_MAGIC = 0x31504754
@@ -51,7 +54,8 @@ _SIGS = {
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, ctypes.c_uint32, _P]),
     "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
-    "tg_sparse_layer": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _L, _I, _P, _L, _P, _F, _P, _L, _P, _P, _P]),
+    "tg_sparse_layer": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _L, _P, _P, _P, _P, _P, _L, _I, _P, _L, _P, _F, _P, _L,
+                             _P, _P, _P]),
     "tg_compact_chunk": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P, _I,
                               _P, _L, _P]),
     "tg_compact_chunk_workspace": (_I, [_I, _I, _I, _P]),
@@ -269,11 +273,14 @@ def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok
 
 
 def tg_sparse_layer(plan_host, plan_dev, n_pages, K, q, minmax, sel, pt_ids, score_ws, epoch, pool, pool_pages,
-                    pt_off, scale, workspace, out, lse=None, dev_status=None, stream=None):
-    """Score + top-K + sparse decode of one layer in one kernel (tg.h: tg_sparse_layer)."""
+                    pt_off, scale, workspace, out, lse=None, dev_status=None, stream=None, rows=None, n_rows=0,
+                    due=None, wait_limit_ns=0):
+    """Score + top-K + sparse decode of one layer in one kernel (tg.h: tg_sparse_layer).  rows / due:
+    the re-ranked rows (device int32) and the per-row map of them (device uint8); None: every row."""
     import torch
     _check(load().tg_sparse_layer(_stream(stream), plan_host.ctypes.data, _dev(plan_dev, torch.uint8, "plan_dev"),
-                                  int(n_pages), int(K), _dev(q, torch.bfloat16, "q"),
+                                  int(n_pages), int(K), int(n_rows), _dev(rows, torch.int32, "rows"),
+                                  _dev(due, torch.uint8, "due"), int(wait_limit_ns), _dev(q, torch.bfloat16, "q"),
                                   _dev(minmax, torch.bfloat16, "minmax"), _dev(sel, torch.int32, "sel"),
                                   _dev(pt_ids, torch.int32, "pt_ids"), _dev(score_ws, torch.uint8, "score_ws"),
                                   score_ws.numel(), int(epoch), _dev(pool, torch.bfloat16, "pool"), int(pool_pages),

@@ -37,6 +37,8 @@ struct DecodeArgs {
   float scale_log2;
   int wait_tables;  // wait for the previous kernel before reading q, pt_off, pt_ids
   const int32_t *row_ready;  // [batch*H]: wait until the rows of this CTA's items hold `epoch` (or NULL)
+  const uint8_t *row_due;    // [batch*H]: only rows marked 1 are waited for (NULL: every row)
+  uint64_t wait_ns;          // limit of each row-ready wait
   int epoch;
 };
 
@@ -175,7 +177,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
   if (a.row_ready)
     for (int i = tid; i < n_items; i += NT) {
       const tg_work_item it = a.items[i_begin + i];
-      if (it.t1 > it.t0 && !wait_flag(a.row_ready + it.b * a.H + it.h, a.epoch, kWaitLimitNs))
+      const int r = it.b * a.H + it.h;
+      if (it.t1 > it.t0 && (!a.row_due || a.row_due[r]) && !wait_flag(a.row_ready + r, a.epoch, a.wait_ns))
         report(a.status, TG_STATUS_TIMEOUT);
     }
   if (items_in_smem)
@@ -653,6 +656,8 @@ inline DecodeArgs decode_args(const tg_plan_header *hd, const tg_plan_layer *lt,
   args.scale_log2 = scale * kLog2e;
   args.wait_tables = (hd->flags & TG_PLAN_WAIT_TABLES) != 0;
   args.row_ready = nullptr;
+  args.row_due = nullptr;
+  args.wait_ns = kWaitLimitNs;
   args.epoch = 0;
   return args;
 }

@@ -77,6 +77,7 @@ int launch_fused(const char *fn_name, const CUtensorMap &map, const ScoreArgs &s
 }  // namespace
 
 extern "C" int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const void *plan_dev, int n_pages, int K,
+                               int n_rows, const int32_t *rows, const uint8_t *due, int64_t wait_limit_ns,
                                const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,
                                void *score_ws, int64_t score_ws_bytes, int epoch, const uint16_t *pool,
                                int64_t pool_pages, const int64_t *pt_off, float scale, void *workspace,
@@ -96,9 +97,14 @@ extern "C" int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const 
     return tgi::fail(TG_ERR_SHAPE, "tg_sparse_layer: need 1 <= K=%d <= n_pages=%d <= %d", K, n_pages,
                      32 * kWarpKeysMax);
   if (epoch < 1) return tgi::fail(TG_ERR_INVALID_ARG, "tg_sparse_layer: epoch must be >= 1");
+  if (wait_limit_ns < 0) return tgi::fail(TG_ERR_INVALID_ARG, "tg_sparse_layer: wait_limit_ns < 0");
+  if (rows && (n_rows < 0 || (int64_t)n_rows > (int64_t)batch * H))
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_sparse_layer: n_rows=%d outside [0, batch*H]", n_rows);
+  if (rows && !due) return tgi::fail(TG_ERR_INVALID_ARG, "tg_sparse_layer: a row list needs its due map");
   if ((int64_t)batch * H * n_pages > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_sparse_layer: page ids overflow int32");
-  const int64_t rows = (int64_t)batch * H;
-  const int64_t keys_bytes = tgi::align_up(rows * n_pages * 4, 256), cnt_bytes = tgi::align_up(rows * 4, 256);
+  const int64_t nrow_total = (int64_t)batch * H;
+  const int32_t *rows_list = rows;
+  const int64_t keys_bytes = tgi::align_up(nrow_total * n_pages * 4, 256), cnt_bytes = tgi::align_up(nrow_total * 4, 256);
   if (score_ws_bytes < keys_bytes + 2 * cnt_bytes)
     return tgi::fail(TG_ERR_CAPACITY, "tg_sparse_layer: score workspace %lld < %lld bytes", (long long)score_ws_bytes,
                      (long long)(keys_bytes + 2 * cnt_bytes));
@@ -121,9 +127,9 @@ extern "C" int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const 
   sa.sel = sel;
   sa.pt_ids = pt_ids;
   sa.status = dev_status;
-  sa.rows = nullptr;
-  sa.total_rows = rows;
-  sa.units = rows * n_pages;
+  sa.rows = rows_list;
+  sa.total_rows = nrow_total;
+  sa.units = (rows_list ? (int64_t)n_rows : nrow_total) * n_pages;
   sa.g = g;
   sa.n_pages = n_pages;
   sa.K = K;
@@ -135,6 +141,8 @@ extern "C" int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const 
   DecodeArgs da = decode_args(hd, lt, plan_dev, static_cast<uint8_t *>(workspace), q, out, lse, pt_off, pt_ids,
                               pool_pages, scale, dev_status, nullptr);
   da.row_ready = ready;
+  da.row_due = rows_list ? due : nullptr;
+  if (wait_limit_ns > 0) da.wait_ns = (uint64_t)wait_limit_ns;
   da.epoch = epoch;
   da.wait_tables = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -202,12 +202,15 @@ class SparseDecoder:
         self.select(q, minmax, stream=stream, layer=layer)
         self.attend(q, pool, out, lse=lse, stream=stream, layer=layer)
 
-    def step_fused(self, q, minmax, pool, out, lse=None, stream=None, layer=0):
-        """select + attend of every row in one kernel (tg_sparse_layer; d = 128, n_pages <= 1024)."""
+    def step_fused(self, q, minmax, pool, out, lse=None, stream=None, layer=0, rows=None, n_rows=0, due=None,
+                   wait_limit_ns=0):
+        """select + attend in one kernel (tg_sparse_layer; d = 128, n_pages <= 1024): every row, or
+        only the listed rows (device int32 rows[:n_rows], with the per-row uint8 map `due`)."""
         self._epoch = getattr(self, "_epoch", 0) % (2 ** 31 - 2) + 1
         tg_sparse_layer(self.plan, self.plan_dev, self.n_pages, self.K, q, minmax, self.sel[layer],
                         self.pt_ids[layer], self.score_ws, self._epoch, pool, self.batch * self.H * self.n_pages,
-                        self.pt_off, self.scale, self.workspace, out, lse=lse, dev_status=self.status, stream=stream)
+                        self.pt_off, self.scale, self.workspace, out, lse=lse, dev_status=self.status, stream=stream,
+                        rows=rows, n_rows=n_rows, due=due, wait_limit_ns=wait_limit_ns)
 
     def algorithmic_bytes(self, scored_rows=None) -> int:
         """MinMax read (of the scored rows; all by default) + selected K/V pages + page ids +

@@ -383,6 +383,78 @@ def test_fused_layer_equals_separate_kernels(lib, cuda, g, K):
         assert torch.equal(res_f[l][0], res_s[l][0]) and torch.equal(res_f[l][1], res_s[l][1]), l
 
 
+def _fused_case(cuda, g=4, K=6):
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=3, N=480, L=1, H_q=8 * g)
+    P, n_pages = w.P, w.N // w.P
+    mk = lambda: SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=40, device=cuda)
+    Kt, Vt = synth.keys_values(w, 0, cuda)
+    layer = (build_minmax(Kt, P), _dense_pool(Kt, Vt, P))
+    out = lambda: (torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda),
+                   torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda))
+    return w, mk, layer, out
+
+
+def test_fused_layer_reranks_only_the_listed_rows(lib, cuda):
+    """Stability-aware rerank in the fused layer: after a full step, a step with a new query
+    re-ranks only the listed rows (the others keep their pages) -- the same selection and
+    output, bit for bit, as tg_page_score_topk_rows followed by tg_decode_attn."""
+    w, mk, (mm, pool), out = _fused_case(cuda)
+    fused, sep = mk(), mk()
+    q0 = synth.queries(w, 0, cuda)
+    q1 = synth.queries(w, 1, cuda)
+    rows_l = [0, 4, 5, 11, 23]
+    rows = torch.tensor(rows_l, dtype=torch.int32, device=cuda)
+    due = torch.zeros(w.batch * w.H, dtype=torch.uint8, device=cuda)
+    due[rows.long()] = 1
+    rf, rs = out(), out()
+    fused.step_fused(q0, mm, pool, *rf)
+    sep.step(q0, mm, pool, *rs)
+    fused.step_fused(q1, mm, pool, *rf, rows=rows, n_rows=len(rows_l), due=due)
+    sep.select_rows(q1, mm, rows, len(rows_l))
+    sep.attend(q1, pool, *rs)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(fused.status) == 0 and lib.tg_check_status(sep.status) == 0
+    assert torch.equal(fused.sel, sep.sel) and torch.equal(fused.pt_ids, sep.pt_ids)
+    assert torch.equal(rf[0], rs[0]) and torch.equal(rf[1], rs[1])
+    # the listed rows moved with the query, the others kept step 0's pages
+    full = mk()
+    rq = out()
+    full.step(q1, mm, pool, *rq)
+    torch.cuda.synchronize()
+    sel_new, sel_all = fused.sel.view(w.batch * w.H, -1), full.sel.view(w.batch * w.H, -1)
+    assert torch.equal(sel_new[rows.long()], sel_all[rows.long()])
+
+
+def test_fused_layer_wait_for_a_row_nothing_selects_runs_out(lib, cuda):
+    """The decode phase's wait for a re-ranked row is bounded: a row marked due that the row
+    list omits is never selected, so its wait runs out after the given limit (1 ms), the kernel
+    finishes, TG_STATUS_TIMEOUT is reported (tg_check_status: TG_ERR_TIMEOUT) and the context
+    stays usable for the next call."""
+    from non_uniform_paged_gb300 import STATUS_TIMEOUT, TGError
+    w, mk, (mm, pool), out = _fused_case(cuda)
+    dec = mk()
+    q = synth.queries(w, 0, cuda)
+    r = out()
+    dec.step_fused(q, mm, pool, *r)               # every row selected once
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(dec.status) == 0
+    rows = torch.tensor([1, 2], dtype=torch.int32, device=cuda)
+    due = torch.zeros(w.batch * w.H, dtype=torch.uint8, device=cuda)
+    due[[1, 2, 7]] = 1                           # row 7 is due but not listed: nothing raises it
+    dec.step_fused(q, mm, pool, *r, rows=rows, n_rows=2, due=due, wait_limit_ns=1_000_000)
+    torch.cuda.synchronize()
+    assert int(dec.status.item()) & STATUS_TIMEOUT
+    with pytest.raises(TGError) as e:
+        lib.tg_check_status(dec.status)
+    assert e.value.code == lib.ERR_TIMEOUT
+    # the context still works: a full step after resetting the status word is clean
+    dec.status.zero_()
+    dec.step_fused(q, mm, pool, *r)
+    torch.cuda.synchronize()
+    assert lib.tg_check_status(dec.status) == 0
+
+
 def test_all_pages_equals_dense(lib, cuda):
     """K = n_pages: sparse decode is dense attention over the whole context."""
     from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
