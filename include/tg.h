@@ -447,7 +447,14 @@ int tg_decode_attn_static_scratch(tg_stream_t stream, const void *plan_host, con
  *   may be NULL) is increased by the number of pages copied.  grid_limit > 0
  *   caps the CTAs (one row at a time each), for a low-priority background copy.
  *   A bad row or block sets TG_STATUS_BAD_INPUT / TG_STATUS_BAD_PAGE.
- *   Sizes: 1 <= K <= n_pages, n_pages <= 16384, K <= 1024. */
+ *   Sizes: 1 <= K <= n_pages, n_pages <= 16384, K <= 1024.
+ * A layout that satisfies these rules (the one the Python TieredSparseDecoder
+ *   builds): the pool holds the unstable rows' dense regions first, then the
+ *   stable rows' blocks.  With u(r) the rank of row r among the unstable rows
+ *   and s(r) its rank among the stable rows (both in row order), n_u and n_s
+ *   their counts: dense_base[r] = u(r) * n_pages for an unstable row;
+ *   slot_block[r][k] = n_u * n_pages + s(r) * K + k for a stable row (-1 for an
+ *   unstable one); pool_pages = n_u * n_pages + n_s * K. */
 int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
                     const uint8_t *unstable, int batch, int H, int n_pages, int K, const int32_t *sel,
                     int32_t *slot_page, const int32_t *slot_block, const int64_t *dense_base,
@@ -468,7 +475,11 @@ int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int gri
  *   tg_alloc_release: returns pages; released pages are reused last-in first-
  *     out.  A page not allocated, or listed twice, is TG_ERR_INVALID_ARG and
  *     nothing is released.
- *   tg_alloc_query: free and allocated page counts. */
+ *   tg_alloc_query: free and allocated page counts.
+ * To place a request of tg_build_pages' tables: pass its lists (l, b, g), at
+ *   pt_off index (l*batch + b)*G + g, in (layer, group) order as pages_per_list
+ *   (pt_off[i+1] - pt_off[i] each); the returned ids then fill those lists in the
+ *   same order, list after list (the Python RaggedCache does exactly this). */
 int tg_alloc_state_bytes(int64_t n_pages, int64_t *bytes);
 int tg_alloc_init(void *state, int64_t state_cap, int64_t n_pages);
 int tg_alloc_admit(void *state, int n_lists, const int32_t *pages_per_list, int32_t *ids, int64_t ids_cap,
