@@ -124,10 +124,15 @@ int tg_query_ncta(int d, int g, int *N_CTA);
  * Phi_{l,i} units; CTA j of the group's S_{l,i} CTAs takes units
  * [floor(j W / S), floor((j+1) W / S)).  Each piece of one head's run is one
  * tg_work_item.  A plan is a single self-describing byte buffer:
- *   tg_plan_header | tg_plan_layer[L] | per layer: int32 cta_off[N_CTA+1], tg_work_item[]
- * (every section 16-byte aligned; offsets are in bytes from the buffer start). */
+ *   tg_plan_header | tg_plan_layer[L] | per layer: int32 cta_off[N_CTA+1],
+ *   tg_work_item lead[N_CTA], tg_work_item items[]
+ * (every section 16-byte aligned; offsets are in bytes from the buffer start).
+ * lead[c] is a copy of CTA c's first item (zeros when it has none) whose
+ * reserved[0] holds the CTA's item count and reserved[1] the index of that first
+ * item in items[]: a CTA finds its first item and its count at a fixed place, in
+ * one load, without reading cta_off first. */
 #define TG_PLAN_MAGIC 0x31504754u /* "TGP1" */
-#define TG_PLAN_VERSION 2
+#define TG_PLAN_VERSION 3
 
 /* Plan flag: each tg_decode_attn launch of this plan waits for the previous
  * kernel in the stream to complete before it reads q, pt_off or pt_ids (it
@@ -150,6 +155,7 @@ typedef struct tg_plan_header {
 
 typedef struct tg_plan_layer {
   int64_t cta_off; /* byte offset of int32 [N_CTA + 1]: items of CTA c are [cta_off[c], cta_off[c+1]) */
+  int64_t lead;    /* byte offset of tg_work_item [N_CTA]: each CTA's first item, count and index */
   int64_t items;   /* byte offset of tg_work_item [n_items] */
   int32_t n_items;
   int32_t n_slots; /* partial slots of this layer */
@@ -162,7 +168,7 @@ typedef struct tg_work_item {
   int32_t slot0;   /* first partial slot of the run of (b, h) (when nparts > 1) */
   int32_t part;    /* this CTA's piece of the run, 0 .. nparts-1 */
   int32_t nparts;  /* CTAs that share the run; 1 = this CTA finishes it alone */
-  int32_t reserved[3];
+  int32_t reserved[3]; /* 0 in items[]; in lead[]: item count, first item's index, 0 */
 } tg_work_item;
 
 /* tg_plan_decode -- build the plan for all L layers.

@@ -23,7 +23,7 @@ __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
            "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
-           "tg_check_status", "tg_version", "plan_header", "plan_items", "WORK_ITEM_DTYPE",
+           "tg_check_status", "tg_version", "plan_header", "plan_items", "plan_lead", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT", "ERR_INVALID_ARG",
            "ERR_SHAPE", "ERR_NONFINITE", "ERR_CAPACITY", "ERR_CUDA", "ERR_TIMEOUT", "ERR_DEVICE"]
 
@@ -193,7 +193,8 @@ _HEADER_DTYPE = np.dtype([("magic", "<u4"), ("version", "<i4"), ("L", "<i4"), ("
                           ("N_CTA", "<i4"), ("max_slots", "<i4"), ("flags", "<u4"), ("reserved", "<i4"),
                           ("plan_bytes", "<i8"),
                           ("workspace_bytes", "<i8"), ("layers", "<i8")])
-_LAYER_DTYPE = np.dtype([("cta_off", "<i8"), ("items", "<i8"), ("n_items", "<i4"), ("n_slots", "<i4")])
+_LAYER_DTYPE = np.dtype([("cta_off", "<i8"), ("lead", "<i8"), ("items", "<i8"), ("n_items", "<i4"),
+                         ("n_slots", "<i4")])
 WORK_ITEM_DTYPE = np.dtype([("b", "<i4"), ("h", "<i4"), ("hpos", "<i4"), ("g", "<i4"), ("t0", "<i4"),
                             ("t1", "<i4"), ("slot0", "<i4"), ("part", "<i4"), ("nparts", "<i4"),
                             ("reserved", "<i4", (3,))])
@@ -205,6 +206,16 @@ def plan_header(plan: np.ndarray) -> dict:
     if int(h["magic"]) != PLAN_MAGIC:
         raise ValueError("not a tg plan")
     return {k: int(h[k]) for k in _HEADER_DTYPE.names}
+
+
+def plan_lead(plan: np.ndarray, layer: int) -> np.ndarray:
+    """lead WORK_ITEM_DTYPE [N_CTA] of one plan layer: each CTA's first item, with reserved[0] its
+    item count and reserved[1] the first item's index (tg.h: tg_plan_layer)."""
+    hd = plan_header(plan)
+    lt = np.frombuffer(plan[hd["layers"]:hd["layers"] + _LAYER_DTYPE.itemsize * hd["L"]].tobytes(),
+                       _LAYER_DTYPE)[layer]
+    return np.frombuffer(plan[lt["lead"]:lt["lead"] + hd["N_CTA"] * WORK_ITEM_DTYPE.itemsize].tobytes(),
+                         WORK_ITEM_DTYPE)
 
 
 def plan_items(plan: np.ndarray, layer: int):

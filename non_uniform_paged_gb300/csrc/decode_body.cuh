@@ -21,6 +21,7 @@ constexpr float kLog2e = 1.44269504088896340736f;
 
 struct DecodeArgs {
   const tg_work_item *items;
+  const tg_work_item *lead;  // [N_CTA]: each CTA's first item; reserved[0] its item count, [1] its index
   const int32_t *cta_off;
   const uint16_t *q;
   uint16_t *out;
@@ -164,11 +165,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
   // ---------------- this CTA's work items and their page-table bases, one parallel round trip.
   // Page tables and q are read from L2 (ld.global.cg): the kernel before this one in the
   // stream may have written them just before this grid started
-  const int i_begin = a.cta_off[cta];
-  const int n_items = a.cta_off[cta + 1] - i_begin;
+  // the CTA's first item, its item count and its index in one load (no dependent read of cta_off)
+  const tg_work_item lead = a.lead[cta];
+  const int n_items = lead.reserved[0];
+  const int i_begin = lead.reserved[1];
   const bool items_in_smem = n_items <= kMaxItems;
-  if (items_in_smem)
-    for (int i = tid; i < n_items; i += NT) s_items[i] = a.items[i_begin + i];
+  if (items_in_smem) {
+    // (thread i stores item i: it also reads it below for the page-table base)
+    tg_work_item first = lead;
+    first.reserved[0] = first.reserved[1] = 0;
+    for (int i = tid; i < n_items; i += NT) s_items[i] = i == 0 ? first : a.items[i_begin + i];
+  }
   // page tables written by the kernel just before this one (which let this grid start
   // early): wait for it first
   if (a.wait_tables) griddep_wait();
@@ -634,6 +641,7 @@ inline DecodeArgs decode_args(const tg_plan_header *hd, const tg_plan_layer *lt,
   const uint8_t *pd = static_cast<const uint8_t *>(plan_dev);
   DecodeArgs args;
   args.items = reinterpret_cast<const tg_work_item *>(pd + lt->items);
+  args.lead = reinterpret_cast<const tg_work_item *>(pd + lt->lead);
   args.cta_off = reinterpret_cast<const int32_t *>(pd + lt->cta_off);
   args.q = q;
   args.out = out;

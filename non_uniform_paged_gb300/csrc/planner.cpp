@@ -289,6 +289,8 @@ extern "C" int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, 
   for (int l = 0; l < L; ++l) {
     lt[l].cta_off = pos;
     pos = tgi::align_up(pos + (int64_t)(N_CTA + 1) * 4, 16);
+    lt[l].lead = pos;
+    pos = tgi::align_up(pos + (int64_t)N_CTA * sizeof(tg_work_item), 16);
     lt[l].items = pos;
     lt[l].n_items = (int32_t)items[l].size();
     lt[l].n_slots = slots[l];
@@ -318,6 +320,15 @@ extern "C" int tg_plan_decode(int L, int batch, int H, int H_q, int H_p, int P, 
     std::memcpy(base + lt[l].cta_off, cta_off[l].data(), (N_CTA + 1) * 4);
     if (!items[l].empty())
       std::memcpy(base + lt[l].items, items[l].data(), items[l].size() * sizeof(tg_work_item));
+    // each CTA's first item with its item count and index, at a fixed place
+    tg_work_item *lead = reinterpret_cast<tg_work_item *>(base + lt[l].lead);
+    for (int c = 0; c < N_CTA; ++c) {
+      const int32_t n = cta_off[l][c + 1] - cta_off[l][c];
+      if (n > 0) lead[c] = items[l][cta_off[l][c]];
+      lead[c].reserved[0] = n;
+      lead[c].reserved[1] = cta_off[l][c];
+      lead[c].reserved[2] = 0;
+    }
   }
   return tgi::ok();
 }

@@ -112,6 +112,16 @@ def _check_plan(lib, w, N_CTA, N=None, uniform=False):
                     assert s not in used_slots
                     used_slots.add(s)
         assert used_slots == set(range(len(used_slots)))
+        # lead[c]: CTA c's first item at a fixed place, with its item count and the item's index
+        lead = lib.plan_lead(plan, l)
+        assert len(lead) == N_CTA
+        for c in range(N_CTA):
+            n = int(off[c + 1] - off[c])
+            assert int(lead[c]["reserved"][0]) == n and int(lead[c]["reserved"][1]) == int(off[c]), (l, c)
+            if n:
+                first = items[off[c]]
+                assert all(int(lead[c][f]) == int(first[f]) for f in ("b", "h", "hpos", "g", "t0", "t1", "slot0",
+                                                                     "part", "nparts")), (l, c)
     return plan, S
 
 
