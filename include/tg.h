@@ -243,13 +243,24 @@ int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_d
  *   of this layer; pt_off int64 [batch*G + 1] of this layer's lists; pt_ids int32;
  *   pool bf16 [pool_pages][H_p][2][P][d] (output, 16-byte aligned);
  *   kept_idx int32 [batch][H][Nmax] (output, may be NULL): row (b, h) starts with
- *   the n retained token indices, ascending; dev_status may be NULL.
- *   Host sizes: d % 8 == 0, d <= 512, P % 16 == 0, Nmax >= 1. */
+ *   the n retained token indices, ascending;
+ *   workspace: scratch of at least tg_compact_topk_workspace(batch, H, Nmax) bytes,
+ *   4-byte aligned, no initial contents needed (the call writes every entry it
+ *   reads: each row's n-th largest key, and per block of 1024 positions the keys
+ *   above it and equal to it before the block); concurrent calls need separate
+ *   workspaces; TG_ERR_CAPACITY if it is smaller; dev_status may be NULL.
+ *   Host sizes: d % 8 == 0, d <= 512, P % 16 == 0, Nmax >= 1.
+ * Launches two kernels on `stream`: a select kernel of one thread-block cluster per
+ *   row, and the copy kernel as its programmatic dependent. */
 int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int Nmax,
                     const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
                     const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
                     const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool,
-                    int32_t *kept_idx, int32_t *dev_status);
+                    int32_t *kept_idx, void *workspace, int64_t workspace_bytes, int32_t *dev_status);
+
+/* tg_compact_topk_workspace -- bytes of workspace tg_compact_topk needs:
+ *   batch * H * (4 + 2 * ceil(Nmax / 1024)) * 4. */
+int tg_compact_topk_workspace(int batch, int H, int Nmax, int64_t *workspace_bytes);
 
 /* ------------------------------------------------------------------ f1 ---
  * tg_compact_chunk -- retention fused into chunked prefill: after each chunk of

@@ -19,7 +19,7 @@ import numpy as np
 from . import _build
 
 __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta", "tg_plan_decode",
-           "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_build_minmax", "tg_page_score_topk",
+           "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_compact_topk_workspace", "tg_build_minmax", "tg_page_score_topk",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
            "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
@@ -50,7 +50,8 @@ _SIGS = {
     "tg_plan_decode": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _L, _P, _P]),
     "tg_decode_attn": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _L, _P, _P, _P, _P]),
     "tg_decode_attn_static_scratch": (_I, [_P, _P, _P, _I, _P, _P, _L, _P, _P, _F, _P, _P, _P, _P]),
-    "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P]),
+    "tg_compact_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _L, _P, _P, _P, _L, _P]),
+    "tg_compact_topk_workspace": (_I, [_I, _I, _I, _P]),
     "tg_build_minmax": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tg_page_score_topk": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _L, ctypes.c_uint32, _P]),
     "tg_plan_set_flags": (_I, [_P, ctypes.c_uint32]),
@@ -269,9 +270,18 @@ def tg_decode_attn_static_scratch(plan_host: np.ndarray, plan_dev, layer: int, q
         _dev(dev_status, torch.int32, "dev_status"), _dev(cta_time, torch.int64, "cta_time")))
 
 
+def tg_compact_topk_workspace(batch: int, H: int, Nmax: int) -> int:
+    """Bytes of workspace tg_compact_topk needs (tg.h: tg_compact_topk_workspace)."""
+    lib = load()
+    n = ctypes.c_int64(0)
+    _check(lib.tg_compact_topk_workspace(int(batch), int(H), int(Nmax), ctypes.addressof(n)))
+    return n.value
+
+
 def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok, pt_off, pt_ids, pool_pages,
-                    pool, kept_idx=None, dev_status=None, stream=None):
-    """Top-n retention + compaction of one layer into the group pages (tg.h: tg_compact_topk)."""
+                    pool, workspace, kept_idx=None, dev_status=None, stream=None):
+    """Top-n retention + compaction of one layer into the group pages (tg.h: tg_compact_topk);
+    `workspace` is a uint8 device tensor of at least tg_compact_topk_workspace bytes."""
     import torch
     lib = load()
     _check(lib.tg_compact_topk(_stream(stream), batch, H, H_p, P, d, Nmax, _dev(N, torch.int32, "N"),
@@ -280,6 +290,7 @@ def tg_compact_topk(batch, H, H_p, P, d, Nmax, N, scores, K, V, head_order, ntok
                                _dev(ntok, torch.int32, "ntok"), _dev(pt_off, torch.int64, "pt_off"),
                                _dev(pt_ids, torch.int32, "pt_ids"), int(pool_pages),
                                _dev(pool, torch.bfloat16, "pool"), _dev(kept_idx, torch.int32, "kept_idx"),
+                               _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                _dev(dev_status, torch.int32, "dev_status")))
 
 

@@ -6,23 +6,28 @@
 // ready) and 3.2 Ragged Paging (each H_p-head group writes into its own pages
 // of H_p x 2 x P x d elements).
 //
-// One 1024-thread CTA per SM; a row (request, KV head) gets C of them (C chosen so
-// the grid fills the GPU, or, for up to 1024 rows, shares in proportion to the
-// rows' work, rounded on the running sum).  CTA j of a row owns tokens
-// [j N / C, (j+1) N / C) and talks to no other CTA:
-//  1. exact top-n by an MSB-first radix select over order-preserving keys of
-//     the float32 scores (every CTA of the row finds the same n-th largest key
-//     T and how many keys equal to T to keep; the keys sit in shared memory when
-//     the row fits, else in L2);
-//  2. block-wide counts of the kept keys before its chunk give the chunk's
-//     first output position;
-//  3. one ascending sweep of its chunk, four positions per thread per round,
-//     keeps key > T, plus the lowest-indexed keys equal to T, numbers them with
-//     a block scan and copies their K and V rows (a fixed 16-byte column per
-//     thread, two groups of rows alternating between load and store) to page
-//     k/P, row k%P of the head's block inside its group page;
-//  4. the row's last CTA zero-fills the rows of the head's last page past n,
-//     so a decode kernel may read whole tiles.
+// Two kernels per layer.  Positions of a row (request, KV head) are cut into blocks of
+// kBlk = 1024.
+//  select  one thread-block cluster of C CTAs per row.  CTA j loads its chunk of the row
+//          (a range of whole blocks) once, as order-preserving keys of the float32 scores,
+//          into shared memory, and checks it for NaN.  The exact n-th largest key T of the
+//          whole row comes from an MSB-first radix select in four 8-bit passes: each CTA
+//          histograms its own chunk, and after a cluster barrier every CTA adds up the C
+//          histograms through distributed shared memory, so all of them take the same
+//          digit; the sums over the lower ranks give each CTA the keys above T and equal
+//          to T before its chunk.  The cluster then writes T, need_eq (the keys equal to
+//          T that a top-n takes: the lowest-indexed ones) and, for every block, the keys
+//          > T and == T before it, to the workspace.  The row's keys are read once.
+//  copy    1024-thread CTAs take shares of the rows' blocks, in proportion to the rows'
+//          work (retained tokens plus positions swept).  A CTA reads the counts before its
+//          first block from the workspace and sweeps its blocks in ascending order, four
+//          positions per thread per round: it keeps key > T, plus keys equal to T while
+//          fewer than need_eq of them came before, numbers them with a block scan and
+//          copies their K and V rows (a fixed 16-byte column per thread, two groups of
+//          rows alternating between load and store) to page k/P, row k%P of the head's
+//          block inside its group page.  The row's last CTA zero-fills the rows of the
+//          head's last page past n, so a decode kernel may read whole tiles.  It is a
+//          programmatic dependent of select, which lets it launch as select's CTAs finish.
 #include "block_select.cuh"
 #include "ptx.cuh"
 #include "tg_internal.h"
@@ -35,9 +40,267 @@ namespace {
 
 using namespace tgk;
 
+constexpr int kBlk = 1024;  // positions per block of the prefix-count table
+
+// ---------------------------------------------------------------- select --
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelKeys = 24576;  // keys of a chunk held in shared memory (96 KB, two CTAs per SM); the rest are re-read from L2
+constexpr int kMaxCluster = 8;
+constexpr int kWsHead = 4;  // workspace row: T, need_eq, 2 unused, then (keys > T, keys == T) before each block
+
+struct SelectArgs {
+  const int32_t *N;
+  const float *scores;
+  const int32_t *ntok;
+  int32_t *ws;
+  int32_t *status;
+  int64_t ws_row;  // ints per workspace row
+  int H, Nmax, C;  // C: CTAs per cluster (one cluster per row)
+  int vec;         // score rows start 16-byte aligned: chunks load as float4
+};
+
+__global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const SelectArgs a) {
+  extern __shared__ uint32_t keys[];  // the first kSelKeys keys of this CTA's chunk
+  __shared__ int hist[2][256];        // this CTA's digit counts, alternating between passes
+  __shared__ int tot[256], low[256];  // the cluster's counts, and those of the lower ranks
+  __shared__ int pick[4];
+  __shared__ int bcnt[2][kSelThreads];  // per block of a group: keys > T, keys == T
+  __shared__ int wsum[2][kSelWarps];
+  __shared__ int err;
+
+  const int C = a.C, rank = (int)cluster_ctarank(), row = blockIdx.x / C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Nb = a.N[row / a.H], n = a.ntok[row];
+  // a row with nothing to select (the copy kernel reports bad sizes); every CTA of the
+  // cluster reads the same values, so the whole cluster leaves before its first barrier
+  if (Nb < 0 || Nb > a.Nmax || n <= 0 || n > Nb) return;
+  const int nbr = (Nb + kBlk - 1) / kBlk;
+  const int blk0 = (int)((int64_t)rank * nbr / C), blk1 = (int)((int64_t)(rank + 1) * nbr / C);
+  const int p0 = blk0 * kBlk, cnt = max(0, min(blk1 * kBlk, Nb) - p0);
+  const int cached = min(cnt, kSelKeys);
+  const float *src = a.scores + (size_t)row * a.Nmax + p0;
+  auto key_at = [&](int i) -> uint32_t { return i < cached ? keys[i] : float_key(src[i]); };
+
+  for (int i = tid; i < 2 * 256; i += kSelThreads) (&hist[0][0])[i] = 0;
+  if (tid == 0) err = 0;
+  __syncthreads();
+
+  // load the chunk (two float4 loads in flight per thread), check for NaN, and count the
+  // first digit (a warp's equal top bytes, which coincide for real scores, add once)
+  bool nan_seen = false;
+  auto count_top = [&](uint32_t key, bool valid) {
+    const uint32_t dg = valid ? key >> 24 : 256u;
+    const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+    if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[0][dg], __popc(peers));
+  };
+  const int nv = a.vec ? cnt >> 2 : 0;  // float4 groups
+  for (int base = 0; base < nv; base += 2 * kSelThreads) {
+    float4 f[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int g = base + u * kSelThreads + tid;
+      f[u] = g < nv ? __ldg(reinterpret_cast<const float4 *>(src) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int g = base + u * kSelThreads + tid;
+      const bool valid = g < nv;
+      const uint4 k = make_uint4(float_key(f[u].x), float_key(f[u].y), float_key(f[u].z), float_key(f[u].w));
+      if (valid) {
+        nan_seen |= is_nan_key(k.x) | is_nan_key(k.y) | is_nan_key(k.z) | is_nan_key(k.w);
+        if (4 * g < cached) *reinterpret_cast<uint4 *>(keys + 4 * g) = k;
+      }
+      count_top(k.x, valid);
+      count_top(k.y, valid);
+      count_top(k.z, valid);
+      count_top(k.w, valid);
+    }
+  }
+  for (int base = 4 * nv; base < cnt; base += kSelThreads) {
+    const int i = base + tid;
+    const bool valid = i < cnt;
+    const uint32_t k = valid ? float_key(src[i]) : 0u;
+    if (valid) {
+      nan_seen |= is_nan_key(k);
+      if (i < cached) keys[i] = k;
+    }
+    count_top(k, valid);
+  }
+  if (nan_seen) err = 1;
+  __syncthreads();
+  if (err && tid == 0) report(a.status, TG_STATUS_NONFINITE);
+
+  uint32_t prefix = 0, mask = 0;
+  int k_rem = n, gt_lo = 0, eq_lo = 0;
+  for (int p = 0; p < 4; ++p) {
+    const int shift = 24 - 8 * p;
+    int *h = hist[p & 1];
+    if (p > 0) {
+      // digit p of the keys that match the digits chosen so far (this buffer was last read
+      // by the other CTAs before they arrived at the previous pass's barrier)
+      if (p > 1) {
+        for (int i = tid; i < 256; i += kSelThreads) h[i] = 0;
+        __syncthreads();
+      }
+      for (int base = 0; base < cnt; base += 4 * kSelThreads) {
+        uint32_t kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * kSelThreads + tid;
+          kk[u] = i < cnt ? key_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (base + u * kSelThreads + tid < cnt && (kk[u] & mask) == prefix) atomicAdd(&h[(kk[u] >> shift) & 255u], 1);
+      }
+      __syncthreads();
+    }
+    cluster_arrive();  // this pass's histograms are complete in every CTA ...
+    cluster_wait();
+    if (tid < 256) {
+      // ... and each thread adds up one digit over the cluster
+      int v[kMaxCluster];
+      const uint32_t addr = smem_addr(&h[tid]);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) v[r] = r == rank ? h[tid] : ld_cluster_s32(cluster_map(addr, (uint32_t)r));
+      int s = 0, l = 0;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) {
+          s += v[r];
+          if (r < rank) l += v[r];
+        }
+      tot[tid] = s;
+      low[tid] = l;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down for the digit
+      // that holds the k_rem-th key, and count the lower ranks' keys in the digits above it
+      int lt[8], ll[8], st = 0, sl = 0;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        lt[t] = tot[255 - 8 * lane - t];
+        ll[t] = low[255 - 8 * lane - t];
+        st += lt[t];
+        sl += ll[t];
+      }
+      int inc = st, incl = sl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o), w = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) {
+          inc += v;
+          incl += w;
+        }
+      }
+      const int before = inc - st;
+      if (before < k_rem && k_rem <= inc) {
+        int above = before, above_l = incl - sl;
+        bool found = false;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (!found && above + lt[t] >= k_rem) {
+            found = true;
+            pick[0] = 255 - 8 * lane - t;
+            pick[1] = above;
+            pick[2] = above_l;
+            pick[3] = ll[t];
+          }
+          if (!found) {
+            above += lt[t];
+            above_l += ll[t];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)pick[0] << shift;
+    mask |= 255u << shift;
+    k_rem -= pick[1];
+    gt_lo += pick[2];
+    eq_lo = pick[3];
+  }
+  cluster_arrive_relaxed();  // done reading the other CTAs' histograms
+
+  // per block of the chunk: keys > T and == T before it (a warp counts one block; groups of
+  // kSelThreads blocks are scanned one after another)
+  const uint32_t T = prefix;
+  int32_t *wrow = a.ws + (size_t)row * a.ws_row;
+  if (rank == 0 && tid == 0) {
+    wrow[0] = (int32_t)T;
+    wrow[1] = k_rem;
+  }
+  const int nloc = blk1 - blk0;
+  int carry_gt = gt_lo, carry_eq = eq_lo;
+  for (int g0 = 0; g0 < nloc; g0 += kSelThreads) {
+    const int ng = min(kSelThreads, nloc - g0);
+    for (int j = warp; j < ng; j += kSelWarps) {
+      const int q0 = (g0 + j) * kBlk, q1 = min(q0 + kBlk, cnt);
+      int gt = 0, eq = 0;
+      for (int i = q0 + lane; i < q1; i += 32) {
+        const uint32_t k = key_at(i);
+        gt += k > T;
+        eq += k == T;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        gt += __shfl_xor_sync(0xffffffffu, gt, o);
+        eq += __shfl_xor_sync(0xffffffffu, eq, o);
+      }
+      if (lane == 0) {
+        bcnt[0][j] = gt;
+        bcnt[1][j] = eq;
+      }
+    }
+    __syncthreads();
+    const int vg = tid < ng ? bcnt[0][tid] : 0, ve = tid < ng ? bcnt[1][tid] : 0;
+    int ig = vg, ie = ve;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, ig, o), y = __shfl_up_sync(0xffffffffu, ie, o);
+      if (lane >= o) {
+        ig += x;
+        ie += y;
+      }
+    }
+    if (lane == 31) {
+      wsum[0][warp] = ig;
+      wsum[1][warp] = ie;
+    }
+    __syncthreads();
+    int bg = 0, be = 0, tg = 0, te = 0;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) {
+      if (w < warp) {
+        bg += wsum[0][w];
+        be += wsum[1][w];
+      }
+      tg += wsum[0][w];
+      te += wsum[1][w];
+    }
+    if (tid < ng) {
+      wrow[kWsHead + 2 * (blk0 + g0 + tid)] = carry_gt + bg + ig - vg;
+      wrow[kWsHead + 2 * (blk0 + g0 + tid) + 1] = carry_eq + be + ie - ve;
+    }
+    carry_gt += tg;
+    carry_eq += te;
+    __syncthreads();
+  }
+  // the copy kernel may launch now (letting it take SMs earlier, while this kernel still
+  // selects, measured 20-30% slower on long rows)
+  griddep_launch_dependents();
+  cluster_wait();  // no CTA leaves while another may still read its histograms
+}
+
+// ------------------------------------------------------------------ copy --
 constexpr int kThreads = 1024;
-constexpr int kRound = 4;  // positions per thread in one round of the kept-token sweep
-constexpr int kSmemKeys = 49152;  // rows up to this length keep their keys in shared memory (192 KB)
+constexpr int kRound = 4;       // positions per thread in one round of the kept-token sweep
+constexpr int kPropRows = 1024;  // rows that the proportional split handles (one per thread)
+constexpr int kMinBlocks = 2;   // blocks per CTA at least
+constexpr int kSweepDiv = 16;   // one swept position costs about 1/16 of one kept token's copy
 
 struct CompactArgs {
   const int32_t *N;
@@ -46,25 +309,22 @@ struct CompactArgs {
   const int32_t *head_order, *ntok;
   const int64_t *pt_off;
   const int32_t *pt_ids;
+  const int32_t *ws;
+  int64_t ws_row;
   int64_t pool_pages;
   uint16_t *pool;
   int32_t *kept_idx;
   int32_t *status;
   int H, H_p, G, P, d, Nmax;
   int parts;  // CTAs per row (the even split)
-  int prop;   // share the grid's CTAs among the rows in proportion to their retained tokens
+  int prop;   // share the grid's CTAs among the rows in proportion to their work
   int rows;   // batch * H
 };
 
-constexpr int kPropRows = 1024;  // rows that the proportional split handles (one per thread)
-constexpr int kMinPart = 2048;   // tokens per CTA at least
-constexpr int kSweepDiv = 16;    // one swept position costs about 1/16 of one kept token's copy
-
 // Proportional shares: every row gets one CTA; the others go to the rows in proportion to
 // their work, retained tokens plus positions swept, rounded on the running sum (a row's CTAs
-// each keep at least kMinPart tokens of its range).  Every
-// CTA derives the same shares from ntok and writes its (row, part, parts) to out[0..2], or
-// out[0] = -1 past the last share.
+// each sweep at least kMinBlocks blocks).  Every CTA derives the same shares from ntok and
+// writes its (row, part, parts) to out[0..2], or out[0] = -1 past the last share.
 __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int *scan, int *out) {
   const int rows = a.rows, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // a row's work: its kept tokens' copies, plus the sweep over all its N positions (about
@@ -73,7 +333,7 @@ __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int 
   if (tid < rows) {
     const int Nr = max(0, a.N[tid / a.H]);
     nr = max(0, a.ntok[tid]) + Nr / kSweepDiv;
-    cap = max(0, Nr / kMinPart - 1);
+    cap = max(0, (Nr + kBlk - 1) / kBlk / kMinBlocks - 1);
   }
   // inclusive prefix of the work over the rows (row order), and the total
   long long cum = nr;
@@ -116,28 +376,23 @@ __device__ __forceinline__ void prop_share(const CompactArgs &a, int *hist, int 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const CompactArgs a) {
-  extern __shared__ uint32_t cache[];  // the row's keys when they fit, else the select's candidate list
-  __shared__ int hist[256];
+__global__ void __launch_bounds__(kThreads, 1) compact_copy_kernel(const CompactArgs a) {
+  __shared__ int hist[64];
   __shared__ int scan[33];
-  __shared__ int sel_scratch[4];
+  __shared__ int share[4];
   __shared__ int tok_list[kRound * kThreads];
   __shared__ int rank_scratch[kRound * kThreads / 32 + 1];
-  __shared__ int err_flag;
 
   int row = blockIdx.x / a.parts, part = blockIdx.x % a.parts, parts = a.parts;
   if (a.prop) {
-    prop_share(a, hist, scan, sel_scratch);
-    if (sel_scratch[0] < 0) return;  // past the last share
-    row = sel_scratch[0];
-    part = sel_scratch[1];
-    parts = sel_scratch[2];
-    __syncthreads();  // (hist, scan and sel_scratch are reused below)
+    prop_share(a, hist, scan, share);
+    if (share[0] < 0) return;  // past the last share
+    row = share[0];
+    part = share[1];
+    parts = share[2];
   }
   const int b = row / a.H, h = row % a.H;
   const int Nb = a.N[b], n = a.ntok[row];
-  if (threadIdx.x == 0) err_flag = 0;
-  __syncthreads();
   if (Nb < 0 || Nb > a.Nmax || n < 0 || n > Nb) {
     if (threadIdx.x == 0) report(a.status, TG_STATUS_BAD_INPUT);
     return;
@@ -159,90 +414,39 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
   }
   if (n == 0) return;
 
+  const int nbr = (Nb + kBlk - 1) / kBlk;
+  const int blk0 = (int)((int64_t)part * nbr / parts), blk1 = (int)((int64_t)(part + 1) * nbr / parts);
+  const int c_begin = blk0 * kBlk, c_end = min(blk1 * kBlk, Nb);
   const float *srow = a.scores + (size_t)row * a.Nmax;
-  const bool cached = a.Nmax <= kSmemKeys;  // the launch sized the cache for Nmax keys
-  bool nan_seen = false;
-  // the row's scores, eight loads in flight per thread: into the key cache when they fit,
-  // else only checked for NaN
-  for (int t0 = threadIdx.x; t0 < Nb; t0 += 8 * kThreads) {
-    float f[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int t = t0 + u * kThreads;
-      f[u] = t < Nb ? srow[t] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int t = t0 + u * kThreads;
-      if (t < Nb) {
-        nan_seen |= is_nan(f[u]);
-        if (cached) cache[t] = float_key(f[u]);
-      }
-    }
-  }
-  if (nan_seen) err_flag = 1;
-  __syncthreads();
-  if (err_flag && threadIdx.x == 0 && part == 0) report(a.status, TG_STATUS_NONFINITE);
-  auto key_of = [&](int t) -> uint32_t { return cached ? cache[t] : float_key(srow[t]); };
-
-  uint32_t T;
-  int need_eq, n_eq;
-  // keys read from global memory: once the first digit is chosen, the unused key cache holds
-  // the candidates left, and the remaining passes read only those
-  block_select_kth<kThreads>(Nb, n, key_of, cached ? nullptr : cache, cached ? 0 : kSmemKeys, hist, sel_scratch, T,
-                             need_eq, n_eq);
-
   const int d16 = a.d / 8;  // 16-byte chunks per row
   // copy layout: rpp rows per pass, chunk c8 / 8 of row r0 + j * rpp for this thread
   const int rpp = kThreads / d16, r0 = (int)threadIdx.x / d16;
   const int c8 = ((int)threadIdx.x % d16) * 8;
   const int pshift = (a.P & (a.P - 1)) == 0 ? __ffs(a.P) - 1 : -1;  // page of a slot by a shift when P is 2^k
   const size_t src_row0 = (size_t)row * a.Nmax;
-  const int c_begin = (int)((int64_t)part * Nb / parts), c_end = (int)((int64_t)(part + 1) * Nb / parts);
-  // keys kept before this chunk: all of them above T, and the first need_eq equal to T
-  // (per-thread counts, four keys in flight, then one block sum)
-  int gt_before = 0, eq_before = 0;
-  {
-    int gl = 0, el = 0;
-    for (int c0 = 0; c0 < c_begin; c0 += 4 * kThreads) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = c0 + u * kThreads + threadIdx.x;
-        kk[u] = t < c_begin ? key_of(t) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c0 + u * kThreads + (int)threadIdx.x < c_begin) {
-          gl += kk[u] > T;
-          el += kk[u] == T;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gl += __shfl_xor_sync(0xffffffffu, gl, o);
-      el += __shfl_xor_sync(0xffffffffu, el, o);
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) {
-      scan[warp] = gl;
-      hist[warp] = el;
-    }
-    __syncthreads();
-    for (int w = 0; w < kThreads / 32; ++w) {
-      gt_before += scan[w];
-      eq_before += hist[w];
-    }
-    __syncthreads();
+
+  griddep_wait();  // T, need_eq and the block counts come from the select kernel
+  const int32_t *wrow = a.ws + (size_t)row * a.ws_row;
+  const uint32_t T = (uint32_t)wrow[0];
+  const int need_eq = wrow[1];
+  int taken = n, eq_seen = 0;
+  if (c_begin < c_end) {
+    eq_seen = wrow[kWsHead + 2 * blk0 + 1];
+    taken = wrow[kWsHead + 2 * blk0] + min(eq_seen, need_eq);
   }
-  int taken = gt_before + min(eq_before, need_eq), eq_seen = eq_before;
   // rounds of kRound * kThreads positions, position c0 + u * kThreads + thread
   for (int c0 = c_begin; c0 < c_end && taken < n; c0 += kRound * kThreads) {
     bool gt[kRound], eq[kRound], sel[kRound];
+    float f[kRound];
 #pragma unroll
     for (int u = 0; u < kRound; ++u) {
       const int t = c0 + u * kThreads + threadIdx.x;
-      const uint32_t key = t < c_end ? key_of(t) : 0u;
+      f[u] = t < c_end ? srow[t] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+      const int t = c0 + u * kThreads + threadIdx.x;
+      const uint32_t key = float_key(f[u]);
       gt[u] = t < c_end && key > T;
       eq[u] = t < c_end && key == T;
     }
@@ -329,48 +533,110 @@ __global__ void __launch_bounds__(kThreads, 1) compact_topk_kernel(const Compact
 
 }  // namespace
 
+namespace {
+int64_t compact_ws_ints_per_row(int Nmax) { return kWsHead + 2 * (int64_t)((Nmax + kBlk - 1) / kBlk); }
+}  // namespace
+
+extern "C" int tg_compact_topk_workspace(int batch, int H, int Nmax, int64_t *workspace_bytes) {
+  if (!workspace_bytes) return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk_workspace: NULL output");
+  if (batch < 0 || H <= 0 || Nmax <= 0)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk_workspace: sizes must be positive");
+  *workspace_bytes = (int64_t)batch * H * compact_ws_ints_per_row(Nmax) * (int64_t)sizeof(int32_t);
+  return tgi::ok();
+}
+
 extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, int P, int d, int Nmax,
                                const int32_t *N, const float *scores, const uint16_t *K, const uint16_t *V,
                                const int32_t *head_order, const int32_t *ntok, const int64_t *pt_off,
                                const int32_t *pt_ids, int64_t pool_pages, uint16_t *pool, int32_t *kept_idx,
-                               int32_t *dev_status) {
+                               void *workspace, int64_t workspace_bytes, int32_t *dev_status) {
   if (batch < 0 || H <= 0 || H_p <= 0 || P <= 0 || d <= 0 || Nmax <= 0)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: sizes must be positive");
   if (H % H_p) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: H %% H_p != 0");
   if (P % 16 || d % 8 || d > 512) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: need P %% 16 == 0, d %% 8 == 0, d <= 512");
   if (batch == 0) return tgi::ok();
-  if (!N || !scores || !K || !V || !head_order || !ntok || !pt_off || !pt_ids || !pool)
+  if (!N || !scores || !K || !V || !head_order || !ntok || !pt_off || !pt_ids || !pool || !workspace)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: NULL pointer argument");
   if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(pool)) & 15)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: K, V and pool must be 16-byte aligned");
-  CompactArgs a;
-  a.N = N; a.scores = scores; a.K = K; a.V = V; a.head_order = head_order; a.ntok = ntok;
-  a.pt_off = pt_off; a.pt_ids = pt_ids; a.pool_pages = pool_pages; a.pool = pool; a.kept_idx = kept_idx;
-  a.status = dev_status; a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
-  // the keys of a row when they fit, else the select's candidate list (kSmemKeys entries)
-  const int smem = (Nmax <= kSmemKeys ? Nmax : kSmemKeys) * (int)sizeof(uint32_t);
+  if (reinterpret_cast<uintptr_t>(workspace) & 3)
+    return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: workspace must be 4-byte aligned");
+  const int rows = batch * H;
+  const int64_t ws_row = compact_ws_ints_per_row(Nmax);
+  if (workspace_bytes < (int64_t)rows * ws_row * (int64_t)sizeof(int32_t))
+    return tgi::fail(TG_ERR_CAPACITY, "tg_compact_topk: workspace of %lld bytes, %lld needed",
+                     (long long)workspace_bytes, (long long)((int64_t)rows * ws_row * 4));
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(compact_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
-  if (e == cudaSuccess) {
-    // CTAs per row: about two waves of one resident 1024-thread CTA per SM when a row's keys
-    // fit in shared memory (each CTA's select is then cheap), one wave when they are read
-    // from L2 (every CTA of a row repeats the select); at most 16, and chunks of at least
-    // 2048 tokens
-    const int rows = batch * H;
-    const int waves = Nmax <= kSmemKeys ? 2 : 1;
-    int parts = (waves * sms + rows - 1) / rows;
-    parts = std::max(1, std::min({parts, 16, (Nmax + 2047) / 2048}));
-    a.parts = parts;
-    a.rows = rows;
-    a.prop = parts > 1 && rows <= kPropRows;
-    // proportional shares take exactly the wanted waves (no partial wave at the end)
-    const int64_t grid = a.prop ? std::max<int64_t>(rows, (int64_t)waves * sms) : (int64_t)rows * parts;
-    if (grid > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
-    compact_topk_kernel<<<(unsigned)grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    e = cudaGetLastError();
-  }
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: %s", cudaGetErrorString(e));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int nblk = (Nmax + kBlk - 1) / kBlk;
+
+  // select: C CTAs per row, one cluster each.  As many as one wave of two CTAs per SM holds,
+  // more where the longest row's chunks would not fit the shared-memory key cache (up to
+  // kMaxCluster), and no CTA without a block of the longest row
+  SelectArgs sa;
+  sa.N = N; sa.scores = scores; sa.ntok = ntok; sa.ws = static_cast<int32_t *>(workspace); sa.status = dev_status;
+  sa.ws_row = ws_row; sa.H = H; sa.Nmax = Nmax;
+  sa.vec = (Nmax % 4 == 0) && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
+  {
+    const int fill = std::max(1, 2 * sms / rows);  // one wave of two CTAs per SM
+    const int fit = (int)(((int64_t)nblk * kBlk + kSelKeys - 1) / kSelKeys);
+    sa.C = std::max(1, std::min({std::max(fill, fit), kMaxCluster, nblk}));
+  }
+  if ((int64_t)rows * sa.C > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
+  {
+    const int smem = std::min(nblk * kBlk, kSelKeys) * (int)sizeof(uint32_t);
+    e = cudaFuncSetAttribute(compact_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelKeys * 4);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(rows * sa.C));
+      cfg.blockDim = dim3(kSelThreads);
+      cfg.dynamicSmemBytes = (size_t)smem;
+      cfg.stream = st;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = (unsigned)sa.C;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, compact_select_kernel, sa);
+    }
+  }
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: select: %s", cudaGetErrorString(e));
+
+  // copy: about two waves of one resident 1024-thread CTA per SM, shared among the rows in
+  // proportion to their work (or an even split of at most 16 CTAs per row past kPropRows
+  // rows), each CTA at least kMinBlocks blocks
+  CompactArgs a;
+  a.N = N; a.scores = scores; a.K = K; a.V = V; a.head_order = head_order; a.ntok = ntok;
+  a.pt_off = pt_off; a.pt_ids = pt_ids; a.ws = sa.ws; a.ws_row = ws_row; a.pool_pages = pool_pages;
+  a.pool = pool; a.kept_idx = kept_idx; a.status = dev_status;
+  a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
+  const int waves = 2;
+  int parts = (waves * sms + rows - 1) / rows;
+  parts = std::max(1, std::min({parts, 16, nblk / kMinBlocks}));
+  a.parts = parts;
+  a.rows = rows;
+  a.prop = parts > 1 && rows <= kPropRows;
+  // proportional shares take exactly the wanted waves (no partial wave at the end)
+  const int64_t grid = a.prop ? std::max<int64_t>(rows, (int64_t)waves * sms) : (int64_t)rows * parts;
+  if (grid > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: grid too large");
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, compact_copy_kernel, a);
+  }
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: copy: %s", cudaGetErrorString(e));
   return tgi::ok();
 }

@@ -1,5 +1,8 @@
-// Thin inline-PTX wrappers for sm_103a: mbarriers, TMA tensor loads, ldmatrix,
-// movmatrix, bf16 mma.sync and ex2.  Every wait here is bounded by a time limit.
+// Thin inline-PTX wrappers for sm_103a: mbarriers, TMA tensor loads, cluster barriers and
+// distributed shared memory, ldmatrix, movmatrix, bf16 mma.sync and ex2.  Every mbarrier wait
+// here is bounded by a time limit; a cluster barrier is a hardware barrier that completes
+// when every thread of the cluster's CTAs has arrived, which the kernels that use it do on
+// every path.
 #pragma once
 
 #include <cuda.h>
@@ -92,6 +95,35 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- thread-block clusters: rank, barrier and distributed shared memory
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster arrives (release: this CTA's shared-memory writes
+// become visible to the others) ...
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// ... an arrival that only says "done reading the others' shared memory"
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+// ... and waits for all of them (acquire)
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// shared-memory address `addr` of this CTA mapped to the same variable in CTA `rank`
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ---- programmatic dependent launch
 // allow the next grid in the stream to be scheduled as this grid's CTAs complete
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -145,6 +177,8 @@ __device__ __forceinline__ uint32_t float_key(float f) {
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// true for exactly the keys float_key gives a NaN (above +inf's key, or below -inf's)
+__device__ __forceinline__ bool is_nan_key(uint32_t k) { return k > 0xff800000u || k < 0x007fffffu; }
 // OR `bits` into an optional device status word
 __device__ __forceinline__ void report(int32_t *status, int32_t bits) {
   if (status) atomicOr(status, bits);

@@ -22,7 +22,7 @@ import numpy as np
 import torch
 
 from . import (tg_build_pages, tg_split_map, tg_query_ncta, tg_plan_decode, tg_decode_attn,
-               tg_compact_topk, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
+               tg_compact_topk, tg_compact_topk_workspace, tg_build_minmax, tg_page_score_topk, tg_page_score_workspace,
                tg_page_score_topk_rows, tg_rerank_rows, tg_plan_set_flags, PLAN_WAIT_TABLES,
                SCORE_LET_NEXT_START, tg_tier_promote, tg_compact_chunk, tg_compact_chunk_workspace,
                tg_sparse_layer)
@@ -57,6 +57,7 @@ class RaggedCache:
         self.plan_dev = torch.from_numpy(self.plan).to(dev)
         self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._compact_ws = {}  # tg_compact_topk's workspace, by Nmax
         self.pool = None
         if alloc_pool:
             self.pool = torch.empty(max(self.n_pages, 1) * H_p * 2 * P * d, dtype=torch.bfloat16, device=dev)
@@ -105,9 +106,14 @@ class RaggedCache:
     # ---- prefill: top-n retention into the pages
     def compact_layer(self, layer, scores, K, V, kept_idx=None, stream=None):
         Nmax = scores.shape[-1]
+        ws = self._compact_ws.get(Nmax)
+        if ws is None:
+            ws = torch.empty(tg_compact_topk_workspace(self.batch, self.H, Nmax), dtype=torch.uint8,
+                             device=self.device)
+            self._compact_ws = {Nmax: ws}  # one size at a time: the last Nmax used
         tg_compact_topk(self.batch, self.H, self.H_p, self.P, self.d, Nmax, self.N_dev, scores, K, V,
                         self.order_dev[layer], self.ntok_dev[layer], self.list_offsets(layer), self.pt_ids_dev,
-                        self.n_pages, self.pool, kept_idx=kept_idx, dev_status=self.status, stream=stream)
+                        self.n_pages, self.pool, ws, kept_idx=kept_idx, dev_status=self.status, stream=stream)
 
     def compact_layer_chunked(self, layer, scores, K, V, C, stream=None, chunks=None):
         """Retention fused into chunked prefill (tg_compact_chunk): the prompt's scores and K/V
