@@ -45,9 +45,16 @@ constexpr int kBlk = 1024;  // positions per block of the prefix-count table
 // ---------------------------------------------------------------- select --
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelKeys = 24576;  // keys of a chunk held in shared memory (96 KB, two CTAs per SM); the rest are re-read from L2
+constexpr int kSelKeys = 22528;  // keys of a chunk held in shared memory (88 KB, two CTAs per SM); the rest are re-read from L2
+constexpr int kSelBlocks = kSelKeys / kBlk;  // blocks held in shared memory
+constexpr int kPiece = 4096;                 // keys per bulk copy (16 KB)
+constexpr int kPieces = (kSelKeys + kPiece - 1) / kPiece;
+constexpr int kBits0 = 12, kBits1 = 10;      // digit widths: 12, 10, 10 bits from the top
+constexpr int kBins0 = 1 << kBits0, kBins1 = 1 << kBits1;
 constexpr int kMaxCluster = 8;
 constexpr int kWsHead = 4;  // workspace row: T, need_eq, 2 unused, then (keys > T, keys == T) before each block
+constexpr uint64_t kCopyWaitNs = 2000000000ull;  // give up a copy wait after 2 s
+static_assert(kSelBlocks < 32 && kSelKeys % kBlk == 0 && kBins1 == 2 * kSelThreads, "select layout");
 
 struct SelectArgs {
   const int32_t *N;
@@ -57,17 +64,20 @@ struct SelectArgs {
   int32_t *status;
   int64_t ws_row;  // ints per workspace row
   int H, Nmax, C;  // C: CTAs per cluster (one cluster per row)
-  int vec;         // score rows start 16-byte aligned: chunks load as float4
+  int vec;         // score rows start 16-byte aligned: chunks arrive by bulk copies
 };
 
 __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const SelectArgs a) {
-  extern __shared__ uint32_t keys[];  // the first kSelKeys keys of this CTA's chunk
-  __shared__ int hist[2][256];        // this CTA's digit counts, alternating between passes
-  __shared__ int tot[256], low[256];  // the cluster's counts, and those of the lower ranks
+  extern __shared__ __align__(128) uint32_t keys[];  // the first kSelKeys keys of this CTA's chunk
+  __shared__ __align__(16) int hist_a[kBins0];        // digit counts of passes 0 and 2
+  __shared__ __align__(16) int hist_b[kBins1];        // of pass 1, later the per-block counts
+  __shared__ int sup_buf[2][256];           // this CTA's super-digit counts, alternating between passes
+  __shared__ int wtot[2][kSelWarps];
   __shared__ int pick[4];
-  __shared__ int bcnt[2][kSelThreads];  // per block of a group: keys > T, keys == T
-  __shared__ int wsum[2][kSelWarps];
+  __shared__ int nc[kSelBlocks], gt0[kSelBlocks], coff[kSelBlocks + 1];  // candidates per cached block
+  __shared__ __align__(8) uint64_t bars[kPieces];
   __shared__ int err;
+  int(&bcnt)[2][kSelThreads] = *reinterpret_cast<int(*)[2][kSelThreads]>(hist_b);
 
   const int C = a.C, rank = (int)cluster_ctarank(), row = blockIdx.x / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -78,155 +88,290 @@ __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const Se
   const int nbr = (Nb + kBlk - 1) / kBlk;
   const int blk0 = (int)((int64_t)rank * nbr / C), blk1 = (int)((int64_t)(rank + 1) * nbr / C);
   const int p0 = blk0 * kBlk, cnt = max(0, min(blk1 * kBlk, Nb) - p0);
-  const int cached = min(cnt, kSelKeys);
+  const int cached = min(cnt, kSelKeys), ncb = (cached + kBlk - 1) / kBlk;
   const float *src = a.scores + (size_t)row * a.Nmax + p0;
-  auto key_at = [&](int i) -> uint32_t { return i < cached ? keys[i] : float_key(src[i]); };
+  const int nbulk = a.vec ? (cached & ~3) : 0;  // keys that arrive by bulk copies
+  const int npieces = (nbulk + kPiece - 1) / kPiece;
 
-  for (int i = tid; i < 2 * 256; i += kSelThreads) (&hist[0][0])[i] = 0;
-  if (tid == 0) err = 0;
+  if (tid == 0) {
+    err = 0;
+    for (int i = 0; i < npieces; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  for (int i = tid; i < kBins0; i += kSelThreads) hist_a[i] = 0;
+  for (int i = tid; i < kBins1; i += kSelThreads) hist_b[i] = 0;
   __syncthreads();
+  if (tid == 0)
+    for (int i = 0; i < npieces; ++i) {
+      const int k0 = i * kPiece, nk = min(kPiece, nbulk - k0);
+      mbar_arrive_expect_tx(&bars[i], (uint32_t)nk * 4u);
+      bulk_load(keys + k0, src + k0, (uint32_t)nk * 4u, &bars[i]);
+    }
 
-  // load the chunk (two float4 loads in flight per thread), check for NaN, and count the
-  // first digit (a warp's equal top bytes, which coincide for real scores, add once)
+  // first digit (the top 12 bits: sign, exponent and three mantissa bits, which spread real
+  // scores over many counters) of every key, counted while the chunk arrives; NaN checked
+  constexpr int kShift0 = 32 - kBits0;
   bool nan_seen = false;
-  auto count_top = [&](uint32_t key, bool valid) {
-    const uint32_t dg = valid ? key >> 24 : 256u;
-    const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-    if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[0][dg], __popc(peers));
-  };
-  const int nv = a.vec ? cnt >> 2 : 0;  // float4 groups
-  for (int base = 0; base < nv; base += 2 * kSelThreads) {
-    float4 f[2];
+  // keys past the bulk copies: the cached tail, then the part of the chunk read from L2
+  for (int i = nbulk + tid; i < cached; i += kSelThreads) {
+    const uint32_t k = float_key(src[i]);
+    nan_seen |= is_nan_key(k);
+    keys[i] = k;
+    atomicAdd(&hist_a[k >> kShift0], 1);
+  }
+  for (int base = cached; base < cnt; base += 4 * kSelThreads) {
+    uint32_t kk[4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int g = base + u * kSelThreads + tid;
-      f[u] = g < nv ? __ldg(reinterpret_cast<const float4 *>(src) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * kSelThreads + tid;
+      kk[u] = i < cnt ? float_key(src[i]) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int g = base + u * kSelThreads + tid;
-      const bool valid = g < nv;
-      const uint4 k = make_uint4(float_key(f[u].x), float_key(f[u].y), float_key(f[u].z), float_key(f[u].w));
-      if (valid) {
-        nan_seen |= is_nan_key(k.x) | is_nan_key(k.y) | is_nan_key(k.z) | is_nan_key(k.w);
-        if (4 * g < cached) *reinterpret_cast<uint4 *>(keys + 4 * g) = k;
+    for (int u = 0; u < 4; ++u)
+      if (base + u * kSelThreads + tid < cnt) {
+        nan_seen |= is_nan_key(kk[u]);
+        atomicAdd(&hist_a[kk[u] >> kShift0], 1);
       }
-      count_top(k.x, valid);
-      count_top(k.y, valid);
-      count_top(k.z, valid);
-      count_top(k.w, valid);
+  }
+  // the bulk-copied pieces, turned into keys in place as each one lands
+  bool timed_out = false;
+  for (int i = 0; i < npieces; ++i) {
+    if (!mbar_wait(&bars[i], 0, kCopyWaitNs)) timed_out = true;
+    const int g0 = i * kPiece / 4, ng = min(kPiece, nbulk - i * kPiece) / 4;
+    uint4 *k4 = reinterpret_cast<uint4 *>(keys);
+    for (int g = tid; g < ng; g += kSelThreads) {
+      uint4 k = k4[g0 + g];
+      k.x = float_key(__uint_as_float(k.x));
+      k.y = float_key(__uint_as_float(k.y));
+      k.z = float_key(__uint_as_float(k.z));
+      k.w = float_key(__uint_as_float(k.w));
+      nan_seen |= is_nan_key(k.x) | is_nan_key(k.y) | is_nan_key(k.z) | is_nan_key(k.w);
+      k4[g0 + g] = k;
+      atomicAdd(&hist_a[k.x >> kShift0], 1);
+      atomicAdd(&hist_a[k.y >> kShift0], 1);
+      atomicAdd(&hist_a[k.z >> kShift0], 1);
+      atomicAdd(&hist_a[k.w >> kShift0], 1);
     }
   }
-  for (int base = 4 * nv; base < cnt; base += kSelThreads) {
-    const int i = base + tid;
-    const bool valid = i < cnt;
-    const uint32_t k = valid ? float_key(src[i]) : 0u;
-    if (valid) {
-      nan_seen |= is_nan_key(k);
-      if (i < cached) keys[i] = k;
-    }
-    count_top(k, valid);
-  }
-  if (nan_seen) err = 1;
+  if (nan_seen) atomicOr(&err, 1);
+  if (timed_out) atomicOr(&err, 2);
   __syncthreads();
-  if (err && tid == 0) report(a.status, TG_STATUS_NONFINITE);
+  if (tid == 0 && (err & 1)) report(a.status, TG_STATUS_NONFINITE);
+  if (tid == 0 && (err & 2)) report(a.status, TG_STATUS_TIMEOUT);
 
   uint32_t prefix = 0, mask = 0;
   int k_rem = n, gt_lo = 0, eq_lo = 0;
-  for (int p = 0; p < 4; ++p) {
-    const int shift = 24 - 8 * p;
-    int *h = hist[p & 1];
-    if (p > 0) {
-      // digit p of the keys that match the digits chosen so far (this buffer was last read
-      // by the other CTAs before they arrived at the previous pass's barrier)
-      if (p > 1) {
-        for (int i = tid; i < 256; i += kSelThreads) h[i] = 0;
-        __syncthreads();
-      }
-      for (int base = 0; base < cnt; base += 4 * kSelThreads) {
-        uint32_t kk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = base + u * kSelThreads + tid;
-          kk[u] = i < cnt ? key_at(i) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (base + u * kSelThreads + tid < cnt && (kk[u] & mask) == prefix) atomicAdd(&h[(kk[u] >> shift) & 255u], 1);
-      }
-      __syncthreads();
-    }
-    cluster_arrive();  // this pass's histograms are complete in every CTA ...
-    cluster_wait();
+  // One pass's digit over the cluster, in two steps that read only what every CTA wrote
+  // before the cluster barrier: its 256 super-digit counts (sums of S = bins/256 adjacent
+  // digits), and then, inside the chosen super-digit, its S digit counts.  Each step adds up
+  // the counts over the cluster and over the lower ranks and scans from the top down for the
+  // one that holds the k_rem-th key.
+  auto reduce_pick = [&](int *h, int bins, int shift, int bits, int pass) {
+    const int S = bins / 256;
+    int *sup = sup_buf[pass & 1];  // (the other CTAs read the other buffer until the previous barrier)
+    __syncthreads();               // this CTA's counts of the pass are complete
     if (tid < 256) {
-      // ... and each thread adds up one digit over the cluster
+      int t = 0;
+      for (int i = 0; i < S; i += 4) {
+        const int4 x = *reinterpret_cast<const int4 *>(&h[tid * S + i]);
+        t += x.x + x.y + x.z + x.w;
+      }
+      sup[tid] = t;
+    }
+    cluster_arrive();  // also orders this CTA's own threads
+    cluster_wait();
+    int s = 0, l = 0;
+    if (tid < 256) {
+      const uint32_t addr = smem_addr(&sup[255 - tid]);
       int v[kMaxCluster];
-      const uint32_t addr = smem_addr(&h[tid]);
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) v[r] = r == rank ? h[tid] : ld_cluster_s32(cluster_map(addr, (uint32_t)r));
-      int s = 0, l = 0;
+        if (r < C) v[r] = r == rank ? sup[255 - tid] : ld_cluster_s32(cluster_map(addr, (uint32_t)r));
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
         if (r < C) {
           s += v[r];
           if (r < rank) l += v[r];
         }
-      tot[tid] = s;
-      low[tid] = l;
+    }
+    int is = s, il = l;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, is, o), y = __shfl_up_sync(0xffffffffu, il, o);
+      if (lane >= o) {
+        is += x;
+        il += y;
+      }
+    }
+    if (tid < 256 && lane == 31) {
+      wtot[0][warp] = is;
+      wtot[1][warp] = il;
+    }
+    if (tid == 0) pick[0] = pick[1] = pick[2] = pick[3] = 0;  // (in range whatever the counts)
+    __syncthreads();
+    if (tid < 256) {
+      int bs = 0, bl = 0;
+      for (int w = 0; w < warp; ++w) {
+        bs += wtot[0][w];
+        bl += wtot[1][w];
+      }
+      const int above = bs + is - s;  // keys in the super-digits above this one
+      if (above < k_rem && k_rem <= above + s) {
+        pick[0] = 255 - tid;
+        pick[1] = above;
+        pick[2] = bl + il - l;  // the lower ranks' keys in the super-digits above
+      }
     }
     __syncthreads();
     if (warp == 0) {
-      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down for the digit
-      // that holds the k_rem-th key, and count the lower ranks' keys in the digits above it
-      int lt[8], ll[8], st = 0, sl = 0;
+      // lane u (< S) holds digit sd*S + S-1-u of the chosen super-digit sd
+      const int sd = pick[0], above0 = pick[1], above_l0 = pick[2];
+      int s2 = 0, l2 = 0;
+      if (lane < S) {
+        const int dg = sd * S + S - 1 - lane;
+        const uint32_t addr = smem_addr(&h[dg]);
+        int v[kMaxCluster];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        lt[t] = tot[255 - 8 * lane - t];
-        ll[t] = low[255 - 8 * lane - t];
-        st += lt[t];
-        sl += ll[t];
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < C) v[r] = r == rank ? h[dg] : ld_cluster_s32(cluster_map(addr, (uint32_t)r));
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < C) {
+            s2 += v[r];
+            if (r < rank) l2 += v[r];
+          }
       }
-      int inc = st, incl = sl;
+      int is2 = s2, il2 = l2;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, o), w = __shfl_up_sync(0xffffffffu, incl, o);
+        const int x = __shfl_up_sync(0xffffffffu, is2, o), y = __shfl_up_sync(0xffffffffu, il2, o);
         if (lane >= o) {
-          inc += v;
-          incl += w;
+          is2 += x;
+          il2 += y;
         }
       }
-      const int before = inc - st;
-      if (before < k_rem && k_rem <= inc) {
-        int above = before, above_l = incl - sl;
-        bool found = false;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (!found && above + lt[t] >= k_rem) {
-            found = true;
-            pick[0] = 255 - 8 * lane - t;
-            pick[1] = above;
-            pick[2] = above_l;
-            pick[3] = ll[t];
-          }
-          if (!found) {
-            above += lt[t];
-            above_l += ll[t];
-          }
-        }
+      const int above = above0 + is2 - s2;
+      __syncwarp();
+      if (lane < S && above < k_rem && k_rem <= above + s2) {
+        pick[0] = sd * S + S - 1 - lane;
+        pick[1] = above;
+        pick[2] = above_l0 + il2 - l2;
+        pick[3] = l2;
       }
     }
     __syncthreads();
     prefix |= (uint32_t)pick[0] << shift;
-    mask |= 255u << shift;
+    mask |= ((1u << bits) - 1u) << shift;
     k_rem -= pick[1];
     gt_lo += pick[2];
     eq_lo = pick[3];
+  };
+  reduce_pick(hist_a, kBins0, kShift0, kBits0, 0);
+
+  // Candidates: a warp takes one cached block, half a block at a time into registers (16
+  // keys a lane), counts its keys above the chosen first digit (all of them > T) and writes
+  // those with that digit to the front of the block, over keys already read (their order
+  // inside the block does not matter to any count).
+  const uint32_t d0 = prefix >> kShift0;
+  for (int j = warp; j < ncb; j += kSelWarps) {
+    const int q0 = j * kBlk, len = min(kBlk, cached - q0);
+    int m = 0, g = 0;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      const int h0 = half * (kBlk / 2);
+      uint32_t kv[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = h0 + 4 * (lane + 32 * u);
+        if (i + 3 < len) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(&keys[q0 + i]);
+          kv[4 * u] = x.x; kv[4 * u + 1] = x.y; kv[4 * u + 2] = x.z; kv[4 * u + 3] = x.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kv[4 * u + e] = i + e < len ? keys[q0 + i + e] : 0u;
+        }
+      }
+      int mh = 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const bool v = h0 + 4 * (lane + 32 * (u / 4)) + (u % 4) < len;
+        mh += v && (kv[u] >> kShift0) == d0;
+        g += v && (kv[u] >> kShift0) > d0;
+      }
+      int inc = mh;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += x;
+      }
+      __syncwarp();  // every lane holds its keys before any is overwritten
+      int at = q0 + m + inc - mh;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const bool v = h0 + 4 * (lane + 32 * (u / 4)) + (u % 4) < len;
+        if (v && (kv[u] >> kShift0) == d0) keys[at++] = kv[u];
+      }
+      m += __shfl_sync(0xffffffffu, inc, 31);
+      __syncwarp();
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+    if (lane == 0) {
+      nc[j] = m;
+      gt0[j] = g;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // start of each block's candidates in one flat numbering
+    const int v = lane < ncb ? nc[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += x;
+    }
+    if (lane == 0) coff[0] = 0;
+    if (lane < kSelBlocks) coff[lane + 1] = inc;
+  }
+  __syncthreads();
+  const int ncand = coff[ncb];
+
+  // digits 2 and 3 (10 bits each) over the candidates, and over the keys past the cache
+  for (int p = 1; p < 3; ++p) {
+    const int shift = kShift0 - kBits1 * p;
+    int *h = p == 1 ? hist_b : hist_a;
+    if (p == 2) {
+      // (the other CTAs last read this buffer before they arrived at the previous barrier)
+      for (int i = tid; i < kBins1; i += kSelThreads) h[i] = 0;
+      __syncthreads();
+    }
+    int j = 0;
+    for (int i = tid; i < ncand; i += kSelThreads) {
+      while (coff[j + 1] <= i) ++j;
+      const uint32_t k = keys[j * kBlk + i - coff[j]];
+      if ((k & mask) == prefix) atomicAdd(&h[(k >> shift) & (kBins1 - 1)], 1);
+    }
+    for (int base = cached; base < cnt; base += 4 * kSelThreads) {
+      uint32_t kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kSelThreads + tid;
+        kk[u] = i < cnt ? float_key(src[i]) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (base + u * kSelThreads + tid < cnt && (kk[u] & mask) == prefix)
+          atomicAdd(&h[(kk[u] >> shift) & (kBins1 - 1)], 1);
+    }
+    reduce_pick(h, kBins1, shift, kBits1, p);
   }
   cluster_arrive_relaxed();  // done reading the other CTAs' histograms
 
-  // per block of the chunk: keys > T and == T before it (a warp counts one block; groups of
-  // kSelThreads blocks are scanned one after another)
+  // per block of the chunk: keys > T and == T before it (a warp counts one block: a cached
+  // block from its candidates and its count above the first digit, another from L2; groups of
+  // kSelThreads blocks are scanned one after another).  The counts go where the pass-1
+  // digits were, which no other CTA reads after the last barrier.
   const uint32_t T = prefix;
   int32_t *wrow = a.ws + (size_t)row * a.ws_row;
   if (rank == 0 && tid == 0) {
@@ -237,13 +382,22 @@ __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const Se
   int carry_gt = gt_lo, carry_eq = eq_lo;
   for (int g0 = 0; g0 < nloc; g0 += kSelThreads) {
     const int ng = min(kSelThreads, nloc - g0);
-    for (int j = warp; j < ng; j += kSelWarps) {
-      const int q0 = (g0 + j) * kBlk, q1 = min(q0 + kBlk, cnt);
+    for (int jj = warp; jj < ng; jj += kSelWarps) {
+      const int j = g0 + jj;
       int gt = 0, eq = 0;
-      for (int i = q0 + lane; i < q1; i += 32) {
-        const uint32_t k = key_at(i);
-        gt += k > T;
-        eq += k == T;
+      if (j < ncb) {
+        for (int i = lane; i < nc[j]; i += 32) {
+          const uint32_t k = keys[j * kBlk + i];
+          gt += k > T;
+          eq += k == T;
+        }
+      } else {
+        const int q1 = min(j * kBlk + kBlk, cnt);
+        for (int i = j * kBlk + lane; i < q1; i += 32) {
+          const uint32_t k = float_key(src[i]);
+          gt += k > T;
+          eq += k == T;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -251,8 +405,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const Se
         eq += __shfl_xor_sync(0xffffffffu, eq, o);
       }
       if (lane == 0) {
-        bcnt[0][j] = gt;
-        bcnt[1][j] = eq;
+        bcnt[0][jj] = gt + (j < ncb ? gt0[j] : 0);
+        bcnt[1][jj] = eq;
       }
     }
     __syncthreads();
@@ -267,19 +421,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const Se
       }
     }
     if (lane == 31) {
-      wsum[0][warp] = ig;
-      wsum[1][warp] = ie;
+      wtot[0][warp] = ig;
+      wtot[1][warp] = ie;
     }
     __syncthreads();
     int bg = 0, be = 0, tg = 0, te = 0;
 #pragma unroll
     for (int w = 0; w < kSelWarps; ++w) {
       if (w < warp) {
-        bg += wsum[0][w];
-        be += wsum[1][w];
+        bg += wtot[0][w];
+        be += wtot[1][w];
       }
-      tg += wsum[0][w];
-      te += wsum[1][w];
+      tg += wtot[0][w];
+      te += wtot[1][w];
     }
     if (tid < ng) {
       wrow[kWsHead + 2 * (blk0 + g0 + tid)] = carry_gt + bg + ig - vg;
@@ -573,15 +727,15 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int nblk = (Nmax + kBlk - 1) / kBlk;
 
-  // select: C CTAs per row, one cluster each.  As many as one wave of two CTAs per SM holds,
-  // more where the longest row's chunks would not fit the shared-memory key cache (up to
-  // kMaxCluster), and no CTA without a block of the longest row
+  // select: C CTAs per row, one cluster each, and no CTA without a block of the longest row
   SelectArgs sa;
   sa.N = N; sa.scores = scores; sa.ntok = ntok; sa.ws = static_cast<int32_t *>(workspace); sa.status = dev_status;
   sa.ws_row = ws_row; sa.H = H; sa.Nmax = Nmax;
   sa.vec = (Nmax % 4 == 0) && (reinterpret_cast<uintptr_t>(scores) & 15) == 0;
   {
-    const int fill = std::max(1, 2 * sms / rows);  // one wave of two CTAs per SM
+    // one wave of two CTAs per SM, but at most 4 CTAs (the cluster's counts are read by every
+    // CTA) unless more are needed for the chunks to fit
+    const int fill = std::max(1, std::min(4, 2 * sms / rows));
     const int fit = (int)(((int64_t)nblk * kBlk + kSelKeys - 1) / kSelKeys);
     sa.C = std::max(1, std::min({std::max(fill, fit), kMaxCluster, nblk}));
   }
@@ -607,15 +761,17 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
   }
   if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_compact_topk: select: %s", cudaGetErrorString(e));
 
-  // copy: about two waves of one resident 1024-thread CTA per SM, shared among the rows in
+  // copy: six waves of one resident 1024-thread CTA per SM, shared among the rows in
   // proportion to their work (or an even split of at most 16 CTAs per row past kPropRows
-  // rows), each CTA at least kMinBlocks blocks
+  // rows), each CTA at least kMinBlocks blocks.  A CTA has no fixed cost to speak of (the
+  // select is done), so finer shares balance rows of very different length: two waves
+  // measured 2.11 ms per layer of 256 rows of 4K-64K tokens, six 1.38 ms
   CompactArgs a;
   a.N = N; a.scores = scores; a.K = K; a.V = V; a.head_order = head_order; a.ntok = ntok;
   a.pt_off = pt_off; a.pt_ids = pt_ids; a.ws = sa.ws; a.ws_row = ws_row; a.pool_pages = pool_pages;
   a.pool = pool; a.kept_idx = kept_idx; a.status = dev_status;
   a.H = H; a.H_p = H_p; a.G = H / H_p; a.P = P; a.d = d; a.Nmax = Nmax;
-  const int waves = 2;
+  const int waves = 6;
   int parts = (waves * sms + rows - 1) / rows;
   parts = std::max(1, std::min({parts, 16, nblk / kMinBlocks}));
   a.parts = parts;
