@@ -813,6 +813,7 @@ def bench_tiered(args, w, q, mms, pools, out, stream, device, layers=4, steps=32
         fill = int(sum(int(t.promoted.item()) for t in tiers))
         ms = run(mode == "tiered", list(range(1, steps)))
         res[mode] = {"ms_per_step": statistics.mean(ms) / L * w.L,  # scaled to the 32-layer model
+                     "max_ms_per_step": max(ms) / L * w.L,
                      "ms_per_layer_step": statistics.mean(ms) / L,
                      "rerank_step_ms_per_layer": statistics.mean(ms[period - 1::period]) / L,
                      "other_step_ms_per_layer": statistics.mean([m for i, m in enumerate(ms, 1) if i % period]) / L}
@@ -832,12 +833,79 @@ def bench_tiered(args, w, q, mms, pools, out, stream, device, layers=4, steps=32
                 "dense_kv_bytes_per_layer": tiers[0].dense_kv_bytes()})
             res["tiered"]["gpu_kv_saved_pct"] = 100 * (1 - res["tiered"]["gpu_kv_bytes_per_layer"]
                                                        / res["tiered"]["dense_kv_bytes_per_layer"])
+    res["reload_schedule"] = bench_reload_schedule(w, qs, mms, pools, out, tiers, flat, unstable[:L], L, steps,
+                                                   period, device)
     for t in tiers:
         tg_status = t.status
         __import__("non_uniform_paged_gb300").tg_check_status(tg_status)
     del tiers, flat
     torch.cuda.empty_cache()
     return res
+
+
+def bench_reload_schedule(w, qs, mms, pools, out, tiers, flat, unstable, L, steps, period, device, grid_limit=0):
+    """The page's reload schedule for tiered placement ([FlexiCache] FlexiCache Scheduler, KV
+    transfer): stable heads re-rank one request phase per step (stagger 1).  A reloading
+    request's promoted pages come from host on a low-priority stream, by 64-thread CTAs that
+    stay resident beside the decode's (one per promoted row; grid_limit > 0 caps them), while
+    only that request pauses; the rest of the batch decodes on a high-priority stream.  Against the same schedule with every page on the GPU (no pause).  Reports ms per
+    step (scaled to the model's layers), requests decoded per step and their rate."""
+    from non_uniform_paged_gb300.ragged import RerankSchedule
+    sched = RerankSchedule(unstable, w.batch, period=period, stagger=1, device=device)
+    hi = torch.cuda.Stream(priority=-1)  # CUDA stream priorities: lower number, higher priority
+    lo = torch.cuda.Stream(priority=0)
+    for t in tiers:
+        t.reload_schedule(period)
+
+    def run(tiered_mode):
+        for l, t in enumerate(tiers):  # step 0: every row re-ranked, every stable block filled
+            t.load(pools[l])
+            if tiered_mode:
+                t.rerank(qs[l][0], mms[l], stream=hi)
+            else:
+                flat.select(qs[l][0], mms[l], stream=hi, layer=l)
+        torch.cuda.synchronize()
+        for t in tiers:
+            t.promoted.zero_()
+        torch.cuda.synchronize()
+        timed = list(range(1, steps))
+        ev = _events(2 * len(timed))
+        decoded = []
+        for i, st in enumerate(timed):
+            ev[2 * i].record(hi)
+            paused = np.zeros(w.batch, bool)
+            for l in range(L):
+                rows, n = sched.rows(l, st)
+                if tiered_mode:
+                    paused = tiers[l].step_reload(qs[l][st], mms[l], rows, n, st, out, hi, lo, grid_limit=grid_limit)
+                else:
+                    flat.select_rows(qs[l][st], mms[l], rows, n, stream=hi, layer=l)
+                    flat.attend(qs[l][st], pools[l], out, stream=hi, layer=l)
+            if tiered_mode and i == len(timed) - 1:
+                for t in tiers:  # the last fetches belong to the timed work
+                    if t._fetch_done is not None:
+                        hi.wait_event(t._fetch_done)
+            ev[2 * i + 1].record(hi)
+            decoded.append(w.batch - int(paused.sum()))
+        torch.cuda.synchronize()
+        ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(timed))]
+        per_step = statistics.mean(ms) / L * w.L
+        return {"ms_per_step": per_step, "max_ms_per_step": max(ms) / L * w.L,
+                "requests_decoded_per_step": statistics.mean(decoded),
+                "tokens_per_s": statistics.mean(decoded) / (per_step * 1e-3),
+                "promoted_pages_per_step": sum(int(t.promoted.item()) for t in tiers) / len(timed) / L}
+
+    gpu = run(False)
+    tiered = run(True)
+    return {"period": period, "stagger": 1, "fetch_ctas": "one 64-thread CTA per promoted row" if grid_limit <= 0
+            else f"at most {grid_limit} 64-thread CTAs", "layers_timed": L,
+            "timing": "ms per step of the layers timed, scaled to the model's layers; fetch on a low-priority "
+                      "stream, decode on a high-priority one",
+            "all_gpu": {k: v for k, v in gpu.items() if k != "promoted_pages_per_step"}, "tiered": tiered,
+            "fetch_grid": "a cap of 8-64 CTAs measured 1.1-3.1x slower per step: the host link then keeps too "
+                          "few reads in flight and the decode waits for the fetch",
+            "host_bytes_per_step_per_layer": tiered["promoted_pages_per_step"] * 2 * w.P * w.d * 2,
+            "tiered_vs_all_gpu_tokens": tiered["tokens_per_s"] / gpu["tokens_per_s"]}
 
 
 def report_pages(args):

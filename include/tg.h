@@ -478,6 +478,21 @@ int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int gri
                     const void *host_kv, int page_bytes, void *pool, int64_t pool_pages,
                     int32_t *pt_ids, int64_t *promoted, int32_t *dev_status);
 
+/* tg_tier_promote_background -- tg_tier_promote (same arguments, same results) for a
+ *   copy that runs on a low-priority stream while decoding continues on another:
+ *   [FlexiCache] "FlexiCache Scheduler" (a reloading request pauses, the rest of the
+ *   batch decodes) and "KV transfer" (a low-priority background stream, a limited
+ *   grid).  Its CTAs have 64 threads, at most 64 registers each and 16 KB of shared
+ *   memory, so one stays resident beside a decode or page-score CTA on the same SM
+ *   instead of holding the SM while it waits on the host link.  The caller orders
+ *   it after the scores of the rows it promotes (an event), and the decode of those
+ *   rows after it. */
+int tg_tier_promote_background(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
+                               const uint8_t *unstable, int batch, int H, int n_pages, int K,
+                               const int32_t *sel, int32_t *slot_page, const int32_t *slot_block,
+                               const int64_t *dense_base, const void *host_kv, int page_bytes, void *pool,
+                               int64_t pool_pages, int32_t *pt_ids, int64_t *promoted, int32_t *dev_status);
+
 /* ------------------------------------------------------------------ f2 ---
  * Page allocator for budget reservation.  [Tangram] 3.1 Budget Reservation: a
  * request's compressed footprint is fixed when it is scheduled, so its pages

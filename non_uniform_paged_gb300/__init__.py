@@ -22,7 +22,7 @@ __all__ = ["TGError", "load", "tg_build_pages", "tg_split_map", "tg_query_ncta",
            "tg_decode_attn", "tg_decode_attn_static_scratch", "tg_compact_topk", "tg_compact_topk_workspace", "tg_build_minmax", "tg_page_score_topk",
            "tg_page_score_workspace", "tg_page_score_topk_rows", "tg_rerank_rows", "tg_plan_set_flags",
            "PLAN_WAIT_TABLES", "SCORE_LET_NEXT_START", "PageAllocator",
-           "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
+           "tg_sparse_layer", "tg_compact_chunk", "tg_compact_chunk_workspace", "tg_tier_promote", "tg_tier_promote_background", "tg_alloc_state_bytes", "tg_alloc_init", "tg_alloc_admit", "tg_alloc_release", "tg_alloc_query",
            "tg_check_status", "tg_version", "plan_header", "plan_items", "plan_lead", "WORK_ITEM_DTYPE",
            "STATUS_NONFINITE", "STATUS_BAD_PAGE", "STATUS_TIMEOUT", "STATUS_BAD_INPUT", "ERR_INVALID_ARG",
            "ERR_SHAPE", "ERR_NONFINITE", "ERR_CAPACITY", "ERR_CUDA", "ERR_TIMEOUT", "ERR_DEVICE"]
@@ -61,6 +61,8 @@ _SIGS = {
                               _P, _L, _P]),
     "tg_compact_chunk_workspace": (_I, [_I, _I, _I, _P]),
     "tg_tier_promote": (_I, [_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _L, _P, _P, _P]),
+    "tg_tier_promote_background": (_I, [_P, _I, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _L, _P, _P,
+                                        _P]),
     "tg_alloc_state_bytes": (_I, [_L, _P]),
     "tg_alloc_init": (_I, [_P, _L, _L]),
     "tg_alloc_admit": (_I, [_P, _I, _P, _P, _L, _P]),
@@ -408,20 +410,30 @@ def tg_rerank_rows(unstable, batch, layer, step, period=16, stagger=0) -> np.nda
 
 
 def tg_tier_promote(rows, n_rows, unstable, batch, H, n_pages, K, sel, slot_page, slot_block, dense_base, host_kv,
-                    page_bytes, pool, pt_ids, promoted=None, dev_status=None, grid_limit=0, stream=None):
+                    page_bytes, pool, pt_ids, promoted=None, dev_status=None, grid_limit=0, stream=None,
+                    background=False):
     """Fetch promoted pages of stable heads from pinned host memory into freed GPU blocks and
-    build the decode lists (tg.h: tg_tier_promote).  host_kv is a pinned CPU tensor."""
+    build the decode lists (tg.h: tg_tier_promote; background: tg_tier_promote_background, small
+    CTAs that stay resident beside a decode).  host_kv is a pinned CPU tensor."""
     import torch
     if not (isinstance(host_kv, torch.Tensor) and host_kv.device.type == "cpu" and host_kv.is_pinned()):
         raise TypeError("host_kv must be a pinned CPU torch.Tensor")
     pool_pages = pool.numel() * pool.element_size() // page_bytes
-    _check(load().tg_tier_promote(_stream(stream), int(n_rows), _dev(rows, torch.int32, "rows"), int(grid_limit),
+    fn = load().tg_tier_promote_background if background else load().tg_tier_promote
+    _check(fn(_stream(stream), int(n_rows), _dev(rows, torch.int32, "rows"), int(grid_limit),
                                   _dev(unstable, torch.uint8, "unstable"), batch, H, n_pages, K,
                                   _dev(sel, torch.int32, "sel"), _dev(slot_page, torch.int32, "slot_page"),
                                   _dev(slot_block, torch.int32, "slot_block"),
                                   _dev(dense_base, torch.int64, "dense_base"), host_kv.data_ptr(), int(page_bytes),
                                   _dev(pool, None, "pool"), int(pool_pages), _dev(pt_ids, torch.int32, "pt_ids"),
                                   _dev(promoted, torch.int64, "promoted"), _dev(dev_status, torch.int32, "dev_status")))
+
+
+def tg_tier_promote_background(*args, **kw):
+    """tg_tier_promote with small CTAs for a copy on a background stream (tg.h:
+    tg_tier_promote_background); the arguments of tg_tier_promote."""
+    kw["background"] = True
+    return tg_tier_promote(*args, **kw)
 
 
 def tg_alloc_state_bytes(n_pages: int) -> int:

@@ -27,7 +27,6 @@ namespace {
 
 using namespace tgk;
 
-constexpr int kThreads = 256;
 constexpr int kMaxTierPages = 16384;  // pages per row the shared-memory bitmaps cover
 constexpr int kMaxTierK = 1024;
 
@@ -48,9 +47,21 @@ struct TierArgs {
   int32_t *pt_ids;            // [total][K] decode lists (output)
   int64_t *promoted;          // [1] pages copied (optional, accumulated)
   int32_t *status;
+  int slices;                 // copy units per row (kCopy)
 };
 
-__global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a) {
+// What a launch of the kernel does with each listed row
+constexpr int kWhole = 0;   // lists, copy, new block table and decode list
+constexpr int kCopy = 1;    // lists and 1/slices of the copy (the row's state is not changed)
+constexpr int kCommit = 2;  // lists from the old block table, then the new table and decode list
+
+// NT threads per CTA: 256 for a copy on the decode's stream, 64 (at most 64 registers a
+// thread: 4096 registers and 16 KB of shared memory a CTA) for a background copy whose CTAs
+// stay resident beside a decode or score CTA on the same SM
+template <int NT, int MODE>
+__global__ void __launch_bounds__(NT, 65536 / (NT * 64)) tier_promote_kernel(const TierArgs a) {
+  constexpr int kThreads = NT;
+  constexpr int U = NT == 64 ? 5 : 4;  // host reads in flight per thread
   __shared__ uint32_t in_sel[kMaxTierPages / 32];   // page is in the new selection
   __shared__ uint32_t resident[kMaxTierPages / 32]; // page is held by one of the row's blocks
   __shared__ int32_t freed[kMaxTierK];              // slots to reuse, ascending
@@ -59,16 +70,19 @@ __global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a
   __shared__ int n_freed, n_in;
   const int tid = threadIdx.x;
   const int words = (a.n_pages + 31) / 32;
-  for (int i = blockIdx.x; i < a.n_rows; i += gridDim.x) {
-    const int64_t row = a.rows[i];
+  const int units = MODE == kCopy ? a.n_rows * a.slices : a.n_rows;
+  for (int i = blockIdx.x; i < units; i += gridDim.x) {
+    const int ri = MODE == kCopy ? i / a.slices : i, slice = MODE == kCopy ? i % a.slices : 0;
+    const int64_t row = a.rows[ri];
     if (row < 0 || row >= a.total_rows) {
-      if (tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+      if (tid == 0 && slice == 0) report(a.status, TG_STATUS_BAD_INPUT);
       continue;  // uniform over the CTA
     }
     const int32_t *srow = a.sel + row * a.K;
     int32_t *prow = a.pt_ids + row * a.K;
     if (a.unstable[row % a.H]) {  // all pages on the GPU
-      for (int k = tid; k < a.K; k += kThreads) prow[k] = (int32_t)(a.dense_base[row] + srow[k]);
+      if (MODE != kCopy)
+        for (int k = tid; k < a.K; k += kThreads) prow[k] = (int32_t)(a.dense_base[row] + srow[k]);
       continue;
     }
     int32_t *spage = a.slot_page + row * a.K;
@@ -121,10 +135,13 @@ __global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a
       __syncthreads();
     }
     const int moves = min(n_freed, n_in);  // equal for a valid selection of K distinct pages
-    if (n_freed != n_in && tid == 0) report(a.status, TG_STATUS_BAD_INPUT);
+    if (n_freed != n_in && tid == 0 && MODE != kCopy) report(a.status, TG_STATUS_BAD_INPUT);
     // copy every promoted page into the block of its freed slot: the CTA's threads stride over
-    // all (page, 16-byte vector) pairs, four independent host reads in flight per thread
-    const int64_t total = (int64_t)moves * a.page_vec;
+    // the (page, 16-byte vector) pairs (all of them, or this slice's share), U independent host
+    // reads in flight per thread
+    const int64_t all = MODE == kCommit ? 0 : (int64_t)moves * a.page_vec;
+    const int64_t lo = MODE == kCopy ? all * slice / a.slices : 0;
+    const int64_t total = MODE == kCopy ? all * (slice + 1) / a.slices : all;
     auto vec_src = [&](int64_t e, uint4 *&dst) -> const uint4 * {
       const int m = (int)(e / a.page_vec), v = (int)(e % a.page_vec);
       const int64_t blk = sblock[freed[m]];
@@ -136,11 +153,11 @@ __global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a
       return a.host_kv + (row * a.n_pages + incoming[m]) * (int64_t)a.page_vec + v;
     };
     bool bad_block = false;
-    for (int64_t e0 = tid; e0 < total; e0 += 4 * kThreads) {
-      uint4 val[4];
-      uint4 *dst[4];
+    for (int64_t e0 = lo + tid; e0 < total; e0 += U * kThreads) {
+      uint4 val[U];
+      uint4 *dst[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int64_t e = e0 + (int64_t)u * kThreads;
         dst[u] = nullptr;
         if (e < total) {
@@ -150,11 +167,12 @@ __global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < U; ++u)
         if (dst[u]) *dst[u] = val[u];
     }
     if (bad_block) report(a.status, TG_STATUS_BAD_PAGE);
     __syncthreads();
+    if (MODE == kCopy) continue;  // (the shared tables are rebuilt for the next unit)
     for (int m = tid; m < moves; m += kThreads) spage[freed[m]] = incoming[m];
     if (tid == 0 && a.promoted && moves) atomicAdd(reinterpret_cast<unsigned long long *>(a.promoted), (unsigned long long)moves);
     __syncthreads();
@@ -180,21 +198,22 @@ __global__ void __launch_bounds__(kThreads) tier_promote_kernel(const TierArgs a
 
 }  // namespace
 
-extern "C" int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
-                               const uint8_t *unstable, int batch, int H, int n_pages, int K, const int32_t *sel,
-                               int32_t *slot_page, const int32_t *slot_block, const int64_t *dense_base,
-                               const void *host_kv, int page_bytes, void *pool, int64_t pool_pages,
-                               int32_t *pt_ids, int64_t *promoted, int32_t *dev_status) {
+namespace {
+int promote_launch(const char *name, int threads, tg_stream_t stream, int n_rows, const int32_t *rows,
+                   int grid_limit, const uint8_t *unstable, int batch, int H, int n_pages, int K, const int32_t *sel,
+                   int32_t *slot_page, const int32_t *slot_block, const int64_t *dense_base, const void *host_kv,
+                   int page_bytes, void *pool, int64_t pool_pages, int32_t *pt_ids, int64_t *promoted,
+                   int32_t *dev_status) {
   if (n_rows < 0 || batch < 0 || H <= 0 || n_pages < 1 || K < 1 || K > n_pages)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_tier_promote: bad sizes");
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: bad sizes", name);
   if (n_pages > kMaxTierPages || K > kMaxTierK)
-    return tgi::fail(TG_ERR_SHAPE, "tg_tier_promote: n_pages <= %d and K <= %d", kMaxTierPages, kMaxTierK);
-  if (page_bytes <= 0 || page_bytes % 16) return tgi::fail(TG_ERR_SHAPE, "tg_tier_promote: page_bytes %% 16 != 0");
+    return tgi::fail(TG_ERR_SHAPE, "%s: n_pages <= %d and K <= %d", name, kMaxTierPages, kMaxTierK);
+  if (page_bytes <= 0 || page_bytes % 16) return tgi::fail(TG_ERR_SHAPE, "%s: page_bytes %% 16 != 0", name);
   if (n_rows == 0) return tgi::ok();
   if (!rows || !unstable || !sel || !slot_page || !slot_block || !dense_base || !host_kv || !pool || !pt_ids)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_tier_promote: NULL pointer argument");
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: NULL pointer argument", name);
   if ((reinterpret_cast<uintptr_t>(host_kv) | reinterpret_cast<uintptr_t>(pool)) & 15)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_tier_promote: host_kv and pool must be 16-byte aligned");
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: host_kv and pool must be 16-byte aligned", name);
   // the kernel reads host_kv directly: pinned host memory through its device-mapped address,
   // other host memory only where the device reads pageable memory itself (Grace: through the
   // host page tables over NVLink-C2C)
@@ -212,8 +231,8 @@ extern "C" int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *ro
       host_dev = host_kv;
   }
   if (!host_dev)
-    return tgi::fail(TG_ERR_INVALID_ARG, "tg_tier_promote: host_kv is neither pinned host memory nor readable "
-                                         "pageable memory on this device");
+    return tgi::fail(TG_ERR_INVALID_ARG, "%s: host_kv is neither pinned host memory nor readable "
+                                         "pageable memory on this device", name);
   TierArgs a;
   a.rows = rows;
   a.n_rows = n_rows;
@@ -233,9 +252,47 @@ extern "C" int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *ro
   a.pt_ids = pt_ids;
   a.promoted = promoted;
   a.status = dev_status;
-  const int grid = grid_limit > 0 ? (n_rows < grid_limit ? n_rows : grid_limit) : n_rows;
-  tier_promote_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  a.slices = 1;
+  if (threads == 64) {
+    // background: the copy in slices over up to one small CTA per SM, then the tables
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
+    int cap = grid_limit > 0 && grid_limit < sms ? grid_limit : sms;
+    a.slices = (cap + n_rows - 1) / n_rows;
+    const int64_t units = (int64_t)n_rows * a.slices;
+    const int grid = (int)(units < cap ? units : cap);
+    tier_promote_kernel<64, kCopy><<<grid, 64, 0, st>>>(a);
+    tier_promote_kernel<64, kCommit><<<n_rows < cap ? n_rows : cap, 64, 0, st>>>(a);
+  } else {
+    const int grid = grid_limit > 0 ? (n_rows < grid_limit ? n_rows : grid_limit) : n_rows;
+    tier_promote_kernel<256, kWhole><<<grid, 256, 0, st>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "tg_tier_promote: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return tgi::fail(TG_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
   return tgi::ok();
+}
+}  // namespace
+
+extern "C" int tg_tier_promote(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
+                               const uint8_t *unstable, int batch, int H, int n_pages, int K, const int32_t *sel,
+                               int32_t *slot_page, const int32_t *slot_block, const int64_t *dense_base,
+                               const void *host_kv, int page_bytes, void *pool, int64_t pool_pages,
+                               int32_t *pt_ids, int64_t *promoted, int32_t *dev_status) {
+  return promote_launch("tg_tier_promote", 256, stream, n_rows, rows, grid_limit, unstable, batch, H, n_pages, K,
+                        sel, slot_page, slot_block, dense_base, host_kv, page_bytes, pool, pool_pages, pt_ids,
+                        promoted, dev_status);
+}
+
+extern "C" int tg_tier_promote_background(tg_stream_t stream, int n_rows, const int32_t *rows, int grid_limit,
+                                          const uint8_t *unstable, int batch, int H, int n_pages, int K,
+                                          const int32_t *sel, int32_t *slot_page, const int32_t *slot_block,
+                                          const int64_t *dense_base, const void *host_kv, int page_bytes,
+                                          void *pool, int64_t pool_pages, int32_t *pt_ids, int64_t *promoted,
+                                          int32_t *dev_status) {
+  return promote_launch("tg_tier_promote_background", 64, stream, n_rows, rows, grid_limit, unstable, batch, H,
+                        n_pages, K, sel, slot_page, slot_block, dense_base, host_kv, page_bytes, pool, pool_pages,
+                        pt_ids, promoted, dev_status);
 }

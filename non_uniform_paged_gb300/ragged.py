@@ -229,6 +229,28 @@ class SparseDecoder:
         return mm + kv + ids + qo
 
 
+def reload_phase_plans(batch, H, H_q, d, P, K, n_cta, period=16):
+    """Decode plans of the reload schedule ([FlexiCache] "FlexiCache Scheduler": while a request
+    reloads, only that request pauses and the rest of the batch decodes).  Request b reloads
+    its stable heads at the steps with (step + b) % period == 0, the rows that tg_rerank_rows
+    lists for stable heads with stagger 1.  Phase p = step % period: the requests reloading
+    then hold no tokens in the phase's plan (H_p = 1 lists of K pages of P tokens per head).
+    Returns [(plan, workspace_bytes, paused)] per phase, plan None when every request pauses;
+    paused is a bool array [batch]."""
+    out = []
+    for p in range(period):
+        paused = np.array([(p + b) % period == 0 for b in range(batch)], dtype=bool)
+        if paused.all():
+            out.append((None, 0, paused))
+            continue
+        ntok = np.full((1, batch, H), K * P, np.int32)
+        ntok[0, paused] = 0
+        S = tg_split_map(ntok.sum(axis=1).astype(np.int64), n_cta)
+        plan, ws = tg_plan_decode(S, np.arange(H, dtype=np.int32)[None], ntok, H_q, 1, P, d)
+        out.append((plan, ws, paused))
+    return out
+
+
 class TieredSparseDecoder:
     """Sparse decode of one layer with tiered KV placement ([FlexiCache] "Tiered KV placement").
 
@@ -310,6 +332,61 @@ class TieredSparseDecoder:
     def attend(self, q, out, lse=None, stream=None):
         tg_decode_attn(self.plan, self.plan_dev, 0, q, self.pool, self.pool_pages, self.pt_off, self.pt_ids,
                        self.scale, self.workspace, out, lse=lse, dev_status=self.status, stream=stream)
+
+    def reload_schedule(self, period=16):
+        """Set up the page's reload schedule (reload_phase_plans): one decode plan per phase, and
+        per phase the device list of the stable rows whose pages the reloading requests fetch."""
+        self.period = period
+        self.phase_plans = []
+        ws = self.workspace_bytes
+        for plan, wsb, paused in reload_phase_plans(self.batch, self.H, self.H_q, self.d, self.P, self.K,
+                                                     self.n_cta, period):
+            self.phase_plans.append((plan, None if plan is None else torch.from_numpy(plan).to(self.dev), paused))
+            ws = max(ws, wsb)
+        if ws > self.workspace.numel():
+            self.workspace = torch.zeros(ws, dtype=torch.uint8, device=self.dev)
+        self.phase_stable = []
+        for p in range(period):
+            r = np.array([b * self.H + h for b in range(self.batch) if (p + b) % period == 0
+                          for h in range(self.H) if not self.unstable_h[h]], np.int32)
+            self.phase_stable.append((torch.from_numpy(r if r.size else np.zeros(1, np.int32)).to(self.dev),
+                                      int(r.size)))
+        self._fetch_done = None
+
+    def step_reload(self, q, minmax, rows, n_rows, step, out, stream, fetch_stream, lse=None, grid_limit=0):
+        """One decode step of the reload schedule (reload_schedule first).  On `stream`: score the
+        rows due (rows, n_rows: tg_rerank_rows with stagger 1), then decode every request that is
+        not reloading.  On `fetch_stream` (a low-priority stream), after the scores: the
+        reloading requests' promoted pages, fetched from host by small CTAs that stay resident
+        beside the decode's (tg_tier_promote_background; grid_limit > 0 caps them).  A
+        request that reloaded at the previous step decodes again only after its fetch: `stream`
+        waits for it.  Returns the paused mask [batch]: their rows are empty heads in the step's
+        plan (out = 0, lse = -inf), and their step is to be taken again."""
+        p = step % self.period
+        if n_rows:
+            tg_page_score_topk_rows(self.batch, self.H, self.g, self.d, self.n_pages, self.K, rows, n_rows, q,
+                                    minmax, self.sel, pt_ids=self.pt_ids, dense_base=self.dense_base,
+                                    workspace=self.score_ws, dev_status=self.status, stream=stream)
+        st_rows, n_st = self.phase_stable[p]
+        fetched = None
+        if n_st:
+            scored = torch.cuda.Event()
+            scored.record(stream)
+            fetch_stream.wait_event(scored)
+            tg_tier_promote(st_rows, n_st, self.unstable_dev, self.batch, self.H, self.n_pages, self.K, self.sel,
+                            self.slot_page, self.slot_block, self.dense_base, self.host_kv, self.page_bytes,
+                            self.pool, self.pt_ids, promoted=self.promoted, dev_status=self.status,
+                            grid_limit=grid_limit, stream=fetch_stream, background=True)
+            fetched = torch.cuda.Event()
+            fetched.record(fetch_stream)
+        if self._fetch_done is not None:
+            stream.wait_event(self._fetch_done)
+        plan, plan_dev, paused = self.phase_plans[p]
+        if plan is not None:
+            tg_decode_attn(plan, plan_dev, 0, q, self.pool, self.pool_pages, self.pt_off, self.pt_ids, self.scale,
+                           self.workspace, out, lse=lse, dev_status=self.status, stream=stream)
+        self._fetch_done = fetched
+        return paused
 
     def gpu_kv_bytes(self) -> int:
         return self.pool_pages * self.page_bytes

@@ -1,5 +1,6 @@
 """Tiered KV placement (tg_tier_promote): promoted-page fetch from pinned host memory into
-GPU blocks reused in place, against the oracle; tiered sparse decode against all-GPU."""
+GPU blocks reused in place, against the oracle; tiered sparse decode against all-GPU, also
+under the reload schedule (fetch on a background stream, only the reloading request paused)."""
 import ctypes
 import math
 
@@ -18,6 +19,8 @@ def _random_sel(rng, total, n_pages, K):
 
 
 def test_tier_promote_matches_oracle(lib, cuda):
+    # odd iterations take tg_tier_promote_background: the copy in slices over small CTAs, then
+    # the block tables and decode lists in a second launch
     batch, H, n_pages, K, page_elems = 3, 4, 23, 6, 40  # 80-byte pages
     unstable = np.array([1, 0, 0, 1], np.uint8)
     total = batch * H
@@ -52,7 +55,7 @@ def test_tier_promote_matches_oracle(lib, cuda):
         lib.tg_tier_promote(torch.from_numpy(rows).to(cuda), rows.size, *args, torch.from_numpy(sel).to(cuda),
                             sp_dev, torch.from_numpy(slot_block).to(cuda), torch.from_numpy(dense_base).to(cuda),
                             host, page_elems * 2, pool, ids, promoted=promoted, dev_status=status,
-                            grid_limit=int(rng.integers(0, 4)))
+                            grid_limit=int(rng.integers(0, 4)), background=bool(it % 2))
         torch.cuda.synchronize()
         assert lib.tg_check_status(status) == 0
         got_sp, got_ids = sp_dev.cpu().numpy(), ids.cpu().numpy()
@@ -152,3 +155,64 @@ def test_tiered_decode_equals_all_gpu_sparse(lib, cuda):
             assert copies - copies_before < stable_rows * K  # later ones move only what changed
         copies_before = copies
     assert tier.gpu_kv_bytes() < tier.dense_kv_bytes()
+
+
+def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda):
+    """[FlexiCache] FlexiCache Scheduler and KV transfer: with stagger 1 the requests reload their
+    stable heads one phase at a time.  A reloading request's promoted pages come from host on a
+    low-priority stream while that request pauses, and the rest of the batch decodes.  At every
+    step the decoding requests' outputs equal sparse decode over all-GPU pages with the same
+    plan, bit for bit; that includes the requests that reloaded at the step before (their
+    fetched pages are in place).  The paused requests' rows are empty heads in the step's plan."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, TieredSparseDecoder, build_minmax, reload_phase_plans
+    w = synth.workload(4, batch=5, N=640, L=1)
+    P, n_pages, K, period = w.P, w.N // w.P, 8, 4
+    Kt, Vt = synth.keys_values(w, 0, cuda)
+    mm = build_minmax(Kt, P)
+    dense = _dense_pool(Kt, Vt, P)
+    unstable = np.zeros(w.H, np.uint8)
+    unstable[[1, 6]] = 1
+    tier = TieredSparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, unstable, n_cta=32, device=cuda)
+    tier.load(dense)
+    tier.reload_schedule(period)
+    ref = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=32, device=cuda)
+    ws_ref = torch.zeros(max(p[1] for p in reload_phase_plans(w.batch, w.H, w.H_q, w.d, P, K, 32, period)),
+                         dtype=torch.uint8, device=cuda)
+    fetch = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(9)
+    q = synth.queries(w, 0, cuda).float()
+    qb = q.to(torch.bfloat16)
+    tier.rerank(qb, mm)  # step 0: every row re-ranked, every stable block filled
+    ref.select(qb, mm)
+    copies0 = None
+    for step in range(1, 2 * period + 2):
+        q = q + 0.4 * torch.randn(q.shape, generator=gen, device=cuda)
+        qb = q.to(torch.bfloat16)
+        rows_h = lib.tg_rerank_rows(unstable[None], w.batch, 0, step, period, 1)
+        rows = torch.from_numpy(rows_h.astype(np.int32)).to(cuda)
+        out_t = torch.full((w.batch, w.H_q, w.d), float("nan"), dtype=torch.bfloat16, device=cuda)
+        lse_t = torch.full((w.batch, w.H_q), float("nan"), dtype=torch.float32, device=cuda)
+        torch.cuda.synchronize()
+        copies0 = int(tier.promoted.item())
+        paused = tier.step_reload(qb, mm, rows, rows_h.size, step, out_t, main, fetch, lse=lse_t)
+        ref.select_rows(qb, mm, rows, rows_h.size)
+        plan, plan_dev, _ = tier.phase_plans[step % period]
+        out_r = torch.empty_like(out_t)
+        lse_r = torch.empty_like(lse_t)
+        lib.tg_decode_attn(plan, plan_dev, 0, qb, dense, w.batch * w.H * n_pages, ref.pt_off, ref.pt_ids[0],
+                           ref.scale, ws_ref, out_r, lse=lse_r, dev_status=ref.status)
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(tier.status) == 0 and lib.tg_check_status(ref.status) == 0
+        expect = np.array([(step + b) % period == 0 for b in range(w.batch)])
+        assert np.array_equal(paused, expect) and expect.any() and not expect.all(), step
+        act = torch.from_numpy(~paused).to(cuda)
+        assert torch.equal(out_t[act], out_r[act]) and torch.equal(lse_t[act], lse_r[act]), step
+        # a paused request's rows hold no tokens in the phase's plan: out = 0, lse = -inf (an empty head)
+        assert (out_t[~act].float() == 0).all() and (lse_t[~act] == float("-inf")).all(), step
+        rl = rows.long()
+        assert torch.equal(tier.sel[rl], ref.sel[0].view(-1, K)[rl]), step
+        # only the reloading requests' stable rows fetch pages, and fewer than all of their blocks
+        n_fetch_rows = int(paused.sum()) * int((unstable == 0).sum())
+        assert 0 <= int(tier.promoted.item()) - copies0 <= n_fetch_rows * K, step

@@ -193,3 +193,31 @@ def test_plan_flags(lib):
     assert lib.plan_header(plan)["flags"] == lib.PLAN_WAIT_TABLES
     with pytest.raises(lib.TGError):
         lib.tg_plan_set_flags(plan, 0x80)
+
+
+@pytest.mark.parametrize("batch,period", [(6, 4), (40, 16), (3, 4), (1, 2)])
+def test_reload_phase_plans_pause_only_the_reloading_requests(lib, batch, period):
+    """[FlexiCache] FlexiCache Scheduler: at phase p the requests with (p + b) % period == 0
+    reload and pause; the phase's plan covers every token of every other request's rows once,
+    none of the paused ones', and splits all N_CTA CTAs."""
+    from non_uniform_paged_gb300.ragged import reload_phase_plans
+    H, H_q, d, P, K, n_cta = 8, 32, 128, 16, 8, 24
+    phases = reload_phase_plans(batch, H, H_q, d, P, K, n_cta, period)
+    assert len(phases) == period
+    for p, (plan, ws, paused) in enumerate(phases):
+        expect = np.array([(p + b) % period == 0 for b in range(batch)])
+        assert np.array_equal(paused, expect), p
+        if expect.all():
+            assert plan is None
+            continue
+        hd = lib.plan_header(plan)
+        assert hd["N_CTA"] == n_cta and ws == hd["workspace_bytes"]
+        off, items = lib.plan_items(plan, 0)
+        assert off[0] == 0 and off[-1] == items.size and np.all(np.diff(off) >= 0)
+        covered = np.zeros((batch, H), np.int64)
+        for it in items:
+            if it["t1"] > it["t0"]:  # (a CTA left without work holds one empty item)
+                assert not paused[it["b"]], (p, it)
+            covered[it["b"], it["h"]] += it["t1"] - it["t0"]
+        want = np.where(paused[:, None], 0, K * P)
+        assert np.array_equal(covered, np.broadcast_to(want, (batch, H))), p
