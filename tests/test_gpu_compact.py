@@ -103,3 +103,21 @@ def test_nan_score_is_reported_and_other_rows_stay_exact(lib, cuda):
     s = synth.scores(w, 0, cuda)
     s[0, 0, 59999] = float("nan")
     _compact(lib, w, cuda, s, np.array([60000]), expect_status=STATUS_NONFINITE, skip_rows={(0, 0)})
+
+
+def test_rows_not_16_byte_aligned_load_key_by_key(lib, cuda):
+    """Nmax = 1501: rows of scores do not start on 16-byte boundaries, so the select kernel
+    loads its chunks with plain loads instead of bulk copies; ties on a coarse grid."""
+    w = synth.small(batch=3, N=1501, L=1)
+    s = torch.round(synth.scores(w, 0, cuda) * 2) / 2
+    _compact(lib, w, cuda, s, synth.contexts(w))
+
+
+def test_row_longer_than_the_clusters_shared_memory(lib, cuda):
+    """One row of 200000 tokens: even a cluster of 8 CTAs holds at most 8 x 22528 keys in shared
+    memory, so the rest of each chunk is re-read from L2 in every pass and in the per-block
+    counts; scores on a grid of quarters (ties across the n-th key), and an all-equal row."""
+    w = synth.small(batch=1, N=200000, L=1, H=2, H_q=4, H_p=1, budget_args=(0.3, 0.6), ctx_dist="fixed")
+    s = torch.round(synth.scores(w, 0, cuda) * 4) / 4
+    s[0, 1] = -1.25
+    _compact(lib, w, cuda, s, np.array([200000]))
