@@ -263,4 +263,125 @@ __device__ void block_select_kth(int count, int k, GetKey get, uint32_t *list, i
   n_eq = sel_count;
 }
 
+// The same selection with digits of 12, 10 and 10 bits and plain shared-memory atomics: the
+// top 12 bits of a float key (sign, exponent and three mantissa bits) spread real scores over
+// many counters, where the 8-bit first digit of block_select_kth piles them into a few (which
+// that function meets with warp grouping, at a high cost per key).  hist0 holds 4096 ints and
+// may share its memory with `list` (it is dead once the first digit is chosen); hist1 holds
+// 1024 ints of its own; scratch holds NT / 32 + 4 ints.  After the first digit, the keys under
+// it are copied into `list` when at most `cap` (NULL: none), and the other passes read only them.
+template <int NT, typename GetKey>
+__device__ void block_select_kth_wide(int count, int k, GetKey get, uint32_t *list, int cap, int *hist0, int *hist1,
+                                      int *scratch, uint32_t &T, int &need_eq, int &n_eq) {
+  constexpr int U = 4, NWARP = NT / 32;
+  static_assert(NT % 32 == 0 && 4096 % NT == 0 && NT <= 1024, "block size");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, mask = 0;
+  int k_rem = k, sel_count = count, n_list = -1;
+  // the digit (of `bins` counters in h) that holds the k_rem-th key: thread t owns the bins
+  // bins-1-t*per .. bins-(t+1)*per (from the top down), a block scan finds the owner
+  auto pick = [&](const int *h, int bins, int shift, int bits) {
+    const int per = bins / NT, top = bins - 1 - tid * per;
+    int s = 0;
+    for (int j = 0; j < per; ++j) s += h[top - j];
+    int inc = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) scratch[4 + warp] = inc;
+    __syncthreads();
+    int before = inc - s;
+    for (int w = 0; w < warp; ++w) before += scratch[4 + w];
+    if (before < k_rem && k_rem <= before + s) {
+      int above = before;
+      for (int j = 0; j < per; ++j) {
+        const int c = h[top - j];
+        if (above + c >= k_rem) {
+          scratch[0] = top - j;
+          scratch[1] = above;
+          scratch[2] = c;
+          break;
+        }
+        above += c;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)scratch[0] << shift;
+    mask |= ((1u << bits) - 1u) << shift;
+    k_rem -= scratch[1];
+    sel_count = scratch[2];
+    __syncthreads();  // (scratch and the counters are reused)
+  };
+  // first digit, over every key
+  for (int i = tid; i < 4096; i += NT) hist0[i] = 0;
+  __syncthreads();
+  for (int base = 0; base < count; base += NT * U) {
+    uint32_t kk[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT + tid;
+      kk[u] = i < count ? get(i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * NT + tid < count) atomicAdd(&hist0[kk[u] >> 20], 1);
+  }
+  __syncthreads();
+  pick(hist0, 4096, 20, 12);
+  if (list && sel_count <= cap) {
+    // copy the keys under the first digit into the list (order does not matter for counts)
+    if (tid == 0) scratch[3] = 0;
+    __syncthreads();
+    for (int base = 0; base < count; base += NT * U) {
+      uint32_t kk[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * NT + tid;
+        kk[u] = i < count ? get(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool keep = base + u * NT + tid < count && (kk[u] & mask) == prefix;
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        int at = 0;
+        if (lane == 0 && bal) at = atomicAdd(&scratch[3], __popc(bal));
+        at = __shfl_sync(0xffffffffu, at, 0);
+        if (keep) list[at + __popc(bal & ((1u << lane) - 1u))] = kk[u];
+      }
+    }
+    n_list = sel_count;
+    __syncthreads();
+  }
+  // two digits of 10 bits over the list (or every key)
+  for (int shift = 10; shift >= 0; shift -= 10) {
+    for (int i = tid; i < 1024; i += NT) hist1[i] = 0;
+    __syncthreads();
+    if (n_list >= 0) {
+      for (int i = tid; i < n_list; i += NT) {
+        const uint32_t key = list[i];
+        if ((key & mask) == prefix) atomicAdd(&hist1[(key >> shift) & 1023u], 1);
+      }
+    } else {
+      for (int base = 0; base < count; base += NT * U) {
+        uint32_t kk[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = base + u * NT + tid;
+          kk[u] = i < count ? get(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (base + u * NT + tid < count && (kk[u] & mask) == prefix) atomicAdd(&hist1[(kk[u] >> shift) & 1023u], 1);
+      }
+    }
+    __syncthreads();
+    pick(hist1, 1024, shift, 10);
+  }
+  T = prefix;
+  need_eq = k_rem;
+  n_eq = sel_count;
+}
+
 }  // namespace tgk

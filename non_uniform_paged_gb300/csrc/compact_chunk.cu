@@ -65,9 +65,8 @@ struct ChunkArgs {
 
 __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkArgs a) {
   extern __shared__ uint32_t cache[];  // score keys of the candidates when they fit
-  __shared__ int hist[256];
   __shared__ int scan[33];
-  __shared__ int sel_scratch[4];
+  __shared__ int sel_scratch[kWarps + 4];
   // the selects' key list, then the entering chunk positions (ascending)
   __shared__ int work[2 * kMaxChunk];
   int *const incoming = work;
@@ -164,15 +163,20 @@ __global__ void __launch_bounds__(kThreads, 1) compact_chunk_kernel(const ChunkA
   int n_in = 0;
   uint32_t T_hi = 0u, T_lo = 0u;
   if (!append) {
+    // the selects' key list, with the first digit's 4096 counters in the same memory; the later
+    // digits' 1024 counters at the end of it
     uint32_t *const list = reinterpret_cast<uint32_t *>(work);
+    int *const hist0 = work, *const hist1 = work + 2 * kMaxChunk - 1024;
+    const int cap = 2 * kMaxChunk - 1024;
     int need_hi, n_eq;
-    block_select_kth<kThreads>(m, n, hi_of, list, 2 * kMaxChunk, hist, sel_scratch, T_hi, need_hi, n_eq);
+    block_select_kth_wide<kThreads>(m, n, hi_of, list, cap, hist0, hist1, sel_scratch, T_hi, need_hi, n_eq);
     // among the keys equal to T_hi, the need_hi lowest tokens (largest ~token) survive; with no
     // tie across the cut every one of them does, and T_lo = 0 keeps them all
     if (n_eq > need_hi) {
       int unused0, unused1;
-      block_select_kth<kThreads>(m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; },
-                                 list, 2 * kMaxChunk, hist, sel_scratch, T_lo, unused0, unused1);
+      block_select_kth_wide<kThreads>(
+          m, need_hi, [&](int i) { return hi_of(i) == T_hi ? ~(uint32_t)tok_of(i) : 0u; }, list, cap, hist0, hist1,
+          sel_scratch, T_lo, unused0, unused1);
     }
   }
   auto survives = [&](int i) {
