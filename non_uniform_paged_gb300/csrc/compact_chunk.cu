@@ -42,7 +42,7 @@ constexpr int kMaxChunk = 8192;        // tokens per chunk (entering-token list 
 constexpr int kSmemKeys = 40960;       // candidates whose score keys are cached in shared memory (160 KB)
 constexpr int kLoadUnroll = 12;        // slot keys each thread has in flight while loading
 constexpr int kCopyThreads = 256;      // copy kernel: 8 warps per CTA
-constexpr int kCopyTokens = 4;         // tokens a warp copies at once (their K/V vectors in flight)
+constexpr int kCopyTokens = 8;         // tokens a warp copies at once (their K/V vectors in flight)
 
 constexpr int kWarps = kThreads / 32;
 
