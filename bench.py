@@ -846,14 +846,17 @@ def bench_tiered(args, w, q, mms, pools, out, stream, device, layers=4, steps=32
 def bench_reload_schedule(w, qs, mms, pools, out, tiers, flat, unstable, L, steps, period, device, grid_limit=0):
     """The page's reload schedule for tiered placement ([FlexiCache] FlexiCache Scheduler, KV
     transfer): stable heads re-rank one request phase per step (stagger 1).  A reloading
-    request's promoted pages come from host on a low-priority stream, by 64-thread CTAs that
-    stay resident beside the decode's (one per promoted row; grid_limit > 0 caps them), while
-    only that request pauses; the rest of the batch decodes on a high-priority stream.  Against the same schedule with every page on the GPU (no pause).  Reports ms per
+    request's promoted pages come from host on a second stream, by 64-thread CTAs that stay
+    resident beside the decode's (one per promoted row; grid_limit > 0 caps them), while only
+    that request pauses; the rest of the batch decodes on the first stream.  Against the same schedule with every page on the GPU (no pause).  Reports ms per
     step (scaled to the model's layers), requests decoded per step and their rate."""
     from non_uniform_paged_gb300.ragged import RerankSchedule
     sched = RerankSchedule(unstable, w.batch, period=period, stagger=1, device=device)
-    hi = torch.cuda.Stream(priority=-1)  # CUDA stream priorities: lower number, higher priority
-    lo = torch.cuda.Stream(priority=0)
+    # two streams of equal priority: a low-priority fetch stream (the page's choice) measured
+    # 2.06-2.36 ms per step with one step of 11 ms, when the fetch was starved and the next
+    # step's decode waited for it; equal priorities 2.05-2.18 ms, worst step 2.5 ms
+    hi = torch.cuda.Stream()
+    lo = torch.cuda.Stream()
     for t in tiers:
         t.reload_schedule(period)
 
@@ -899,8 +902,8 @@ def bench_reload_schedule(w, qs, mms, pools, out, tiers, flat, unstable, L, step
     tiered = run(True)
     return {"period": period, "stagger": 1, "fetch_ctas": "one 64-thread CTA per promoted row" if grid_limit <= 0
             else f"at most {grid_limit} 64-thread CTAs", "layers_timed": L,
-            "timing": "ms per step of the layers timed, scaled to the model's layers; fetch on a low-priority "
-                      "stream, decode on a high-priority one",
+            "timing": "ms per step of the layers timed, scaled to the model's layers; fetch and decode on two "
+                      "streams of equal priority",
             "all_gpu": {k: v for k, v in gpu.items() if k != "promoted_pages_per_step"}, "tiered": tiered,
             "fetch_grid": "a cap of 8-64 CTAs measured 1.1-3.1x slower per step: the host link then keeps too "
                           "few reads in flight and the decode waits for the fetch",

@@ -356,7 +356,8 @@ class TieredSparseDecoder:
     def step_reload(self, q, minmax, rows, n_rows, step, out, stream, fetch_stream, lse=None, grid_limit=0):
         """One decode step of the reload schedule (reload_schedule first).  On `stream`: score the
         rows due (rows, n_rows: tg_rerank_rows with stagger 1), then decode every request that is
-        not reloading.  On `fetch_stream` (a low-priority stream), after the scores: the
+        not reloading.  On `fetch_stream` (a second stream; a lower priority than `stream`'s can
+        starve the fetch and stall the next step), after the scores: the
         reloading requests' promoted pages, fetched from host by small CTAs that stay resident
         beside the decode's (tg_tier_promote_background; grid_limit > 0 caps them).  A
         request that reloaded at the previous step decodes again only after its fetch: `stream`
