@@ -443,6 +443,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) compact_select_kernel(const Se
     carry_eq += te;
     __syncthreads();
   }
+  // after a copy wait that gave up, one thread waits (again bounded) for the copies still in
+  // flight, so none lands in the shared memory of a CTA that has left (the CTA stays until
+  // its last thread exits)
+  if (tid == 0 && (err & 2))
+    for (int i = 0; i < npieces; ++i) mbar_wait(&bars[i], 0, kCopyWaitNs);
   // the copy kernel may launch now (letting it take SMs earlier, while this kernel still
   // selects, measured 20-30% slower on long rows)
   griddep_launch_dependents();
