@@ -1,8 +1,8 @@
 // Block-wide helpers for exact top-k selection with ties to the lower index:
 // exclusive scans of per-thread flags (one, or U per thread) and MSB-first radix selects over
-// order-preserving uint32 keys (a plain one, and one that narrows to a candidate
-// list in shared memory).  Used by the one-shot and the chunked token compaction
-// and by the page top-K of long rows.
+// order-preserving uint32 keys (a plain one for short rows, and one with wide digits that
+// narrows to a candidate list in shared memory).  Used by the one-shot compaction's copy
+// (the scans), the chunked token compaction and the page top-K of long rows.
 #pragma once
 
 #include <cstdint>
@@ -155,121 +155,15 @@ __device__ __forceinline__ void block_radix_select(int count, int k, GetKey get,
   need_eq = k_rem;
 }
 
-// The same selection, for rows whose keys are read from global memory or are many: also
-// returns n_eq, the number of keys equal to T.  After a pass whose chosen digit leaves at
-// most `cap` keys, those keys are copied into `list` (shared memory; NULL for none) and the
-// remaining passes read only them.  Passes over get() keep four keys in flight per thread.
-template <int NT, typename GetKey>
-__device__ void block_select_kth(int count, int k, GetKey get, uint32_t *list, int cap, int *hist, int *scratch,
-                                 uint32_t &T, int &need_eq, int &n_eq) {
-  constexpr int U = 4;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int k_rem = k, n_list = -1, sel_count = count;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += NT) hist[i] = 0;
-    __syncthreads();
-    // histogram of the next digit among keys that match the prefix so far (the first
-    // pass groups a warp's equal digits, which coincide there; later digits are spread out)
-    auto count_digit = [&](uint32_t key, bool valid) {
-      const uint32_t dg = valid && (key & mask) == prefix ? (key >> shift) & 255u : 256u;
-      if (shift == 24) {
-        const uint32_t peers = __match_any_sync(0xffffffffu, dg);
-        if (dg < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
-      } else if (dg < 256u) {
-        atomicAdd(&hist[dg], 1);
-      }
-    };
-    if (n_list < 0) {
-      for (int base = 0; base < count; base += NT * U) {
-        uint32_t kk[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = base + u * NT + tid;
-          kk[u] = i < count ? get(i) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) count_digit(kk[u], base + u * NT + tid < count);
-      }
-    } else {
-      for (int base = 0; base < n_list; base += NT) {
-        const int i = base + tid;
-        count_digit(i < n_list ? list[i] : 0u, i < n_list);
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits 255-8l down to 248-8l; scan from the top digit down
-      int local[8];
-      int sum = 0;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        local[t] = hist[255 - 8 * lane - t];
-        sum += local[t];
-      }
-      int inc = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-      }
-      const int before = inc - sum;  // keys in digits above this lane's block
-      if (before < k_rem && k_rem <= inc) {
-        int above = before;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (above + local[t] >= k_rem) {
-            scratch[0] = 255 - 8 * lane - t;
-            scratch[1] = above;
-            scratch[2] = local[t];
-            break;
-          }
-          above += local[t];
-        }
-      }
-      if (lane == 0) scratch[3] = 0;
-    }
-    __syncthreads();
-    const uint32_t digit = (uint32_t)scratch[0];
-    k_rem -= scratch[1];
-    sel_count = scratch[2];
-    prefix |= digit << shift;
-    mask |= 255u << shift;
-    if (list && n_list < 0 && shift > 0 && sel_count <= cap) {
-      // copy the keys under the new prefix into the list (order does not matter for counts)
-      for (int base = 0; base < count; base += NT * U) {
-        uint32_t kk[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = base + u * NT + tid;
-          kk[u] = i < count ? get(i) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const bool keep = base + u * NT + tid < count && (kk[u] & mask) == prefix;
-          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-          int at = 0;
-          if (lane == 0 && bal) at = atomicAdd(&scratch[3], __popc(bal));
-          at = __shfl_sync(0xffffffffu, at, 0);
-          if (keep) list[at + __popc(bal & ((1u << lane) - 1u))] = kk[u];
-        }
-      }
-      n_list = sel_count;
-    }
-    __syncthreads();
-  }
-  T = prefix;
-  need_eq = k_rem;
-  n_eq = sel_count;
-}
-
-// The same selection with digits of 12, 10 and 10 bits and plain shared-memory atomics: the
-// top 12 bits of a float key (sign, exponent and three mantissa bits) spread real scores over
-// many counters, where the 8-bit first digit of block_select_kth piles them into a few (which
-// that function meets with warp grouping, at a high cost per key).  hist0 holds 4096 ints and
-// may share its memory with `list` (it is dead once the first digit is chosen); hist1 holds
-// 1024 ints of its own; scratch holds NT / 32 + 4 ints.  After the first digit, the keys under
-// it are copied into `list` when at most `cap` (NULL: none), and the other passes read only them.
+// The same selection for many keys, also returning n_eq, the number of keys equal to T, with
+// digits of 12, 10 and 10 bits and plain shared-memory atomics: the top 12 bits of a float key
+// (sign, exponent and three mantissa bits) spread real scores over many counters, where an
+// 8-bit first digit piles them into a few (grouping a warp's equal digits with match_any
+// instead measured at several hundred cycles a key).  hist0 holds 4096 ints and may share its
+// memory with `list` (it is dead once the first digit is chosen); hist1 holds 1024 ints of its
+// own; scratch holds NT / 32 + 4 ints.  After the first digit, the keys under it are copied
+// into `list` when at most `cap` (NULL: none), and the other passes read only them; passes
+// over get() keep four keys in flight per thread.
 template <int NT, typename GetKey>
 __device__ void block_select_kth_wide(int count, int k, GetKey get, uint32_t *list, int cap, int *hist0, int *hist1,
                                       int *scratch, uint32_t &T, int &need_eq, int &n_eq) {

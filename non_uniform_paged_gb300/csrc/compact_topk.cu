@@ -8,16 +8,20 @@
 //
 // Two kernels per layer.  Positions of a row (request, KV head) are cut into blocks of
 // kBlk = 1024.
-//  select  one thread-block cluster of C CTAs per row.  CTA j loads its chunk of the row
-//          (a range of whole blocks) once, as order-preserving keys of the float32 scores,
-//          into shared memory, and checks it for NaN.  The exact n-th largest key T of the
-//          whole row comes from an MSB-first radix select in four 8-bit passes: each CTA
-//          histograms its own chunk, and after a cluster barrier every CTA adds up the C
-//          histograms through distributed shared memory, so all of them take the same
-//          digit; the sums over the lower ranks give each CTA the keys above T and equal
-//          to T before its chunk.  The cluster then writes T, need_eq (the keys equal to
-//          T that a top-n takes: the lowest-indexed ones) and, for every block, the keys
-//          > T and == T before it, to the workspace.  The row's keys are read once.
+//  select  one thread-block cluster of C CTAs per row.  CTA j brings its chunk of the row
+//          (a range of whole blocks) into shared memory once, by bulk copies, turns the
+//          float32 scores into order-preserving keys in place and checks them for NaN.  The
+//          exact n-th largest key T of the whole row comes from an MSB-first radix select
+//          with digits of 12, 10 and 10 bits: each CTA counts its own chunk's digits, and
+//          after a cluster barrier every CTA adds up the cluster's counts through
+//          distributed shared memory (first 256 sums of adjacent digits, then the digits
+//          inside the chosen sum), so all of them take the same digit; the sums over the
+//          lower ranks give each CTA the keys above T and equal to T before its chunk.
+//          After the first digit each block keeps only its keys under that digit (moved to
+//          its front), and the later passes read only those.  The cluster then writes T,
+//          need_eq (the keys equal to T that a top-n takes: the lowest-indexed ones) and,
+//          for every block, the keys > T and == T before it, to the workspace.  The row's
+//          scores are read from memory once.
 //  copy    1024-thread CTAs take shares of the rows' blocks, in proportion to the rows'
 //          work (retained tokens plus positions swept).  A CTA reads the counts before its
 //          first block from the workspace and sweeps its blocks in ascending order, four
