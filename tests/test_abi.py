@@ -61,3 +61,38 @@ def test_compact_chunk_workspace_size_and_short_workspace_refused(lib):
     assert b"workspace" in so.tg_last_error_string()
     with pytest.raises(lib.TGError):
         lib.tg_compact_chunk_workspace(batch, 0, C)
+
+
+def test_compact_topk_workspace_size_and_short_workspace_refused(lib):
+    """tg_compact_topk_workspace: per row T, need_eq, two unused ints, then (keys > T, keys == T)
+    for every block of 1024 positions.  A workspace one byte short is refused on the host
+    (TG_ERR_CAPACITY), before any launch; the pointers below are never dereferenced."""
+    batch, H, Nmax = 3, 8, 5000
+    need = lib.tg_compact_topk_workspace(batch, H, Nmax)
+    assert need == batch * H * (4 + 2 * -(-Nmax // 1024)) * 4
+    so = lib.load()
+    fake = ctypes.c_void_p(4096)
+    rc = so.tg_compact_topk(None, batch, H, 2, 16, 128, Nmax, fake, fake, fake, fake, fake, fake, fake, fake, 1,
+                            fake, None, fake, need - 1, None)
+    assert rc == -4  # TG_ERR_CAPACITY
+    assert b"workspace" in so.tg_last_error_string()
+    rc = so.tg_compact_topk(None, batch, H, 2, 16, 128, Nmax, fake, fake, fake, fake, fake, fake, fake, fake, 1,
+                            fake, None, None, need, None)
+    assert rc == -1  # TG_ERR_INVALID_ARG: no workspace
+    with pytest.raises(lib.TGError):
+        lib.tg_compact_topk_workspace(batch, H, 0)
+
+
+def test_tier_promote_background_checks_arguments_on_the_host(lib):
+    """tg_tier_promote_background takes tg_tier_promote's arguments and refuses the same bad
+    ones before any launch: sizes out of range and NULL pointers."""
+    so = lib.load()
+    fake = ctypes.c_void_p(4096)
+    # K > n_pages
+    rc = so.tg_tier_promote_background(None, 1, fake, 0, fake, 1, 2, 4, 8, fake, fake, fake, fake, fake, 32, fake, 8,
+                                       fake, None, None)
+    assert rc == -1 and b"tg_tier_promote_background" in so.tg_last_error_string()
+    # a NULL selection
+    rc = so.tg_tier_promote_background(None, 1, fake, 0, fake, 1, 2, 8, 4, None, fake, fake, fake, fake, 32, fake, 8,
+                                       fake, None, None)
+    assert rc == -1 and b"NULL" in so.tg_last_error_string()
