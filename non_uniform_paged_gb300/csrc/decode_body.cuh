@@ -497,17 +497,39 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
         const float *po = a.ws_o + (size_t)it.slot0 * g * D;     // [nparts][g][D]
         if (np * g <= kFacMax) {
           // factors 2^(m_p - M) of every part go to shared memory; per head, one warp gathers
-          // M and L with its lanes striding over the parts (independent loads)
+          // M and L with its lanes striding over the parts (independent loads).  Up to 64 parts,
+          // each lane reads its (m, l) pairs once and keeps them in registers
           for (int hh = ew; hh < g; hh += NE) {
-            float M = -INFINITY;
-            for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(pml + ((size_t)p * g + hh) * 2));
+            float M = -INFINITY, Ls = 0.f;
+            if (np <= 64) {
+              float2 ml[2];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float Ls = 0.f;
-            for (int p = lane; p < np; p += 32) {
-              const float f = ex2(__ldcg(pml + ((size_t)p * g + hh) * 2) - M);
-              fac[p * g + hh] = f;
-              Ls += __ldcg(pml + ((size_t)p * g + hh) * 2 + 1) * f;
+              for (int j = 0; j < 2; ++j) {
+                const int p = lane + 32 * j;
+                ml[j] = p < np ? __ldcg(reinterpret_cast<const float2 *>(pml + ((size_t)p * g + hh) * 2))
+                               : make_float2(-INFINITY, 0.f);
+                M = fmaxf(M, ml[j].x);
+              }
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int p = lane + 32 * j;
+                if (p < np) {
+                  const float f = ex2(ml[j].x - M);
+                  fac[p * g + hh] = f;
+                  Ls += ml[j].y * f;
+                }
+              }
+            } else {
+              for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(pml + ((size_t)p * g + hh) * 2));
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+              for (int p = lane; p < np; p += 32) {
+                const float f = ex2(__ldcg(pml + ((size_t)p * g + hh) * 2) - M);
+                fac[p * g + hh] = f;
+                Ls += __ldcg(pml + ((size_t)p * g + hh) * 2 + 1) * f;
+              }
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
@@ -518,19 +540,19 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
           }
           epilogue_sync<NET>();
           // O = sum_p o_p 2^(m_p - M), parts in order.  A thread takes four consecutive outputs
-          // of one head (16-byte loads; partial rows are 16-byte aligned), eight parts per
+          // of one head (16-byte loads; partial rows are 16-byte aligned), sixteen parts per
           // batch in flight
           for (int e = 4 * etid; e < g * D; e += 4 * NET) {
             const int hd = e / D, dd = e % D;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = 0; p < np; p += 8) {
-              float4 v[8];
+            for (int p = 0; p < np; p += 16) {
+              float4 v[16];
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+              for (int u = 0; u < 16; ++u)
                 v[u] = p + u < np ? __ldcg(reinterpret_cast<const float4 *>(po + (size_t)(p + u) * g * D + e))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+              for (int u = 0; u < 16; ++u)
                 if (p + u < np) {
                   const float f = fac[(p + u) * g + hd];
                   O.x += v[u].x * f;
