@@ -362,7 +362,8 @@ class TieredSparseDecoder:
         beside the decode's (tg_tier_promote_background; grid_limit > 0 caps them).  A
         request that reloaded at the previous step decodes again only after its fetch: `stream`
         waits for it.  Returns the paused mask [batch]: their rows are empty heads in the step's
-        plan (out = 0, lse = -inf), and their step is to be taken again."""
+        plan (out = 0, lse = -inf), and their step is to be taken again.  When every request
+        reloads, nothing is decoded and out / lse are not written."""
         p = step % self.period
         if n_rows:
             tg_page_score_topk_rows(self.batch, self.H, self.g, self.d, self.n_pages, self.K, rows, n_rows, q,

@@ -157,7 +157,8 @@ def test_tiered_decode_equals_all_gpu_sparse(lib, cuda):
     assert tier.gpu_kv_bytes() < tier.dense_kv_bytes()
 
 
-def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda):
+@pytest.mark.parametrize("batch,period", [(5, 4), (1, 2)])
+def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda, batch, period):
     """[FlexiCache] FlexiCache Scheduler and KV transfer: with stagger 1 the requests reload their
     stable heads one phase at a time.  A reloading request's promoted pages come from host on a
     low-priority stream while that request pauses, and the rest of the batch decodes.  At every
@@ -165,8 +166,8 @@ def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda):
     plan, bit for bit; that includes the requests that reloaded at the step before (their
     fetched pages are in place).  The paused requests' rows are empty heads in the step's plan."""
     from non_uniform_paged_gb300.ragged import SparseDecoder, TieredSparseDecoder, build_minmax, reload_phase_plans
-    w = synth.workload(4, batch=5, N=640, L=1)
-    P, n_pages, K, period = w.P, w.N // w.P, 8, 4
+    w = synth.workload(4, batch=batch, N=640, L=1)
+    P, n_pages, K = w.P, w.N // w.P, 8
     Kt, Vt = synth.keys_values(w, 0, cuda)
     mm = build_minmax(Kt, P)
     dense = _dense_pool(Kt, Vt, P)
@@ -176,7 +177,7 @@ def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda):
     tier.load(dense)
     tier.reload_schedule(period)
     ref = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, n_cta=32, device=cuda)
-    ws_ref = torch.zeros(max(p[1] for p in reload_phase_plans(w.batch, w.H, w.H_q, w.d, P, K, 32, period)),
+    ws_ref = torch.zeros(max(1, max(p[1] for p in reload_phase_plans(w.batch, w.H, w.H_q, w.d, P, K, 32, period))),
                          dtype=torch.uint8, device=cuda)
     fetch = torch.cuda.Stream()
     main = torch.cuda.current_stream()
@@ -201,12 +202,16 @@ def test_reload_schedule_pauses_only_the_reloading_request(lib, cuda):
         plan, plan_dev, _ = tier.phase_plans[step % period]
         out_r = torch.empty_like(out_t)
         lse_r = torch.empty_like(lse_t)
-        lib.tg_decode_attn(plan, plan_dev, 0, qb, dense, w.batch * w.H * n_pages, ref.pt_off, ref.pt_ids[0],
-                           ref.scale, ws_ref, out_r, lse=lse_r, dev_status=ref.status)
+        if plan is not None:
+            lib.tg_decode_attn(plan, plan_dev, 0, qb, dense, w.batch * w.H * n_pages, ref.pt_off, ref.pt_ids[0],
+                               ref.scale, ws_ref, out_r, lse=lse_r, dev_status=ref.status)
         torch.cuda.synchronize()
         assert lib.tg_check_status(tier.status) == 0 and lib.tg_check_status(ref.status) == 0
         expect = np.array([(step + b) % period == 0 for b in range(w.batch)])
-        assert np.array_equal(paused, expect) and expect.any() and not expect.all(), step
+        assert np.array_equal(paused, expect), step
+        if expect.all():  # every request reloads: nothing is decoded, nothing written
+            assert plan is None and out_t.float().isnan().all() and lse_t.isnan().all(), step
+            continue
         act = torch.from_numpy(~paused).to(cuda)
         assert torch.equal(out_t[act], out_r[act]) and torch.equal(lse_t[act], lse_r[act]), step
         # a paused request's rows hold no tokens in the phase's plan: out = 0, lse = -inf (an empty head)
