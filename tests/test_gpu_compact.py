@@ -121,3 +121,11 @@ def test_row_longer_than_the_clusters_shared_memory(lib, cuda):
     s = torch.round(synth.scores(w, 0, cuda) * 4) / 4
     s[0, 1] = -1.25
     _compact(lib, w, cuda, s, np.array([200000]))
+
+
+def test_more_rows_than_the_proportional_split_takes(lib, cuda):
+    """130 requests x 8 KV heads = 1040 rows: past 1024 rows the copy kernel gives each row one
+    CTA instead of proportional shares (and the select kernel runs 1040 clusters)."""
+    w = synth.small(batch=130, N=500, L=1, H=8, H_q=16, H_p=2)
+    s = torch.round(synth.scores(w, 0, cuda) * 2) / 2
+    _compact(lib, w, cuda, s, synth.contexts(w))
