@@ -62,7 +62,10 @@ struct KCfg;
 // NW streaming warps (each with an R-stage copy ring) and NE epilogue warps
 template <>
 struct KCfg<128> {
-  static constexpr int NW = 8, R = 2, NE = 4;
+  // seven streaming warps (112 KB of copies in flight per SM): the SMs' bandwidth shares
+  // spread less than with eight (worst-layer CTA skew 1.12-1.13 against 1.14-1.17 at config 2,
+  // 1.27-1.28 against 1.31-1.34 at config 3, same box), at 1.6% of back-to-back time at config 2
+  static constexpr int NW = 7, R = 2, NE = 4;
 };
 template <>
 struct KCfg<256> {
