@@ -167,7 +167,7 @@ __device__ __forceinline__ void block_radix_select(int count, int k, GetKey get,
 template <int NT, typename GetKey>
 __device__ void block_select_kth_wide(int count, int k, GetKey get, uint32_t *list, int cap, int *hist0, int *hist1,
                                       int *scratch, uint32_t &T, int &need_eq, int &n_eq) {
-  constexpr int U = 4, NWARP = NT / 32;
+  constexpr int U = 4;
   static_assert(NT % 32 == 0 && 4096 % NT == 0 && NT <= 1024, "block size");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0, mask = 0;
