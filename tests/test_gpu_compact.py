@@ -129,3 +129,18 @@ def test_more_rows_than_the_proportional_split_takes(lib, cuda):
     w = synth.small(batch=130, N=500, L=1, H=8, H_q=16, H_p=2)
     s = torch.round(synth.scores(w, 0, cuda) * 2) / 2
     _compact(lib, w, cuda, s, synth.contexts(w))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes(lib, cuda, seed):
+    """Seeded random shapes: requests, KV heads, group size, context up to 5000 (so the select
+    runs clusters of 1 to 5 CTAs, with ragged last blocks), 16-, 32- and 48-slot pages, head
+    dimensions 128 and 256 (the ones the cache plans a decode for), and scores on a grid of
+    quarters (ties across the cut)."""
+    r = np.random.default_rng(100 + seed)
+    H = int(r.choice([2, 4, 8]))
+    H_p = int(r.choice([p for p in (1, 2, 4) if H % p == 0]))
+    w = synth.small(batch=int(r.integers(1, 6)), H=H, H_q=2 * H, H_p=H_p, d=int(r.choice([128, 256])),
+                    P=int(r.choice([16, 32, 48])), N=int(r.integers(1, 5001)), L=1, seed=7 + seed)
+    s = torch.round(synth.scores(w, 0, cuda) * 4) / 4
+    _compact(lib, w, cuda, s, synth.contexts(w))
