@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) compact_copy_kernel(const Compact
 }  // namespace
 
 namespace {
-int64_t compact_ws_ints_per_row(int Nmax) { return kWsHead + 2 * (int64_t)((Nmax + kBlk - 1) / kBlk); }
+int64_t compact_ws_ints_per_row(int Nmax) { return kWsHead + 2 * (((int64_t)Nmax + kBlk - 1) / kBlk); }
 }  // namespace
 
 extern "C" int tg_compact_topk_workspace(int batch, int H, int Nmax, int64_t *workspace_bytes) {
@@ -724,6 +724,8 @@ extern "C" int tg_compact_topk(tg_stream_t stream, int batch, int H, int H_p, in
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: K, V and pool must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(workspace) & 3)
     return tgi::fail(TG_ERR_INVALID_ARG, "tg_compact_topk: workspace must be 4-byte aligned");
+  if ((int64_t)batch * H > INT32_MAX) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: batch * H too large");
+  if (Nmax > INT32_MAX - kBlk) return tgi::fail(TG_ERR_SHAPE, "tg_compact_topk: Nmax too large");
   const int rows = batch * H;
   const int64_t ws_row = compact_ws_ints_per_row(Nmax);
   if (workspace_bytes < (int64_t)rows * ws_row * (int64_t)sizeof(int32_t))

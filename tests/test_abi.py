@@ -81,6 +81,15 @@ def test_compact_topk_workspace_size_and_short_workspace_refused(lib):
     assert rc == -1  # TG_ERR_INVALID_ARG: no workspace
     with pytest.raises(lib.TGError):
         lib.tg_compact_topk_workspace(batch, H, 0)
+    # sizes whose products leave int32 are refused as shapes (TG_ERR_SHAPE), also before any launch
+    big = lib.tg_compact_topk_workspace(1, 1, 2**31 - 1)
+    assert big == (4 + 2 * 2**21) * 4
+    rc = so.tg_compact_topk(None, 2**16, 2**15, 2, 16, 128, Nmax, fake, fake, fake, fake, fake, fake, fake, fake,
+                            1, fake, None, fake, 2**62, None)
+    assert rc == -2 and b"batch * H" in so.tg_last_error_string()
+    rc = so.tg_compact_topk(None, 1, 2, 2, 16, 128, 2**31 - 1, fake, fake, fake, fake, fake, fake, fake, fake,
+                            1, fake, None, fake, 2**62, None)
+    assert rc == -2 and b"Nmax" in so.tg_last_error_string()
 
 
 def test_tier_promote_background_checks_arguments_on_the_host(lib):
