@@ -222,7 +222,10 @@ int tg_plan_set_flags(void *plan_host, uint32_t flags);
  *   by a decode launch); it waits before it touches the workspace, out or lse.
  *   Other kernels complete before it starts, unless they let it start early
  *   (tg_page_score_topk with TG_SCORE_LET_NEXT_START): the plan must then carry
- *   TG_PLAN_WAIT_TABLES, and the launch waits before it reads q and the tables. */
+ *   TG_PLAN_WAIT_TABLES, and the launch waits before it reads q and the tables.
+ *   Such a launch lets the next kernel start only after that wait, when the
+ *   kernel that wrote the tables is complete: a page-score call that follows
+ *   it on the same score workspace cannot overlap the one before it. */
 int tg_decode_attn(tg_stream_t stream, const void *plan_host, const void *plan_dev, int layer,
                    const uint16_t *q, const uint16_t *pool, int64_t pool_pages,
                    const int64_t *pt_off, const int32_t *pt_ids, float scale,
@@ -336,9 +339,11 @@ int tg_build_minmax(tg_stream_t stream, int batch, int H, int N, int P, int d,
  *   workspace; it waits for that kernel before writing sel and pt_ids.
  *   flags: 0, or TG_SCORE_LET_NEXT_START to let the next kernel in the stream
  *   start before sel and pt_ids are complete; that kernel must then wait for
- *   this one before reading them (tg_decode_attn with a plan flagged
- *   TG_PLAN_WAIT_TABLES does).  Without the flag the next kernel starts only
- *   when sel and pt_ids are complete. */
+ *   this one before reading them, and let no later kernel start before that
+ *   wait, since the next call on the same workspace writes it as soon as it
+ *   starts (tg_decode_attn with a plan flagged TG_PLAN_WAIT_TABLES does both).
+ *   Without the flag the next kernel starts only when sel and pt_ids are
+ *   complete. */
 #define TG_SCORE_LET_NEXT_START 0x1u
 int tg_page_score_topk(tg_stream_t stream, int batch, int H, int g, int d, int n_pages, int K,
                        const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,

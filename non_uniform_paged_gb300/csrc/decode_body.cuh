@@ -162,8 +162,11 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
   if (tid == 0) *s_t0 = globaltimer_ns();
 
   // the next kernel in the stream may start as this grid's CTAs finish (programmatic
-  // dependent launch); it waits for this grid before touching shared workspace or outputs
-  griddep_launch_dependents();
+  // dependent launch); it waits for this grid before touching shared workspace or outputs.
+  // A grid that waits for the page lists (wait_tables) lets it start only after that wait:
+  // the kernel that writes the lists (a page-score call) is then complete, so a next
+  // page-score call that starts early cannot write the score workspace under its feet
+  if (!a.wait_tables) griddep_launch_dependents();
 
   // ---------------- this CTA's work items and their page-table bases, one parallel round trip.
   // Page tables and q are read from L2 (ld.global.cg): the kernel before this one in the
@@ -181,7 +184,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap *pool_map_p, const
   }
   // page tables written by the kernel just before this one (which let this grid start
   // early): wait for it first
-  if (a.wait_tables) griddep_wait();
+  if (a.wait_tables) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   // page lists written by other CTAs of this same grid (fused sparse layer): wait for the
   // rows of this CTA's items
   if (a.row_ready)
