@@ -400,7 +400,10 @@ int tg_rerank_rows(int L, int batch, int H, const uint8_t *unstable, int layer, 
  *   as the decode's page lists over pool (the dense cache [batch][H][n_pages] of
  *   H_p = 1 pages).  epoch >= 1 and above every earlier call's on the same score
  *   workspace (e.g. a call counter).  workspace, out, lse, dev_status as
- *   tg_decode_attn.  Launched without programmatic dependent launch. */
+ *   tg_decode_attn.  Launched without programmatic dependent launch.
+ *   CUDA graphs: a captured call replays the epoch it was captured with, so
+ *   zero score_ws ahead of it in the same graph (a captured memset) or replay
+ *   two graphs captured with different epochs in turn. */
 int tg_sparse_layer(tg_stream_t stream, const void *plan_host, const void *plan_dev, int n_pages, int K,
                     int n_rows, const int32_t *rows, const uint8_t *due, int64_t wait_limit_ns,
                     const uint16_t *q, const uint16_t *minmax, int32_t *sel, int32_t *pt_ids,

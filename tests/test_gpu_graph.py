@@ -128,3 +128,41 @@ def test_sparse_steps_replayed_from_a_graph(lib, cuda, overlap):
         mm_h = mm.float().cpu().numpy()
         ref = ofx.select_pages(q.float().cpu().numpy(), mm_h[:, :, :, 0], mm_h[:, :, :, 1], K)
         assert np.array_equal(dec.sel[l].view(w.batch, w.H, K).cpu().numpy(), ref), l
+
+
+def test_fused_sparse_layer_replayed_with_its_score_workspace_zeroed(lib, cuda):
+    """tg_sparse_layer waits for row flags equal to the call's epoch, and a captured call
+    replays the epoch it was captured with.  With the score workspace zeroed ahead of the call
+    in the same graph, every replay waits for its own selections: with a new q copied in before
+    each replay, the outputs and page lists equal the separate kernels' bit for bit."""
+    from non_uniform_paged_gb300.ragged import SparseDecoder, build_minmax
+    w = synth.workload(4, batch=3, N=400, L=1)
+    P, K = w.P, 10
+    n_pages = w.N // P
+    Kt, Vt = synth.keys_values(w, 0, cuda)
+    pool = torch.stack([Kt.view(w.batch, w.H, n_pages, P, w.d), Vt.view(w.batch, w.H, n_pages, P, w.d)],
+                       dim=3).contiguous()
+    mm = build_minmax(Kt, P)
+    fused = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, device=cuda)
+    sep = SparseDecoder(w.batch, w.H, w.H_q, w.d, P, n_pages, K, device=cuda)
+    gen = torch.Generator(device=cuda)
+    gen.manual_seed(5)
+    qs = [torch.randn((w.batch, w.H_q, w.d), generator=gen, device=cuda).to(torch.bfloat16) for _ in range(4)]
+    qbuf = qs[0].clone()
+    out = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+    out_ref, lse_ref = torch.empty_like(out), torch.empty_like(lse)
+
+    def fused_step():
+        fused.score_ws.zero_()
+        fused.step_fused(qbuf, mm, pool, out, lse)
+
+    g = _capture(fused_step)
+    for t in range(len(qs)):
+        qbuf.copy_(qs[t])
+        g.replay()
+        sep.step(qs[t], mm, pool, out_ref, lse_ref)
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(fused.status) == 0 and lib.tg_check_status(sep.status) == 0
+        assert torch.equal(fused.sel, sep.sel) and torch.equal(fused.pt_ids, sep.pt_ids), t
+        assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref), t

@@ -81,3 +81,45 @@ def test_static_scratch_rejects_plans_larger_than_the_array(lib, cuda):
                                           cache.list_offsets(0), cache.pt_ids_dev, cache.scale, out,
                                           dev_status=status)
     assert "scratch" in str(e.value)
+
+
+def test_static_scratch_replayed_from_a_cuda_graph(lib, cuda):
+    # each call clears the array's counters with a memset on the caller's stream, so after a
+    # first eager call (which loads the module and its array) the calls can be captured; the
+    # replays give tg_decode_attn's bits
+    w, cache = _setup(lib, cuda, n_cta=40)
+    qs = [synth.queries(w, layer, cuda) for layer in range(w.L)]
+    refs = []
+    for layer in range(w.L):
+        ref = torch.empty((w.batch, w.H_q, w.d), dtype=torch.bfloat16, device=cuda)
+        ref_lse = torch.empty((w.batch, w.H_q), dtype=torch.float32, device=cuda)
+        cache.decode_layer(layer, qs[layer], ref, ref_lse)
+        refs.append((ref, ref_lse))
+    outs = [torch.empty_like(r) for r, _ in refs]
+    lses = [torch.empty_like(x) for _, x in refs]
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+
+    def step():
+        for layer in range(w.L):
+            lib.tg_decode_attn_static_scratch(cache.plan, cache.plan_dev, layer, qs[layer], cache.pool,
+                                              cache.n_pages, cache.list_offsets(layer), cache.pt_ids_dev,
+                                              cache.scale, outs[layer], lse=lses[layer], dev_status=status)
+
+    step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step()
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for o, x in zip(outs, lses):
+            o.fill_(float("nan"))
+            x.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert lib.tg_check_status(status) == 0
+        for layer in range(w.L):
+            assert torch.equal(outs[layer], refs[layer][0]), (rep, layer)
+            assert torch.equal(lses[layer], refs[layer][1]), (rep, layer)
