@@ -964,13 +964,19 @@ def report_pages(args):
 
 
 def release_device_memory():
-    """Free what earlier sections left behind before a new one is timed.  Closures of a finished
-    section (a step function whose default argument is its cache) can keep a few hundred GB
-    alive until the next garbage collection.  Timed beside that memory, the first H_p point
-    of the sweep ran 17% slower (30.6 against 25.7 ms per step) than when run alone."""
+    """Free what earlier sections left behind, then let the device settle before a new section
+    is timed.  Closures of a finished section (a step function whose default argument is its
+    cache) keep its memory until the next garbage collection.  And for some seconds after a
+    large free the device reads slower: the first H_p sweep point, timed right after the 221 GB
+    headline cache was freed, ran at 27.8-30.6 ms per step; 15 s later, or in a fresh process,
+    at 25.6-25.7 ms.  So after a free of more than 8 GB this waits 1 s per 15 GB (at most 15 s)."""
     import gc
     gc.collect()
+    before = torch.cuda.memory_reserved()
     torch.cuda.empty_cache()
+    freed = before - torch.cuda.memory_reserved()
+    if freed > 8e9:
+        time.sleep(min(15.0, freed / 15e9))
 
 
 def hp_sweep(args, w, device, layers):
