@@ -49,3 +49,24 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.0, 1, None) == 3.0
     assert bench.sum_over_ranks(3.0, 1, None) == 3.0
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """bench.py --impl reference launched as the driver launches N > 1 (torchrun, two gloo ranks on
+    CPU): rank 0 alone times the oracle and prints one JSON line; the other rank exits 0.  The
+    small config-1 workload keeps the oracle's inputs quick to draw on the CPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           "bench.py", "--impl", "reference", "--config", "1", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = lines[0]
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
