@@ -24,6 +24,13 @@
  *    see (a page id past the pool, a NaN score, a wait that gave up) set bits
  *    of the caller's int32 device status word (TG_STATUS_*), which
  *    tg_check_status() reads back.  No kernel traps.
+ *  - GPU entry points only enqueue work on the caller's stream: no host
+ *    synchronisation, no allocation.  They may be captured in a CUDA graph and
+ *    replayed (bit-identical to eager calls); tg_sparse_layer's epoch needs the
+ *    care its entry states.  tg_check_status() synchronises and is not captured.
+ *    Independent callers on concurrent streams need their own workspaces and
+ *    status words; the library keeps no other state between calls (except the
+ *    fixed array of tg_decode_attn_static_scratch).
  *  - Tensors are dense row-major.  bf16 values travel as uint16_t bit patterns.
  *
  * Notation: L layers, batch requests, H KV heads, H_q query heads, g = H_q/H
