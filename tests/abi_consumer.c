@@ -5,6 +5,7 @@
  * CUDA device, with memory from the CUDA runtime.
  *
  *   abi_consumer DIR [gpu]
+ *   abi_consumer DIR sparse
  *
  * DIR holds the inputs as raw little-endian arrays and receives the outputs:
  *   dims        text: batch H H_q H_p P d Nmax N_CTA alpha cluster scale
@@ -18,6 +19,12 @@
  *   t0, t1, part, nparts) in plan order
  * gpu outputs: kept.i32 [batch][H][Nmax], out.u16 [batch][H_q][d], lse.f32 [batch][H_q],
  *   status.i32 [1]
+ * "sparse" runs the page-selection path instead, over a dense cache of H_p = 1 pages:
+ *   sdims       text: batch H H_q d N P K N_CTA scale   (N % P == 0)
+ *   K.u16 V.u16 [batch][H][N][d] bf16;  q.u16 [batch][H_q][d] bf16
+ * It builds the MinMax cache (tg_build_minmax), selects each KV head's top K pages
+ * (tg_page_score_topk) and decodes over them (tg_decode_attn with a plan of K pages per
+ * head); outputs sel.i32 [batch][H][K], out.u16, lse.f32, status.i32.
  * Exit status 0 on success; otherwise the failing call and tg_last_error_string(). */
 #include <stdint.h>
 #include <stdio.h>
@@ -75,6 +82,104 @@ static void *to_device(const void *host, size_t bytes) {
   return d;
 }
 
+/* The page-selection path of one layer (see the header comment). */
+static int run_sparse(void) {
+  int batch, H, H_q, d, N, P, K, N_CTA, b, h, p, n_pages;
+  float scale;
+  FILE *f = fopen(path("sdims"), "r");
+  if (!f) die("open", "sdims");
+  if (fscanf(f, "%d %d %d %d %d %d %d %d %f", &batch, &H, &H_q, &d, &N, &P, &K, &N_CTA, &scale) != 9)
+    die("parse", "sdims");
+  fclose(f);
+  if (batch <= 0 || H <= 0 || H_q % H || P <= 0 || N % P || K <= 0 || K > N / P) die("sdims", "sizes out of range");
+  n_pages = N / P;
+  {
+    const size_t n_kv = (size_t)batch * H * N * d, n_q = (size_t)batch * H_q * d, rows = (size_t)batch * H;
+    const size_t page_elems = (size_t)2 * P * d;  /* one H_p = 1 page: K rows then V rows */
+    const int64_t pool_pages = (int64_t)rows * n_pages;
+    uint16_t *Kh = (uint16_t *)read_file("K.u16", sizeof(uint16_t) * n_kv);
+    uint16_t *Vh = (uint16_t *)read_file("V.u16", sizeof(uint16_t) * n_kv);
+    uint16_t *qh = (uint16_t *)read_file("q.u16", sizeof(uint16_t) * n_q);
+    uint16_t *pool = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)pool_pages * page_elems);
+    int32_t *ntok = (int32_t *)malloc(sizeof(int32_t) * rows), *order = (int32_t *)malloc(sizeof(int32_t) * H);
+    int64_t *Phi = (int64_t *)calloc((size_t)H, sizeof(int64_t)), *pt_off = (int64_t *)malloc(sizeof(int64_t) * (rows + 1));
+    int32_t *S = (int32_t *)malloc(sizeof(int32_t) * H), *sel = (int32_t *)malloc(sizeof(int32_t) * rows * K);
+    uint16_t *out = (uint16_t *)malloc(sizeof(uint16_t) * n_q);
+    float *lse = (float *)malloc(sizeof(float) * (size_t)batch * H_q);
+    int64_t plan_bytes = 0, work_bytes = 0, ws_bytes = 0;
+    int32_t status = 0;
+    uint8_t *plan;
+    void *d_K, *d_q, *d_pool, *d_off, *d_plan, *d_mm = NULL, *d_ws = NULL, *d_sel = NULL, *d_ids = NULL;
+    void *d_work = NULL, *d_out = NULL, *d_lse = NULL, *d_status = NULL;
+    if (!pool || !ntok || !order || !Phi || !pt_off || !S || !sel || !out || !lse) die("malloc", "sparse arrays");
+    /* the dense cache [batch][H][n_pages][2][P][d] from K and V [batch][H][N][d] */
+    for (b = 0; b < batch; ++b)
+      for (h = 0; h < H; ++h)
+        for (p = 0; p < n_pages; ++p) {
+          const size_t row = (size_t)b * H + h, src = (row * N + (size_t)p * P) * d;
+          uint16_t *dst = pool + (row * n_pages + p) * page_elems;
+          memcpy(dst, Kh + src, sizeof(uint16_t) * P * d);
+          memcpy(dst + (size_t)P * d, Vh + src, sizeof(uint16_t) * P * d);
+        }
+    /* host plan: every KV head attends K whole pages; H_p = 1, so group g is head g */
+    for (h = 0; h < H; ++h) order[h] = h;
+    for (b = 0; b < batch; ++b)
+      for (h = 0; h < H; ++h) {
+        ntok[b * H + h] = K * P;
+        Phi[h] += K * P;
+      }
+    TG(tg_split_map(1, H, N_CTA, Phi, S));
+    TG(tg_plan_decode(1, batch, H, H_q, 1, P, d, N_CTA, S, order, ntok, NULL, 0, &plan_bytes, &work_bytes));
+    plan = (uint8_t *)malloc((size_t)plan_bytes);
+    if (!plan) die("malloc", "plan");
+    TG(tg_plan_decode(1, batch, H, H_q, 1, P, d, N_CTA, S, order, ntok, plan, plan_bytes, &plan_bytes, &work_bytes));
+    /* list b*H + h (G = H groups of one head) holds that head's K selected pages */
+    for (b = 0; b <= (int)rows; ++b) pt_off[b] = (int64_t)b * K;
+
+    /* device: MinMax cache, page scores and top-K (page ids into the dense pool), decode */
+    d_K = to_device(Kh, sizeof(uint16_t) * n_kv);
+    d_q = to_device(qh, sizeof(uint16_t) * n_q);
+    d_pool = to_device(pool, sizeof(uint16_t) * (size_t)pool_pages * page_elems);
+    d_off = to_device(pt_off, sizeof(int64_t) * (rows + 1));
+    d_plan = to_device(plan, (size_t)plan_bytes);
+    CU(cudaMalloc(&d_mm, sizeof(uint16_t) * rows * n_pages * 2 * d));
+    TG(tg_page_score_workspace(batch, H, n_pages, &ws_bytes));
+    CU(cudaMalloc(&d_ws, (size_t)ws_bytes));
+    CU(cudaMemset(d_ws, 0, (size_t)ws_bytes));
+    CU(cudaMalloc(&d_sel, sizeof(int32_t) * rows * K));
+    CU(cudaMalloc(&d_ids, sizeof(int32_t) * rows * K));
+    CU(cudaMalloc(&d_work, (size_t)(work_bytes ? work_bytes : 16)));
+    CU(cudaMemset(d_work, 0, (size_t)(work_bytes ? work_bytes : 16)));
+    CU(cudaMalloc(&d_out, sizeof(uint16_t) * n_q));
+    CU(cudaMalloc(&d_lse, sizeof(float) * (size_t)batch * H_q));
+    CU(cudaMalloc(&d_status, sizeof(int32_t)));
+    CU(cudaMemset(d_status, 0, sizeof(int32_t)));
+    TG(tg_build_minmax(NULL, batch, H, N, P, d, (const uint16_t *)d_K, (uint16_t *)d_mm, (int32_t *)d_status));
+    TG(tg_page_score_topk(NULL, batch, H, H_q / H, d, n_pages, K, (const uint16_t *)d_q, (const uint16_t *)d_mm,
+                          (int32_t *)d_sel, (int32_t *)d_ids, d_ws, ws_bytes, 0, (int32_t *)d_status));
+    TG(tg_decode_attn(NULL, plan, d_plan, 0, (const uint16_t *)d_q, (const uint16_t *)d_pool, pool_pages,
+                      (const int64_t *)d_off, (const int32_t *)d_ids, scale, d_work, work_bytes, (uint16_t *)d_out,
+                      (float *)d_lse, (int32_t *)d_status, NULL));
+    CU(cudaDeviceSynchronize());
+    if (tg_check_status((const int32_t *)d_status, &status) != TG_OK && status == 0)
+      die("tg_check_status", tg_last_error_string());
+    CU(cudaMemcpy(sel, d_sel, sizeof(int32_t) * rows * K, cudaMemcpyDeviceToHost));
+    CU(cudaMemcpy(out, d_out, sizeof(uint16_t) * n_q, cudaMemcpyDeviceToHost));
+    CU(cudaMemcpy(lse, d_lse, sizeof(float) * (size_t)batch * H_q, cudaMemcpyDeviceToHost));
+    write_file("sel.i32", sel, sizeof(int32_t) * rows * K);
+    write_file("out.u16", out, sizeof(uint16_t) * n_q);
+    write_file("lse.f32", lse, sizeof(float) * (size_t)batch * H_q);
+    write_file("status.i32", &status, sizeof status);
+
+    cudaFree(d_K); cudaFree(d_q); cudaFree(d_pool); cudaFree(d_off); cudaFree(d_plan); cudaFree(d_mm);
+    cudaFree(d_ws); cudaFree(d_sel); cudaFree(d_ids); cudaFree(d_work); cudaFree(d_out); cudaFree(d_lse);
+    cudaFree(d_status);
+    free(Kh); free(Vh); free(qh); free(pool); free(ntok); free(order); free(Phi); free(pt_off); free(S);
+    free(sel); free(out); free(lse); free(plan);
+    return 0;
+  }
+}
+
 int main(int argc, char **argv) {
   int batch, H, H_q, H_p, P, d, Nmax, N_CTA, cluster;
   float alpha, scale;
@@ -90,8 +195,9 @@ int main(int argc, char **argv) {
   const int32_t *cta_off;
   const tg_work_item *items;
 
-  if (argc < 2) die("usage", "abi_consumer DIR [gpu]");
+  if (argc < 2) die("usage", "abi_consumer DIR [gpu | sparse]");
   snprintf(g_dir, sizeof g_dir, "%s", argv[1]);
+  if (argc > 2 && strcmp(argv[2], "sparse") == 0) return run_sparse();
   f = fopen(path("dims"), "r");
   if (!f) die("open", "dims");
   if (fscanf(f, "%d %d %d %d %d %d %d %d %f %d %f", &batch, &H, &H_q, &H_p, &P, &d, &Nmax, &N_CTA, &alpha,

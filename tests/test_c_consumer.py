@@ -139,3 +139,50 @@ def test_c_consumer_compacts_and_decodes_on_the_gpu(consumer, tmp_path, case):
     diff = np.abs(out - out_ref)
     assert diff.max() <= OUT_MAX_ABS and diff.mean() <= OUT_MEAN_ABS, (diff.max(), diff.mean())
     assert np.abs(lse[fin] - lse_ref[fin]).max() <= LSE_MAX_ABS
+
+
+@pytest.mark.gpu
+def test_c_consumer_selects_pages_and_decodes_on_the_gpu(consumer, tmp_path):
+    """The page-selection path from C: MinMax cache, Quest page scores and top-K pages
+    (bit-exact page lists), then decode attention over the selected pages (tolerance)."""
+    import torch
+    from gpu_helpers import OUT_MAX_ABS, OUT_MEAN_ABS, LSE_MAX_ABS
+    from oracle import flexicache as ofx
+
+    w = synth.workload(4, batch=3, N=400, L=1)
+    K_sel, N_CTA = 10, 40
+    P, n_pages = w.P, w.N // w.P
+    d = str(tmp_path)
+    scale = 1.0 / math.sqrt(w.d)
+    with open(os.path.join(d, "sdims"), "w") as f:
+        f.write(f"{w.batch} {w.H} {w.H_q} {w.d} {w.N} {P} {K_sel} {N_CTA} {scale!r}\n")
+    Kt, Vt = synth.keys_values(w, 0, "cpu")
+    q = synth.queries(w, 0, "cpu")
+    for name, t in (("K.u16", Kt), ("V.u16", Vt), ("q.u16", q)):
+        t.contiguous().view(torch.int16).numpy().tofile(os.path.join(d, name))
+    r = subprocess.run([consumer, d, "sparse"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert _read(d, "status.i32", np.int32)[0] == 0
+
+    K_h, V_h, q_h = Kt.float().numpy(), Vt.float().numpy(), q.float().numpy()
+    mn = np.zeros((w.batch, w.H, n_pages, w.d), np.float32)
+    mx = np.zeros_like(mn)
+    for b in range(w.batch):
+        for h in range(w.H):
+            mn[b, h], mx[b, h] = ofx.page_minmax(K_h[b, h], P)
+    sel_ref = ofx.select_pages(q_h, mn, mx, K_sel)
+    assert np.array_equal(_read(d, "sel.i32", np.int32, (w.batch, w.H, K_sel)), sel_ref)
+
+    bits = _read(d, "out.u16", np.uint16, (w.batch, w.H_q, w.d)).astype(np.uint32) << 16
+    out = bits.view(np.float32).astype(np.float64)
+    lse = _read(d, "lse.f32", np.float32, (w.batch, w.H_q)).astype(np.float64)
+    ref_out = np.zeros((w.batch, w.H_q, w.d))
+    ref_lse = np.zeros((w.batch, w.H_q))
+    for b in range(w.batch):
+        for j in range(w.H_q):
+            h = j // w.g
+            tok = ofx.page_tokens(sel_ref[b, h], P, w.N)
+            ref_out[b, j], ref_lse[b, j] = otg.attention(q_h[b, j], K_h[b, h][tok], V_h[b, h][tok], scale)
+    diff = np.abs(out - ref_out)
+    assert diff.max() <= OUT_MAX_ABS and diff.mean() <= OUT_MEAN_ABS, (diff.max(), diff.mean())
+    assert np.abs(lse - ref_lse).max() <= LSE_MAX_ABS
