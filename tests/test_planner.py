@@ -221,3 +221,42 @@ def test_reload_phase_plans_pause_only_the_reloading_requests(lib, batch, period
             covered[it["b"], it["h"]] += it["t1"] - it["t0"]
         want = np.where(paused[:, None], 0, K * P)
         assert np.array_equal(covered, np.broadcast_to(want, (batch, H))), p
+
+
+def test_pages_split_and_plan_random_shapes(lib):
+    """Seeded random shapes: page tables, split map and per-CTA plan equal the oracle bit for bit.
+    Budgets are drawn from a small set of values so that equal budgets (the clustering order's
+    tie-break), tiny budgets and B = 1 all occur; contexts include empty requests."""
+    r = np.random.default_rng(2024)
+    levels = np.array([1e-30, 0.05, 0.2, 0.2, 0.5, 0.75, 1.0], np.float32)
+    for case in range(60):
+        H = int(r.choice([2, 4, 6, 8, 12, 16]))
+        H_p = int(r.choice([x for x in (1, 2, 3, 4, 8) if H % x == 0]))
+        G = H // H_p
+        L, batch = int(r.integers(1, 4)), int(r.integers(1, 7))
+        P = int(r.choice([16, 32, 48, 64]))
+        d = int(r.choice([128, 256]))
+        g = int(r.choice([1, 2, 4]))
+        alpha = float(np.float32(r.uniform(0.5, 3.0)))
+        cluster = bool(r.integers(0, 2))
+        Bhat = r.choice(levels, size=(L, H)).astype(np.float32)
+        N = r.integers(0, 3000, size=batch).astype(np.int32)
+        N[r.random(batch) < 0.15] = 0
+        N_CTA = int(r.integers(G, 300))
+        got = lib.tg_build_pages(L, batch, H, H_p, P, alpha, Bhat, N, cluster)
+        ref = otg.build_pages(L, batch, H, H_p, P, alpha, Bhat, N, cluster)
+        for k in ("order", "ntok", "pt_off", "pt_ids", "Phi"):
+            assert np.array_equal(got[k], ref[k]), (case, k)
+        assert got["n_pages"] == ref["n_pages"] and got["n_pages_monolithic"] == ref["n_pages_monolithic"], case
+        S = lib.tg_split_map(got["Phi"], N_CTA)
+        for l in range(L):
+            assert S[l].tolist() == otg.split_map_row(ref["Phi"][l], N_CTA), (case, l)
+        plan, _ = lib.tg_plan_decode(S, got["order"], got["ntok"], H * g, H_p, P, d)
+        for l in range(L):
+            want = otg.work_list(S[l], ref["ntok"][l], ref["order"][l], H_p)
+            off, items = lib.plan_items(plan, l)
+            for c in range(N_CTA):
+                have = [[int(it["b"]), int(it["h"]), int(it["hpos"]), int(it["b"]) * G + int(it["g"]),
+                         int(it["t0"]), int(it["t1"]), int(it["nparts"]), int(it["part"])]
+                        for it in items[off[c]:off[c + 1]]]
+                assert have == want[c], (case, l, c)
